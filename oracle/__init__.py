@@ -1,0 +1,120 @@
+"""fp64 CPU oracle for the exact attention forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference arm may import or run anything under
+``oracle/``.  The product path (``exact_attention_forward_08_gb300``) never
+does, and the two share no code: the only common module is ``synthetic``,
+which draws seeded inputs and holds none of the method's arithmetic.
+
+``attn_fwd`` is the plain definition O = softmax(scale * Q K^T) V with the
+per-row log-sum-exp, written out row by row in double precision in
+``attn_oracle.c`` (see that file for the citations).  ``online`` restates the
+pages' online-softmax algebra (block state, two-block merge, conditional
+rescaling) in fp64 for the pins in ``tests/``.
+
+Parity status: pinned (worked example, closed forms, invariants, brute force
+and a library routine; see ``tests/test_oracle_pins.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+from . import online  # noqa: F401  (re-exported)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc into ``oracle/_build/liboracle.so``."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load_library(path: str):
+    """Load a compiled oracle library (the default one, or a test's copy)."""
+    lib = ctypes.CDLL(path)
+    i64 = ctypes.c_int64
+    lib.oracle_attn_fwd.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                    i64, i64, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double,
+                                    ctypes.c_void_p, i64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_attn_fwd.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, rows=None, threads: int | None = None,
+             lib=None):
+    """Reference attention forward.
+
+    q [B,Sq,Hq,dqk], k [B,Sk,Hkv,dqk], v [B,Sk,Hkv,dv]: either float64 arrays or
+    ``uint16`` arrays of bf16 bit patterns (decoded exactly).  ``scale`` defaults
+    to 1/sqrt(dqk).
+
+    rows=None: returns (O [B,Sq,Hq,dv], LSE [B,Hq,Sq]) as float64.
+    rows = int64 array of linear row ids r = (b*Sq + i)*Hq + h: returns
+    (O [n, dv], LSE [n]) for those rows only.
+    ``lib`` selects another compiled copy of the oracle (used by the tests).
+    """
+    arrs = [np.ascontiguousarray(x) for x in (q, k, v)]
+    kinds = {a.dtype for a in arrs}
+    if kinds == {np.dtype(np.uint16)}:
+        elem = 1
+    elif kinds == {np.dtype(np.float64)}:
+        elem = 0
+    else:
+        raise TypeError(f"q, k, v must all be uint16 (bf16 bits) or all float64, got {kinds}")
+    q, k, v = arrs
+    B, Sq, Hq, dqk = q.shape
+    Bk, Sk, Hkv, dqk2 = k.shape
+    Bv, Skv, Hkv2, dv = v.shape
+    if not (B == Bk == Bv and dqk == dqk2 and Sk == Skv and Hkv == Hkv2):
+        raise ValueError(f"inconsistent shapes q{q.shape} k{k.shape} v{v.shape}")
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dqk)
+    full = rows is None
+    if full:
+        n = B * Sq * Hq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n = rows_arr.size
+    o = np.empty((n, dv), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    rc = (lib or _load()).oracle_attn_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, elem, B, Hq, Hkv, Sq, Sk,
+                                 dqk, dv, int(bool(causal)), float(scale),
+                                 None if full else rows_arr.ctypes.data, n, o.ctypes.data, lse.ctypes.data,
+                                 threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_fwd failed with status {rc}")
+    if full:
+        return o.reshape(B, Sq, Hq, dv), lse.reshape(B, Sq, Hq).transpose(0, 2, 1).copy()
+    return o, lse
+
+
+def row_ids(b, i, h, Sq: int, Hq: int) -> np.ndarray:
+    """Linear row ids r = (b*Sq + i)*Hq + h."""
+    return (np.asarray(b, dtype=np.int64) * Sq + np.asarray(i, dtype=np.int64)) * Hq + np.asarray(h, dtype=np.int64)
