@@ -1,0 +1,199 @@
+"""Exact attention forward for GB300 (sm_103a): Python binding of the C ABI.
+
+The binding only marshals arguments to ``libfa_gb300.so`` (``include/fa.h``);
+every step of the computation runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams only.  There is no CPU fallback: if the
+library is missing or a call fails, an exception is raised.
+
+    from exact_attention_forward_08_gb300 import attention_forward
+    o, lse = attention_forward(q, k, v, causal=True)   # q [B,Sq,Hq,d] bf16 on cuda
+
+Raw entry points with the C names: ``fa_fwd``, ``fa_fwd_ex``,
+``fa_device_status``, ``fa_status_string``, ``fa_make_plan``,
+``fa_plan_task``, ``fa_plan_block_masked``, ``fa_version``.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+__all__ = ["fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_status_string", "fa_make_plan", "fa_plan_task",
+           "fa_plan_block_masked", "fa_version", "FaOptions", "FaPlan", "FaTask", "attention_forward",
+           "FaError", "load_library", "LIB_PATH", "STATUS"]
+
+LIB_PATH = _build.LIB
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+          4: "FA_ERR_DEVICE_TIMEOUT"}
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(5)
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)}" if what else STATUS.get(code, str(code)))
+
+
+class FaOptions(ctypes.Structure):
+    _fields_ = [("tau", ctypes.c_float), ("pack", ctypes.c_int), ("grid", ctypes.c_int),
+                ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int)]
+
+
+class FaPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("batch", "heads_q", "heads_kv", "seqlen_q", "seqlen_k", "causal",
+                                            "pack", "groups", "pos_per_tile", "tiles", "mblocks", "kv_blocks",
+                                            "ratio", "section_units")] + [("num_tasks", ctypes.c_int64)]
+
+
+class FaTask(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int), ("g", ctypes.c_int), ("mblock", ctypes.c_int), ("kv_head", ctypes.c_int),
+                ("pos0", ctypes.c_int * 2), ("n_blocks", ctypes.c_int * 2)]
+
+
+_lib = None
+
+_I = ctypes.c_int
+_P = ctypes.c_void_p
+_FWD_ARGS = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float]
+
+
+def load_library(path: str | None = None):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FaError(FA_ERR_CUDA, f"CUDA library not built ({p}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    lib.fa_fwd.argtypes = _FWD_ARGS + [_P]
+    lib.fa_fwd.restype = _I
+    lib.fa_fwd_ex.argtypes = _FWD_ARGS + [ctypes.POINTER(FaOptions), _P]
+    lib.fa_fwd_ex.restype = _I
+    lib.fa_options_default.argtypes = [ctypes.POINTER(FaOptions)]
+    lib.fa_options_default.restype = None
+    lib.fa_device_status.argtypes = [_P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_device_status.restype = _I
+    lib.fa_status_string.argtypes = [_I]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = _I
+    lib.fa_make_plan.argtypes = [_I] * 8 + [ctypes.c_int64, _I, ctypes.POINTER(FaPlan)]
+    lib.fa_make_plan.restype = _I
+    lib.fa_plan_task.argtypes = [ctypes.POINTER(FaPlan), ctypes.c_int64, ctypes.POINTER(FaTask)]
+    lib.fa_plan_task.restype = _I
+    lib.fa_plan_block_masked.argtypes = [ctypes.POINTER(FaPlan), _I, _I]
+    lib.fa_plan_block_masked.restype = _I
+    if path is None:
+        _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# raw C entry points (pointers and sizes)
+# ---------------------------------------------------------------------------
+
+def fa_fwd(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale, stream) -> int:
+    """``fa_fwd`` of include/fa.h; pointer arguments are integers (device addresses)."""
+    return load_library().fa_fwd(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v,
+                                 int(causal), float(scale), stream)
+
+
+def default_options() -> FaOptions:
+    o = FaOptions()
+    load_library().fa_options_default(ctypes.byref(o))
+    return o
+
+
+def fa_fwd_ex(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale, opts,
+              stream) -> int:
+    """``fa_fwd_ex``: ``opts`` is an ``FaOptions`` or None."""
+    return load_library().fa_fwd_ex(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v,
+                                    int(causal), float(scale), ctypes.byref(opts) if opts is not None else None,
+                                    stream)
+
+
+def fa_device_status(stream=None):
+    """Synchronise ``stream`` and read/clear the device status: (code, (code, site, block))."""
+    out = _I(0)
+    detail = (ctypes.c_uint * 3)()
+    rc = load_library().fa_device_status(stream, ctypes.byref(out), detail)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_device_status")
+    return out.value, tuple(detail)
+
+
+def fa_status_string(code: int) -> str:
+    return load_library().fa_status_string(code).decode()
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+def fa_make_plan(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, l2_bytes=0, pack=0) -> FaPlan:
+    plan = FaPlan()
+    rc = load_library().fa_make_plan(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, int(causal), l2_bytes,
+                                     pack, ctypes.byref(plan))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_make_plan")
+    return plan
+
+
+def fa_plan_task(plan: FaPlan, task: int) -> FaTask:
+    t = FaTask()
+    rc = load_library().fa_plan_task(ctypes.byref(plan), task, ctypes.byref(t))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_plan_task")
+    return t
+
+
+def fa_plan_block_masked(plan: FaPlan, pos0: int, j: int) -> bool:
+    return bool(load_library().fa_plan_block_masked(ctypes.byref(plan), pos0, j))
+
+
+# ---------------------------------------------------------------------------
+# torch convenience wrapper (allocation and argument marshalling only)
+# ---------------------------------------------------------------------------
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                      return_lse: bool = True, stream=None, options: FaOptions | None = None):
+    """O (and LSE) for bf16 CUDA tensors q [B,Sq,Hq,dqk], k [B,Sk,Hkv,dqk], v [B,Sk,Hkv,dv].
+
+    Allocates ``out`` [B,Sq,Hq,dv] bf16 and ``lse`` [B,Hq,Sq] fp32 when not given.
+    Launches on ``stream`` (default: torch's current stream).  Raises FaError on
+    any non-OK status.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    B, Sq, Hq, dqk = q.shape
+    _, Sk, Hkv, _ = k.shape
+    dv = v.shape[3]
+    if out is None:
+        out = torch.empty((B, Sq, Hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    s = 0.0 if scale is None else float(scale)
+    rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                   lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Sq, Sk, dqk, dv, causal, s, options, sptr)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return (out, lse) if return_lse else out
+
+
+def flops(batch, heads_q, seqlen_q, seqlen_k, d_qk, d_v, causal) -> float:
+    """2*B*Hq*Sq*Sk*(d_qk + d_v), halved for causal (the nominal convention)."""
+    f = 2.0 * batch * heads_q * seqlen_q * seqlen_k * (d_qk + d_v)
+    return f / 2 if causal else f
+
+
+def default_scale(d_qk: int) -> float:
+    return 1.0 / math.sqrt(d_qk)

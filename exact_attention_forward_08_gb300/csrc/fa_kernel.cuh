@@ -1,0 +1,612 @@
+// Exact attention forward for sm_103a: O = softmax(scale * Q K^T) V and the
+// per-row log-sum-exp, tiled over K/V blocks with an online softmax so the
+// score matrix never reaches HBM.
+//
+// One persistent CTA per SM, 512 threads in four warpgroups
+// ("Flash Attention 4 on Blackwell", sections "The data flow of one K/V
+// block" and "Warpgroup roles"):
+//   WG0 / WG1 (warps 0-7)  softmax of Q stage 0 / 1: thread = row = TMEM lane;
+//                          S is read from TMEM, P (bf16) written back over it.
+//   WG2 (warps 8-11)       O correction (rescale O in TMEM when a row's
+//                          reference moved) and the epilogue: O / row_sum ->
+//                          bf16 -> SMEM -> TMA store, LSE -> global.
+//   warp 12                tcgen05.mma issue (one thread) + TMEM alloc/free.
+//   warp 13                TMA loads (one thread): Q stages, K/V ring.
+// Each task covers two Q tiles (stages) that stream the same K/V blocks, so
+// one stage's softmax overlaps the other stage's MMAs.
+//
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DV),
+// O1 [384,384+DV).  P_s overwrites the first 64 columns of S_s as packed bf16
+// pairs.  SMEM: two Q stages, a ring of K/V tiles, a 16 KB O staging tile,
+// the softmax -> correction mailbox and the mbarriers.
+//
+// Hand-offs per stage s and K/V block j (mbarrier names follow the pages'
+// "Softmax, correction and barrier hand-off" section):
+//   s_full[s]   MMA commit after S_s = Q_s K_j^T             -> softmax
+//   corr_full[s] softmax wrote acc_scale (and, at the last
+//               block, row_sum and the reference)            -> correction
+//   p_full[s]   count 256: 128 softmax threads (P written) +
+//               128 correction threads (O rescaled or not)   -> PV MMA
+//   o_done[s]   MMA commit after O_s += P_s V_j              -> correction / epilogue
+// Every wait is bounded (see ptx.cuh); on a timeout the CTA records the
+// failing site in the status word, every role leaves its loop, in-flight
+// copies and MMAs are drained with bounded waits and TMEM is freed.
+#pragma once
+#include <cuda.h>
+
+#include "fa_schedule.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kThreads = 512;
+constexpr int kChunkBytes = 128 * 64 * 2;  // 128 rows x 64 bf16: one 128B-swizzled TMA box
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLn2 = 0.693147180559945309417f;
+
+// debug_flags bits
+constexpr int kDebugSkipPArrive = 1;  // softmax never arrives on p_full: exercises the bounded waits
+
+struct Params {
+  CUtensorMap tm_q;  // 5-D view (d, pack, groups, Sq, B) of q
+  CUtensorMap tm_k;  // 4-D view (d, Hkv, Sk, B) of k
+  CUtensorMap tm_v;  // 4-D view (dv, Hkv, Sk, B) of v
+  CUtensorMap tm_o;  // 5-D view (dv, pack, groups, Sq, B) of o
+  float* lse;        // [B, Hq, Sq] or null
+  unsigned int* status;
+  Problem prob;
+  float scale_log2;  // scale * log2(e)
+  float tau;         // conditional-rescale threshold, log2 units
+  unsigned long long timeout_ns;
+  int debug_flags;
+};
+
+template <int DQ, int DV>
+struct Layout {
+  static_assert(DQ % 64 == 0 && DV % 64 == 0 && DV <= DQ && DV <= 128 && DQ <= 192, "head dims");
+  static constexpr int NQC = DQ / 64;  // 64-column chunks of a Q or K tile
+  static constexpr int NVC = DV / 64;
+  static constexpr int kQBytes = NQC * kChunkBytes;
+  static constexpr int kSlotBytes = NQC * kChunkBytes;  // a ring slot holds one K tile or one V tile
+  static constexpr int kStageOBytes = kChunkBytes;
+  static constexpr int kMboxBytes = 2 * 3 * 128 * 4;   // [stage][acc_scale,row_sum,ref][row]
+  static constexpr int kMaxSmem = 232448;              // 227 KB per CTA (opt-in)
+  static constexpr int kFixed = 2 * kQBytes + kStageOBytes + kMboxBytes + 1024 + 1024;
+  static constexpr int NS_fit = (kMaxSmem - kFixed) / kSlotBytes;
+  static constexpr int NS = NS_fit > 8 ? 8 : NS_fit;  // K/V ring depth (tiles)
+  static_assert(NS >= 2, "K/V ring needs two slots");
+
+  static constexpr int oQ = 0;
+  static constexpr int oRing = oQ + 2 * kQBytes;
+  static constexpr int oStage = oRing + NS * kSlotBytes;
+  static constexpr int oMbox = oStage + kStageOBytes;
+  static constexpr int oBar = oMbox + kMboxBytes;
+
+  // barrier indices
+  static constexpr int bQFull = 0;        // [2]
+  static constexpr int bQEmpty = 2;       // [2]
+  static constexpr int bKvFull = 4;       // [NS]
+  static constexpr int bKvEmpty = 4 + NS; // [NS]
+  static constexpr int bSFull = 4 + 2 * NS;
+  static constexpr int bPFull = bSFull + 2;
+  static constexpr int bODone = bPFull + 2;
+  static constexpr int bCorrFull = bODone + 2;
+  static constexpr int bEpiFull = bCorrFull + 2;  // WG2: staging tile written (count 128)
+  static constexpr int bStageFree = bEpiFull + 1; // WG2: TMA store finished reading staging (count 1)
+  static constexpr int bDrain = bStageFree + 1;   // MMA drain at exit
+  static constexpr int kNumBars = bDrain + 1;
+
+  static constexpr int oMisc = oBar + kNumBars * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int kBytes = oMisc + 16;
+  static constexpr int kDynSmem = kBytes + 1024;     // slack to align the base to 1024 B
+  static_assert(kDynSmem <= kMaxSmem, "shared memory budget");
+};
+
+// Wait-site codes recorded in status[1] on a timeout: role * 100 + barrier.
+enum : unsigned int {
+  kSiteSoftmaxS = 101,
+  kSiteCorrCorr = 201,
+  kSiteCorrODone = 202,
+  kSiteCorrEpiFull = 203,
+  kSiteCorrStageFree = 204,
+  kSiteMmaKv = 301,
+  kSiteMmaQ = 302,
+  kSiteMmaP = 303,
+  kSiteMmaDrain = 304,
+  kSiteLoadQ = 401,
+  kSiteLoadKv = 402,
+  kSiteLoadDrain = 403,
+};
+
+// A wait that ignores the abort flag (used to drain in-flight async work
+// before TMEM is freed); still bounded by the time limit.
+__device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, unsigned site) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > w.timeout_ns) {
+      raise_abort(w, kStatusTimeout, site);
+      return;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// softmax (WG0 / WG1)
+// ---------------------------------------------------------------------------
+template <int DQ, int DV, bool CAUSAL>
+__device__ __forceinline__ void softmax_role(const Params& p, const int stage, const uint32_t tmem,
+                                             const uint32_t sbase, float* mbox, const WaitCtx& wc) {
+  using L = Layout<DQ, DV>;
+  const Problem& pr = p.prob;
+  const int t = threadIdx.x - stage * 128;  // row of the Q tile == TMEM lane
+  const uint32_t tS = tmem + (static_cast<uint32_t>(t & ~31) << 16) + static_cast<uint32_t>(stage * 128);
+  const uint32_t bar_s = sbase + L::oBar + 8 * (L::bSFull + stage);
+  const uint32_t bar_corr = sbase + L::oBar + 8 * (L::bCorrFull + stage);
+  const uint32_t bar_p = sbase + L::oBar + 8 * (L::bPFull + stage);
+  float* mb_acc = mbox + (stage * 3 + 0) * 128;
+  float* mb_sum = mbox + (stage * 3 + 1) * 128;
+  float* mb_ref = mbox + (stage * 3 + 2) * 128;
+  const float sl2 = p.scale_log2;
+  const float neg_tau = -p.tau;
+  const bool skip_p = (p.debug_flags & kDebugSkipPArrive) != 0;
+  uint32_t phase = 0;
+
+  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
+    const Task tk = decode_task(pr, task);
+    const int n = stage ? tk.n[1] : tk.n[0];
+    if (n == 0) continue;
+    const int pos0 = stage ? tk.pos0[1] : tk.pos0[0];
+    // last key visible to this row (inclusive); keys >= Sk are never visible
+    int64_t last_key = static_cast<int64_t>(pr.Sk) - 1;
+    if (CAUSAL) {
+      const int64_t c = static_cast<int64_t>(pos0 + t / pr.pack) + pr.Sk - pr.Sq;
+      if (c < last_key) last_key = c;
+    }
+    float row_max = -INFINITY;  // kept reference, raw score units
+    float row_sum = 0.f;
+    float ref = 0.f;            // row_max * scale_log2 (0 while the row is empty)
+
+    for (int j = 0; j < n; ++j) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_s, phase, wc, kSiteSoftmaxS));
+      if (!ok) return;
+      phase ^= 1u;
+      tc_fence_after();
+
+      uint32_t r[128];
+      tmem_ld128_wait(tS, r);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
+
+      if (block_needs_mask(pr, pos0, j)) {
+        // columns c <= lim are visible
+        int64_t lim64 = last_key - static_cast<int64_t>(j) * kBN;
+        const int lim = lim64 < -1 ? -1 : (lim64 > 127 ? 127 : static_cast<int>(lim64));
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+
+      float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        m0 = fmaxf(m0, s[c]);
+        m1 = fmaxf(m1, s[c + 1]);
+        m2 = fmaxf(m2, s[c + 2]);
+        m3 = fmaxf(m3, s[c + 3]);
+      }
+      const float bmax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+
+      // conditional rescaling: keep the reference unless the maximum grew by
+      // more than tau (log2 units); the first visible block takes its own max
+      float acc = 1.f;
+      if (bmax != -INFINITY) {
+        if (row_max == -INFINITY) {
+          row_max = bmax;
+        } else if (bmax > row_max) {
+          const float delta = (row_max - bmax) * sl2;
+          if (delta < neg_tau) {
+            acc = ex2_approx(delta);
+            row_max = bmax;
+          }
+        }
+      }
+      ref = (row_max == -INFINITY) ? 0.f : row_max * sl2;
+
+      float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        s[c] = ex2_approx(fmaf(s[c], sl2, -ref));
+        s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, -ref));
+        l0 += s[c];
+        l1 += s[c + 1];
+      }
+      row_sum = row_sum * acc + (l0 + l1);
+
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+      tmem_st32(tS, pk);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[64 + 2 * i], s[64 + 2 * i + 1]);
+      tmem_st32(tS + 32, pk);
+      tmem_wait_st();
+
+      mb_acc[t] = acc;
+      if (j == n - 1) {
+        mb_sum[t] = row_sum;
+        mb_ref[t] = ref;
+      }
+      tc_fence_before();
+      mbar_arrive(bar_corr);
+      if (!skip_p) mbar_arrive(bar_p);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// correction + epilogue (WG2)
+// ---------------------------------------------------------------------------
+template <int DQ, int DV, bool CAUSAL>
+__device__ __forceinline__ void correction_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
+                                                uint8_t* smem, float* mbox, const WaitCtx& wc) {
+  using L = Layout<DQ, DV>;
+  const Problem& pr = p.prob;
+  const int t = threadIdx.x - 256;  // row == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(t & ~31) << 16;
+  const uint32_t bar0 = sbase + L::oBar;
+  uint8_t* staging = smem + L::oStage;
+  const uint32_t staging_s = sbase + L::oStage;
+  uint32_t corr_phase[2] = {0u, 0u};
+  uint32_t pv_count[2] = {0u, 0u};  // PV MMAs of each stage released so far
+  uint32_t chunks = 0;              // epilogue chunks stored so far
+
+  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
+    const Task tk = decode_task(pr, task);
+    float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
+
+    for (int j = 0; j < tk.nmax; ++j) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (j >= tk.n[s]) continue;
+        bool ok = __all_sync(0xffffffffu,
+                             mbar_wait(bar0 + 8 * (L::bCorrFull + s), corr_phase[s], wc, kSiteCorrCorr));
+        if (!ok) goto out;
+        corr_phase[s] ^= 1u;
+        const float acc = mbox[(s * 3 + 0) * 128 + t];
+        if (j == tk.n[s] - 1) {
+          fin_sum[s] = mbox[(s * 3 + 1) * 128 + t];
+          fin_ref[s] = mbox[(s * 3 + 2) * 128 + t];
+        }
+        // warp-uniform skip of the O round trip when no row moved its reference
+        if (j > 0 && __any_sync(0xffffffffu, acc != 1.f)) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), (pv_count[s] - 1u) & 1u, wc,
+                                                 kSiteCorrODone));
+          if (!ok) goto out;
+          tc_fence_after();
+          const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(s * 128);
+#pragma unroll
+          for (int c = 0; c < DV; c += 32) {
+            uint32_t r[32];
+            tmem_ld32_wait(tO + c, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * acc);
+            tmem_st32(tO + c, r);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(bar0 + 8 * (L::bPFull + s));
+        ++pv_count[s];
+      }
+    }
+
+    // epilogue: O / row_sum -> bf16 -> staging -> TMA store; LSE
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int pos0 = tk.pos0[s];
+      if (pos0 >= pr.Sq) continue;  // tile past the end of the sequence
+      const bool has = tk.n[s] > 0;
+      if (has) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), (pv_count[s] - 1u) & 1u,
+                                                          wc, kSiteCorrODone));
+        if (!ok) goto out;
+        tc_fence_after();
+      }
+      float inv = 0.f, lse = -INFINITY;
+      if (has && fin_sum[s] > 0.f) {
+        inv = 1.f / fin_sum[s];
+        lse = (fin_ref[s] + __log2f(fin_sum[s])) * kLn2;
+      }
+      const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(s * 128);
+#pragma unroll 1
+      for (int c = 0; c < L::NVC; ++c) {
+        if (chunks > 0) {
+          const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * L::bStageFree, (chunks - 1u) & 1u, wc,
+                                                            kSiteCorrStageFree));
+          if (!ok) goto out;
+        }
+        uint4* row = reinterpret_cast<uint4*>(staging + t * 128);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          if (has) {
+            tmem_ld32_wait(tO + static_cast<uint32_t>(c * 64 + half * 32), r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+            row[(half * 4 + q) ^ (t & 7)] = v;  // 128-byte swizzle of the TMA box
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar0 + 8 * L::bEpiFull);
+        if (t == 0) {
+          if (!mbar_wait(bar0 + 8 * L::bEpiFull, chunks & 1u, wc, kSiteCorrEpiFull)) {
+            ++chunks;
+            goto out;
+          }
+          tma_store_5d(&p.tm_o, staging_s, c * 64, 0, tk.g, pos0, tk.b);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(bar0 + 8 * L::bStageFree);
+        }
+        ++chunks;
+      }
+      const int pos = pos0 + t / pr.pack;
+      if (p.lse != nullptr && pos < pr.Sq) {
+        const int head = tk.g * pr.pack + t % pr.pack;
+        p.lse[(static_cast<int64_t>(tk.b) * pr.Hq + head) * pr.Sq + pos] = lse;
+      }
+    }
+  }
+out:
+  if (t == 0) bulk_wait_group0();
+}
+
+// ---------------------------------------------------------------------------
+// MMA issue (warp 12, one thread)
+// ---------------------------------------------------------------------------
+// S = Q K^T: M = 128 rows, N = 128 keys, K = DQ in steps of 16 (32 bytes inside
+// a 128-byte swizzled row; a new 16 KB chunk every 64 columns).  Descriptor
+// start addresses are in 16-byte units, so offsets are added to the low field.
+template <int DQ, int DV>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, false, false);
+  const uint64_t qd = smem_desc_sw128(q_addr, 16, 1024);
+  const uint64_t kd = smem_desc_sw128(k_addr, 16, 1024);
+#pragma unroll 1
+  for (int i = 0; i < DQ / 16; ++i) {
+    const uint32_t off = static_cast<uint32_t>((i >> 2) * (kChunkBytes >> 4) + (i & 3) * 2);
+    mma_ss(d_tmem, qd + off, kd + off, kIdesc, i != 0 ? 1u : 0u);
+  }
+}
+
+// O (+)= P V: M = 128 rows, N = DV, K = 128 keys in steps of 16; P is read from
+// TMEM (8 columns of packed bf16 pairs per step), V from SMEM (MN-major: 16
+// key rows of 128 bytes per step; the second 64-column chunk is LBO away).
+template <int DV>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, DV, false, true);
+  const uint64_t vd = smem_desc_sw128(v_addr, kChunkBytes, 1024);
+#pragma unroll 1
+  for (int k = 0; k < kBN / 16; ++k) {
+    mma_ts(d_tmem, p_tmem + static_cast<uint32_t>(k * 8), vd + static_cast<uint32_t>(k * (16 * 128 >> 4)), kIdesc,
+           (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+template <int DQ, int DV>
+__device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
+                                         const WaitCtx& wc) {
+  using L = Layout<DQ, DV>;
+  const Problem& pr = p.prob;
+  const uint32_t bar0 = sbase + L::oBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  auto slot_addr = [&](uint32_t it) { return sbase + L::oRing + (it % L::NS) * L::kSlotBytes; };
+  auto q_addr = [&](int s) { return sbase + L::oQ + static_cast<uint32_t>(s * L::kQBytes); };
+  uint32_t q_phase[2] = {0u, 0u}, p_phase[2] = {0u, 0u};
+  uint32_t kv_it = 0;  // K/V tiles consumed so far (ring order K0, V0, K1, V1, ...)
+
+  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
+    const Task tk = decode_task(pr, task);
+    if (tk.nmax == 0) continue;
+
+    // prologue: S_s = Q_s K_0^T for both stages
+    {
+      const uint32_t slot = kv_it % L::NS;
+      if (!mbar_wait(bar(L::bKvFull + slot), (kv_it / L::NS) & 1u, wc, kSiteMmaKv)) goto out;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (tk.n[s] == 0) continue;
+        if (!mbar_wait(bar(L::bQFull + s), q_phase[s], wc, kSiteMmaQ)) goto out;
+        q_phase[s] ^= 1u;
+        tc_fence_after();
+        issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(kv_it));
+        mma_commit(bar(L::bSFull + s));
+        if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s));
+      }
+      mma_commit(bar(L::bKvEmpty + slot));
+      ++kv_it;
+    }
+
+    for (int j = 0; j < tk.nmax; ++j) {
+      const uint32_t v_it = kv_it;
+      const uint32_t vslot = v_it % L::NS;
+      if (!mbar_wait(bar(L::bKvFull + vslot), (v_it / L::NS) & 1u, wc, kSiteMmaKv)) goto out;
+      const uint32_t k_it = kv_it + 1;  // K_{j+1}
+      bool k_ready = false;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (j >= tk.n[s]) continue;
+        if (!mbar_wait(bar(L::bPFull + s), p_phase[s], wc, kSiteMmaP)) goto out;
+        p_phase[s] ^= 1u;
+        tc_fence_after();
+        issue_pv<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
+                     slot_addr(v_it), j > 0);
+        mma_commit(bar(L::bODone + s));
+        if (j + 1 < tk.n[s]) {
+          if (!k_ready) {
+            if (!mbar_wait(bar(L::bKvFull + k_it % L::NS), (k_it / L::NS) & 1u, wc, kSiteMmaKv)) goto out;
+            k_ready = true;
+          }
+          issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(k_it));
+          mma_commit(bar(L::bSFull + s));
+          if (j + 2 == tk.n[s]) mma_commit(bar(L::bQEmpty + s));
+        }
+      }
+      mma_commit(bar(L::bKvEmpty + vslot));
+      ++kv_it;
+      if (j + 1 < tk.nmax) {
+        mma_commit(bar(L::bKvEmpty + k_it % L::NS));
+        ++kv_it;
+      }
+    }
+  }
+out:
+  // every MMA issued by this thread has completed once the drain barrier fires
+  mma_commit(bar(L::bDrain));
+  mbar_drain_wait(bar(L::bDrain), 0u, wc, kSiteMmaDrain);
+}
+
+// ---------------------------------------------------------------------------
+// TMA loads (warp 13, one thread)
+// ---------------------------------------------------------------------------
+template <int DQ, int DV>
+__device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase, const WaitCtx& wc) {
+  using L = Layout<DQ, DV>;
+  const Problem& pr = p.prob;
+  const uint32_t bar0 = sbase + L::oBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t q_uses[2] = {0u, 0u};
+  uint32_t kv_it = 0;  // K/V tiles issued
+
+  tma_prefetch_desc(&p.tm_q);
+  tma_prefetch_desc(&p.tm_k);
+  tma_prefetch_desc(&p.tm_v);
+
+  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
+    const Task tk = decode_task(pr, task);
+    if (tk.nmax == 0) continue;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (tk.n[s] == 0) continue;
+      if (q_uses[s] > 0 && !mbar_wait(bar(L::bQEmpty + s), (q_uses[s] - 1u) & 1u, wc, kSiteLoadQ)) goto out;
+      const uint32_t qb = bar(L::bQFull + s);
+      mbar_arrive_expect_tx(qb, L::NQC * kChunkBytes);
+      const uint32_t dst = sbase + L::oQ + static_cast<uint32_t>(s * L::kQBytes);
+      for (int c = 0; c < L::NQC; ++c)
+        tma_load_5d(dst + c * kChunkBytes, &p.tm_q, qb, c * 64, 0, tk.g, tk.pos0[s], tk.b);
+      ++q_uses[s];
+    }
+    for (int j = 0; j < tk.nmax; ++j) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // K_j then V_j
+        const uint32_t slot = kv_it % L::NS;
+        if (kv_it >= static_cast<uint32_t>(L::NS) &&
+            !mbar_wait(bar(L::bKvEmpty + slot), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
+          goto out;
+        const uint32_t fb = bar(L::bKvFull + slot);
+        const uint32_t dst = sbase + L::oRing + slot * L::kSlotBytes;
+        const int nch = which == 0 ? L::NQC : L::NVC;
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nch * kChunkBytes));
+        for (int c = 0; c < nch; ++c)
+          tma_load_4d(dst + c * kChunkBytes, which == 0 ? static_cast<const void*>(&p.tm_k) : &p.tm_v, fb,
+                      c * 64, tk.kvh, j * kBN, tk.b);
+        ++kv_it;
+      }
+    }
+  }
+out:
+  // drain: the last copy issued into every buffer has landed
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+    if (q_uses[s] > 0) mbar_drain_wait(bar(L::bQFull + s), (q_uses[s] - 1u) & 1u, wc, kSiteLoadDrain);
+  for (uint32_t i = 0; i < static_cast<uint32_t>(L::NS) && i < kv_it; ++i) {
+    const uint32_t uses = (kv_it - i + L::NS - 1) / L::NS;  // copies issued into slot i
+    mbar_drain_wait(bar(L::bKvFull + i), (uses - 1u) & 1u, wc, kSiteLoadDrain);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int DQ, int DV, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
+  using L = Layout<DQ, DV>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
+  float* mbox = reinterpret_cast<float*>(smem + L::oMbox);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    const uint32_t b = sbase + L::oBar;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(b + 8 * (L::bQFull + s), 1);
+      mbar_init(b + 8 * (L::bQEmpty + s), 1);
+      mbar_init(b + 8 * (L::bSFull + s), 1);
+      mbar_init(b + 8 * (L::bPFull + s), 256);
+      mbar_init(b + 8 * (L::bODone + s), 1);
+      mbar_init(b + 8 * (L::bCorrFull + s), 128);
+    }
+    for (int i = 0; i < L::NS; ++i) {
+      mbar_init(b + 8 * (L::bKvFull + i), 1);
+      mbar_init(b + 8 * (L::bKvEmpty + i), 1);
+    }
+    mbar_init(b + 8 * L::bEpiFull, 128);
+    mbar_init(b + 8 * L::bStageFree, 1);
+    mbar_init(b + 8 * L::bDrain, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 12) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+  // register budget: 128 x (176 + 176 + 104 + 56) = 65536
+  if (warp < 8) {
+    setmaxnreg_inc<176>();
+    softmax_role<DQ, DV, CAUSAL>(p, warp >> 2, tmem, sbase, mbox, wc);
+  } else if (warp < 12) {
+    setmaxnreg_dec<104>();
+    correction_role<DQ, DV, CAUSAL>(p, tmem, sbase, smem, mbox, wc);
+  } else {
+    setmaxnreg_dec<56>();
+    if (warp == 12) {
+      if (lane == 0) mma_role<DQ, DV>(p, tmem, sbase, wc);
+      __syncwarp();
+    } else if (warp == 13) {
+      if (lane == 0) load_role<DQ, DV>(p, sbase, wc);
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,157 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * The operation is the exact attention forward pass with its per-row
+ * log-sum-exp:
+ *
+ *     S = scale * Q K^T,   P = softmax(S) (row-wise),   O = P V,
+ *     L_i = log sum_j exp(S_ij)
+ *
+ * ("Flash Attention 4 on Blackwell" (GPU-HPC book, ch. 13), section
+ * "Attention's real bottleneck": O = softmax(QK^T / sqrt(d)) V;
+ * "Infra: Flash Attention", Algorithm 1 (FlashAttention forward): outputs O and
+ * L_i = m_i + log l_i, and section "Why backward recomputes":
+ * L_i = log sum_j e^{S_ij}.)
+ *
+ * The score matrix is never materialised: K/V are streamed in 128-key blocks
+ * with an online softmax and conditional rescaling (threshold tau in log2
+ * units, "Flash Attention 4 on Blackwell", section "Online softmax and
+ * conditional rescaling").
+ *
+ * Layouts (dense, contiguous, BSHD as in the pages' usage example, section
+ * "Build and validation constraints"):
+ *   q   [batch, seqlen_q, heads_q,  d_qk]  bf16
+ *   k   [batch, seqlen_k, heads_kv, d_qk]  bf16
+ *   v   [batch, seqlen_k, heads_kv, d_v ]  bf16
+ *   o   [batch, seqlen_q, heads_q,  d_v ]  bf16 (written)
+ *   lse [batch, heads_q,  seqlen_q]        fp32, natural log (written; may be NULL)
+ * Query head h reads key/value head h / (heads_q / heads_kv) (GQA/MQA,
+ * "Flash Attention 4 on Blackwell", section "Causal attention and GQA").
+ *
+ * Mask: causal = 0 attends to every key.  causal = 1 is the bottom-right
+ * aligned mask: query i sees key j iff j <= i + seqlen_k - seqlen_q (same
+ * section).  A query row that sees no key (seqlen_q > seqlen_k) gets O = 0
+ * and lse = -inf; the pages leave that row to the operator ("Infra: Flash
+ * Attention", section "Notation and boundary conditions").
+ *
+ * Ownership: every tensor pointer is caller-owned device memory on the
+ * current CUDA device, 16-byte aligned (TMA requirement).  The library
+ * allocates no memory for the caller; it keeps a per-device cache of device
+ * properties and a 16-byte device status word.
+ *
+ * Ordering: calls are asynchronous and stream-ordered on `stream`; no host
+ * synchronisation happens inside.  Argument errors are reported before any
+ * CUDA call.  A device-side timeout of the kernel's bounded waits is recorded
+ * in the status word and read with fa_device_status().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers (same underlying type). */
+struct CUstream_st;
+typedef struct CUstream_st* fa_stream_t;
+
+enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, heads_q % heads_kv != 0, misaligned
+                                 or non-device pointer, bad scale or option */
+  FA_ERR_UNSUPPORTED = 2,     /* head dims outside {(64,64), (128,64), (128,128), (192,64), (192,128)},
+                                 or a device that is not sm_103 / sm_100 family */
+  FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed (cudaGetLastError is left set) */
+  FA_ERR_DEVICE_TIMEOUT = 4   /* a bounded device wait expired (from fa_device_status) */
+};
+
+/*
+ * Exact attention forward.
+ *
+ * batch, heads_q, heads_kv, seqlen_q, seqlen_k >= 0 (heads >= 1 unless batch or
+ * seqlen_q is 0); heads_q % heads_kv == 0.  d_qk in {64, 128, 192},
+ * d_v in {64, 128}, d_v <= d_qk.  scale multiplies QK^T before the softmax;
+ * scale == 0 selects 1/sqrt(d_qk); a negative or non-finite scale is rejected.
+ * A problem with batch, heads or seqlen_q equal to 0 returns FA_OK without a
+ * launch.  seqlen_k == 0 writes O = 0 and lse = -inf.
+ *
+ * Returns FA_OK when the work was enqueued.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+           int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+           fa_stream_t stream);
+
+/* Options for ablations and tests (fa_fwd uses the defaults). */
+typedef struct fa_options {
+  float tau;          /* conditional-rescale threshold, log2 units; < 0 selects 8 */
+  int pack;           /* query heads packed into one 128-row tile; 0 = automatic (the GQA
+                         ratio when it divides 128, else 1); otherwise must divide both */
+  int grid;           /* persistent CTAs; 0 = one per SM */
+  double timeout_s;   /* limit of every device-side wait; <= 0 selects 1 s */
+  int debug_flags;    /* bit 0: the softmax warps never signal P ready, so the MMA warp's
+                         bounded wait expires (tests the failure path; the output is not
+                         valid).  Other bits must be 0. */
+} fa_options;
+
+/* Fill `opts` with the defaults. */
+void fa_options_default(fa_options* opts);
+
+/* fa_fwd with options; opts == NULL means defaults. */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+              int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+              const fa_options* opts, fa_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status
+ * word.  *out receives FA_OK or FA_ERR_DEVICE_TIMEOUT; detail (may be NULL)
+ * receives {code, wait site, block index}.  Returns FA_OK or FA_ERR_CUDA.
+ */
+int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]);
+
+/* Human-readable name of a status code (static storage). */
+const char* fa_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+/*
+ * Host-only view of the tile decomposition the kernel runs (no CUDA call).
+ * A task is (batch b, head group g, m_block): two consecutive 128-row Q tiles
+ * ("stages") that stream the same K/V blocks ("Flash Attention 4 on
+ * Blackwell", section "Scheduling": tasks (batch, kv_head, m_block), each
+ * m_block holding two Q stages; causal tasks run longest first).
+ */
+typedef struct fa_plan {
+  int batch, heads_q, heads_kv, seqlen_q, seqlen_k, causal;
+  int pack;            /* query heads per tile */
+  int groups;          /* heads_q / pack */
+  int pos_per_tile;    /* 128 / pack sequence positions per tile */
+  int tiles;           /* Q tiles per (b, g) */
+  int mblocks;         /* tasks per (b, g) */
+  int kv_blocks;       /* ceil(seqlen_k / 128) */
+  int ratio;           /* heads_q / heads_kv */
+  int section_units;   /* causal order: (b, g) units per L2 section */
+  int64_t num_tasks;
+} fa_plan;
+
+typedef struct fa_task {
+  int b, g, mblock, kv_head;
+  int pos0[2];         /* first sequence position of each stage's tile */
+  int n_blocks[2];     /* K/V blocks each stage visits */
+} fa_task;
+
+/* l2_bytes: L2 budget used to size causal sections (0 selects 64 MiB). */
+int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v,
+                 int causal, int64_t l2_bytes, int pack, fa_plan* out);
+int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out);
+
+/* Does block j need the element mask for a tile starting at pos0? (host view) */
+int fa_plan_block_masked(const fa_plan* plan, int pos0, int j);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */
