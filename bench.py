@@ -1,0 +1,435 @@
+"""Benchmark: attention forward TFLOP/s on GB300 (BF16) and fraction of the
+dense BF16 tensor peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config mha8k] [--impl ours|reference]
+
+A step is one exact attention forward (the whole hot path) over the chosen
+workload, default the MHA non-causal configuration B4 H16 S8192 d128 (32k
+tokens).  Inputs are synthetic (seeded N(0,1) bf16) and resident in HBM when
+the timed region starts; Q, K, V and O together (514 MiB) are larger than L2,
+so no flush is needed between steps.  Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (a deliberately slow baseline, not a target).
+
+Under torchrun (N > 1) every rank runs its own batch of the workload on its
+own GPU (weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s on 1 GB300 (BF16) and % of dense BF16 tensor peak"
+FALLBACK_PEAK_TFLOPS = 1900.0  # burst bf16 of one earlier GB300 measurement
+KERNEL_NAME = "fa_fwd_kernel"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="mha8k")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if a.steps < 1:
+        ap.error("--steps must be >= 1")
+    return a
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def load_peak():
+    """(TFLOP/s, source): the measured burst bf16 GEMM rate, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.gpu = gpu_index
+        self.enabled = enabled
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        if not self.enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        window = [r for r in rows if self.t0 and self.t1 and self.t0 - 0.15 <= r[0] <= self.t1 + 0.15]
+        if not window:
+            window = rows
+        if not window:
+            return None
+        try:
+            mhz = [float(p[1]) for _, p in window]
+            mx = max(float(p[2]) for _, p in window)
+        except ValueError:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in window for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": reasons, "samples": len(window),
+                "power_w_max": max((float(p[3]) for _, p in window if p[3].replace('.', '', 1).isdigit()),
+                                   default=None)}
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; a stored ncu traffic figure is valid only for it."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_forward_08_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(config: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"fa_fwd_{config}_dram.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_hash") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_batch_seed(base_seed: int, rank: int) -> int:
+    """Each rank owns a distinct batch of the workload (distinct inputs)."""
+    return base_seed + 1000003 * rank
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(w, q, k, v, seconds: float):
+    """Time the oracle (as it stands) on uniformly sampled rows of the workload.
+    Returns the cpu_baseline object (TFLOP/s counted with the workload's
+    nominal flops per row)."""
+    import numpy as np
+    import oracle
+
+    threads = oracle.default_threads()
+    total_rows = w.batch * w.seqlen_q * w.heads_q
+    per_row = w.flops() / total_rows
+    rng = np.random.default_rng(12345)
+
+    def run(n):
+        rows = rng.integers(0, total_rows, size=n, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, causal=w.causal, scale=w.softmax_scale, rows=rows, threads=threads)
+        return time.perf_counter() - t0
+
+    n0 = max(threads * 4, 64)
+    dt0 = run(n0)  # calibration
+    n = int(min(total_rows, max(n0, n0 * seconds / max(dt0, 1e-3))))
+    dt = run(n)
+    return {"value": n * per_row / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {total_rows} rows of {w.name} drawn uniformly (fp64 C oracle, {threads} threads, "
+                      f"{dt:.1f} s)", "seconds": round(dt, 2), "rows": n}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import exact_attention_forward_08_gb300 as fa
+    import synthetic
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl" if world > 1 else "gloo")
+    fa.load_library()
+
+    w0 = synthetic.workloads()[args.config]
+    w = synthetic.Workload(**{**w0.__dict__, "seed": rank_batch_seed(w0.seed, rank)})
+    qb, kb, vb = w.generate()
+    to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    qh, kh, vh = (to_t(a).pin_memory() for a in (qb, kb, vb))
+    qd, kd, vd = (t.to(dev) for t in (qh, kh, vh))
+    o = torch.empty(w.shapes["o"], dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.shapes["lse"], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    scale = w.softmax_scale
+
+    def step():
+        rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), w.batch,
+                       w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, sp)
+        if rc != 0:
+            raise fa.FaError(rc, "fa_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    code, detail = fa.fa_device_status()
+    if code != 0:
+        raise fa.FaError(code, f"device status after warm-up {detail}")
+
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    clocks.start()
+    time.sleep(0.3 if clocks.enabled else 0)
+    for _ in range(args.warmup):
+        step()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark("start")
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark("stop")
+    barrier()
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    clk = clocks.stop()
+    code, detail = fa.fa_device_status()
+    if code != 0:
+        raise fa.FaError(code, f"device status after timed region {detail}")
+    ms_step = ms_total / args.steps
+    flops = w.flops()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # end to end: pinned host inputs -> device, forward, O and LSE back to host
+    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev) / args.e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+
+    peak, peak_src = load_peak()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    traffic = stored_traffic(args.config)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.notes}", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
+                   "heads_q": w.heads_q, "heads_kv": w.heads_kv, "seq_len": w.seqlen_q, "d_qk": w.d_qk,
+                   "d_v": w.d_v, "causal": w.causal, "flops_per_step_per_gpu": flops,
+                   "l2": "inputs larger than L2 (Q+K+V+O %.0f MiB per GPU), no flush" %
+                         (w.algorithmic_bytes() / 2 ** 20),
+                   "parallelism": f"weak x{world} (independent batches, no collective)"},
+        "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} (bf16 dense, burst)",
+                     "algorithmic_bytes": w.algorithmic_bytes()},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, qb, kb, vb, args.cpu_seconds)
+    elif rank == 0:
+        result["cpu_baseline"] = None
+    return rank, result
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    """Each step runs the oracle (as it stands) on a bounded uniform sample of
+    the workload's rows; the sample size keeps the whole run to about two
+    minutes.  Rank 0 alone runs; other ranks exit without work."""
+    import numpy as np
+    import oracle
+    import synthetic
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return rank, None
+    w = synthetic.workloads()[args.config]
+    q, k, v = w.generate()
+    threads = oracle.default_threads()
+    total_rows = w.batch * w.seqlen_q * w.heads_q
+    per_row = w.flops() / total_rows
+    rng = np.random.default_rng(777)
+
+    def one(n):
+        rows = rng.integers(0, total_rows, size=n, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, causal=w.causal, scale=w.softmax_scale, rows=rows, threads=threads)
+        return time.perf_counter() - t0
+
+    n_cal = max(4 * threads, 64)
+    rate = n_cal / max(one(n_cal), 1e-3)  # rows per second
+    per_step_s = min(10.0, 120.0 / (args.steps + args.warmup))
+    n = int(max(threads, min(total_rows, rate * per_step_s)))
+    for _ in range(args.warmup):
+        one(n)
+    times = [one(n) for _ in range(args.steps)]
+    s_step = sum(times) / len(times)
+    value = n * per_row / s_step / 1e12
+    sample = (f"{n} of {total_rows} rows of {w.name} per step, drawn uniformly; fp64 C oracle on {threads} "
+              f"host threads")
+    result = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.notes}", "batch_per_gpu": w.batch, "global_batch": w.batch,
+                   "seq_len": w.seqlen_q, "rows_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    return rank, result
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, result = (run_reference if args.impl == "reference" else run_ours)(args)
+    if rank == 0 and result is not None:
+        print(json.dumps(result), flush=True)
+    try:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    except Exception:
+        pass
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -156,7 +156,9 @@ int validate(const void* q, const void* k, const void* v, void* o, const float* 
   if (!(std::isfinite(scale)) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (kernel_index(d_qk, d_v, 0) < 0) return FA_ERR_UNSUPPORTED;
   if (opt.pack < 0 || opt.grid < 0 || (opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
-  if (!(std::isfinite(opt.tau)) && !(opt.tau > 0.f)) return FA_ERR_INVALID_ARG;  // NaN
+  // the kept reference may lag the row maximum by up to tau (log2 units), so
+  // unnormalised weights reach 2^tau: keep them far inside the fp32 range
+  if (!(opt.tau >= 0.f && opt.tau <= 64.f)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(opt.timeout_s) || opt.timeout_s > 3600.0) return FA_ERR_INVALID_ARG;
   if (opt.pack > 0) {
     const int ratio = heads_q / heads_kv;
@@ -250,6 +252,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   std::memset(&p, 0, sizeof(p));
   p.prob = fa::make_problem(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, st->l2_bytes / 2,
                             opt.pack);
+  if (p.prob.num_tasks >= (int64_t(1) << 31)) return FA_ERR_INVALID_ARG;  // the device decodes tasks in 32 bits
   if (encode_q_like(&p.tm_q, q, batch, seqlen_q, heads_q, d_qk, p.prob.pack) != FA_OK) return FA_ERR_CUDA;
   if (encode_kv(&p.tm_k, k, batch, seqlen_k, heads_kv, d_qk) != FA_OK) return FA_ERR_CUDA;
   if (encode_kv(&p.tm_v, v, batch, seqlen_k, heads_kv, d_v) != FA_OK) return FA_ERR_CUDA;

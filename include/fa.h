@@ -85,7 +85,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 /* Options for ablations and tests (fa_fwd uses the defaults). */
 typedef struct fa_options {
-  float tau;          /* conditional-rescale threshold, log2 units; < 0 selects 8 */
+  float tau;          /* conditional-rescale threshold, log2 units; < 0 selects 8; at most 64,
+                         since unnormalised weights reach 2^tau */
   int pack;           /* query heads packed into one 128-row tile; 0 = automatic (the GQA
                          ratio when it divides 128, else 1); otherwise must divide both */
   int grid;           /* persistent CTAs; 0 = one per SM */

@@ -177,6 +177,9 @@ def workloads() -> dict:
                         notes="B4 S8192 Hq32 Hkv8 d128 causal")
     w["mqa"] = Workload("mqa", 4, 32, 1, 8192, 8192, 128, 128, True, seed=30,
                         notes="B4 S8192 Hq32 Hkv1 d128 causal")
+    # smaller case of the MHA kernel for detailed profiling (inputs still > L2)
+    w["prof_mha"] = Workload("prof_mha", 2, 16, 16, 8192, 8192, 128, 128, False, seed=101,
+                             notes="B2 H16 S8192 d128 non-causal (profiling case)")
     w["asym"] = Workload("asym", 2, 16, 16, 16384, 16384, 192, 128, True, seed=4, q_mul=4.0,
                          k_offset=12.0,
                          notes="B2 H16 S16384 d_qk192 d_v128 causal, Q=4N(0,1), K=N(0,1)+0..12")

@@ -1,0 +1,236 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerances for bf16 outputs of unit-normal inputs: max|O - O_ref| <= 2e-2,
+mean|O - O_ref| <= 2e-3, and |LSE - LSE_ref| <= 1e-3 (fp32 LSE).  Rows with no
+visible key must give O = 0 and LSE = -inf exactly.
+
+Small problems compare every output element; the benchmark configurations
+compare sampled rows (first, last and diagonal tiles plus random rows) in the
+launch configuration the bench times.
+"""
+import math
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MAX_TOL, MEAN_TOL, LSE_TOL = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_08_gb300 as m
+    from exact_attention_forward_08_gb300 import _build
+    _build.build()
+    m.load_library()
+    return m
+
+
+def to_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run_gpu(fa, w, q, k, v, options=None):
+    o, lse = fa.attention_forward(to_dev(q), to_dev(k), to_dev(v), causal=w.causal, scale=w.softmax_scale,
+                                  options=options)
+    torch.cuda.synchronize()
+    code, detail = fa.fa_device_status()
+    assert code == 0, f"device status {fa.STATUS.get(code, code)} detail={detail}"
+    return o, lse
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    """o_gpu [n, dv] float64, lse_gpu [n]; same for the oracle."""
+    empty = ~np.isfinite(lse_ref)
+    assert np.array_equal(~np.isfinite(lse_gpu), empty), f"{what}: empty-row pattern differs"
+    if np.any(empty):
+        assert np.all(lse_gpu[empty] == -np.inf) and np.all(o_gpu[empty] == 0.0), f"{what}: empty rows"
+    err = np.abs(o_gpu - o_ref)
+    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
+    emax, emean = float(err.max()), float(err.mean())
+    lerr = float(np.abs(lse_gpu[~empty] - lse_ref[~empty]).max()) if np.any(~empty) else 0.0
+    assert emax <= MAX_TOL, f"{what}: max|dO| {emax:.3e}"
+    assert emean <= MEAN_TOL, f"{what}: mean|dO| {emean:.3e}"
+    assert lerr <= LSE_TOL, f"{what}: max|dLSE| {lerr:.3e}"
+    return emax, emean, lerr
+
+
+def full_check(fa, w, options=None):
+    q, k, v = w.generate()
+    o, lse = run_gpu(fa, w, q, k, v, options)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal=w.causal, scale=w.softmax_scale)
+    og = o.float().cpu().numpy().astype(np.float64).reshape(-1, w.d_v)
+    # LSE [B,Hq,Sq] -> row order (b, i, h)
+    lg = lse.cpu().numpy().astype(np.float64).transpose(0, 2, 1).reshape(-1)
+    lr = lse_ref.transpose(0, 2, 1).reshape(-1)
+    return compare(og, lg, o_ref.reshape(-1, w.d_v), lr, w.name)
+
+
+SMALL = [
+    # name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, extra
+    ("tiny", 1, 1, 1, 128, 128, 64, 64, False, {}),
+    ("ragged", 2, 4, 4, 300, 300, 128, 128, False, {}),
+    ("causal384", 2, 4, 4, 384, 384, 128, 128, True, {}),
+    ("causal_sq_lt_sk", 1, 8, 2, 200, 456, 128, 128, True, {}),
+    ("causal_empty_rows", 1, 8, 2, 456, 200, 128, 128, True, {}),
+    ("gqa4", 1, 32, 8, 500, 500, 128, 128, True, {}),
+    ("mqa32", 1, 32, 1, 300, 300, 128, 128, True, {}),
+    ("ratio3", 1, 6, 2, 77, 77, 192, 128, True, {}),
+    ("ratio256", 1, 256, 1, 20, 40, 64, 64, False, {}),
+    ("asym_offset", 1, 16, 16, 1000, 1000, 192, 128, True, dict(q_mul=4.0, k_offset=12.0)),
+    ("d64", 2, 4, 2, 257, 513, 64, 64, False, {}),
+    ("d128_v64", 1, 3, 1, 140, 260, 128, 64, True, {}),
+    ("d192_v64", 1, 3, 1, 40, 40, 192, 64, False, {}),
+    ("one_key", 1, 2, 2, 1, 1, 128, 128, False, {}),
+    ("short_k", 1, 2, 1, 5, 130, 128, 64, True, {}),
+    ("sk_below_tile", 2, 2, 2, 70, 33, 64, 64, False, {}),
+    ("many_tasks", 3, 8, 8, 1300, 1300, 64, 64, True, {}),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_full(fa, case):
+    name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, extra = case
+    w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, seed=zlib.crc32(name.encode()) % 1000, **extra)
+    full_check(fa, w)
+
+
+def test_sk_zero_gives_zero_and_neg_inf(fa):
+    B, Sq, Hq, d = 2, 70, 4, 128
+    q = to_dev(synthetic.normal_bf16((B, Sq, Hq, d), 1, 1))
+    k = torch.empty((B, 0, Hq, d), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((B, 0, Hq, d), dtype=torch.bfloat16, device="cuda")
+    o = torch.full((B, Sq, Hq, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((B, Hq, Sq), dtype=torch.float32, device="cuda")
+    rc = fa.fa_fwd(q.data_ptr(), k.data_ptr() or q.data_ptr(), v.data_ptr() or q.data_ptr(), o.data_ptr(),
+                   lse.data_ptr(), B, Hq, Hq, Sq, 0, d, d, 0, 0.0, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isinf(lse)) and torch.all(lse < 0)
+
+
+def test_explicit_scale_and_default_scale(fa):
+    w = synthetic.Workload("scale", 1, 2, 2, 130, 200, 128, 128, False, seed=5, scale=0.05)
+    full_check(fa, w)
+    w2 = synthetic.Workload("scale0", 1, 2, 2, 130, 200, 128, 128, False, seed=5)
+    q, k, v = w2.generate()
+    o1, l1 = fa.attention_forward(to_dev(q), to_dev(k), to_dev(v), scale=None)
+    o2, l2 = fa.attention_forward(to_dev(q), to_dev(k), to_dev(v), scale=1 / math.sqrt(128))
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_lse_optional(fa):
+    w = synthetic.Workload("nolse", 1, 2, 2, 100, 100, 64, 64, True, seed=3)
+    q, k, v = w.generate()
+    o = fa.attention_forward(to_dev(q), to_dev(k), to_dev(v), causal=True, return_lse=False)
+    o2, _ = fa.attention_forward(to_dev(q), to_dev(k), to_dev(v), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+
+
+# ---------------------------------------------------------------------------
+# determinism, tau ablation, packing, grid shape
+# ---------------------------------------------------------------------------
+
+def test_repeat_runs_bit_identical(fa):
+    w = synthetic.Workload("det", 2, 8, 2, 700, 700, 128, 128, True, seed=21)
+    q, k, v = w.generate()
+    outs = [run_gpu(fa, w, q, k, v) for _ in range(3)]
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0, 64.0])
+def test_tau_ablation_agrees(fa, tau):
+    """Conditional rescaling is exact in real arithmetic for any threshold."""
+    w = synthetic.Workload("tau", 1, 4, 4, 600, 600, 192, 128, True, seed=31, q_mul=4.0, k_offset=12.0)
+    opts = fa.default_options()
+    opts.tau = tau
+    full_check(fa, w, options=opts)
+
+
+def test_pack1_equals_packed(fa):
+    w = synthetic.Workload("pack", 1, 16, 4, 333, 333, 128, 128, True, seed=41)
+    q, k, v = w.generate()
+    o1, l1 = run_gpu(fa, w, q, k, v)
+    opts = fa.default_options()
+    opts.pack = 1
+    o2, l2 = run_gpu(fa, w, q, k, v, opts)
+    d = (o1.float() - o2.float()).abs().max().item()
+    assert d <= 1e-2 and (l1 - l2).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("grid", [1, 3, 1000])
+def test_grid_shapes(fa, grid):
+    w = synthetic.Workload("grid", 2, 4, 4, 520, 390, 128, 128, True, seed=51)
+    opts = fa.default_options()
+    opts.grid = grid
+    full_check(fa, w, options=opts)
+
+
+def test_rejects_host_pointers(fa):
+    q = torch.zeros((1, 128, 1, 64), dtype=torch.bfloat16)
+    rc = fa.fa_fwd(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), None, 1, 1, 1, 128, 128, 64, 64, 0,
+                   0.0, None)
+    assert rc == fa.FA_ERR_INVALID_ARG
+
+
+def test_stream_ordering(fa):
+    """Launch on a side stream; results match the default-stream launch."""
+    w = synthetic.Workload("stream", 1, 4, 4, 256, 256, 128, 128, False, seed=61)
+    q, k, v = w.generate()
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o1, l1 = fa.attention_forward(qd, kd, vd)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2, l2 = fa.attention_forward(qd, kd, vd, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ---------------------------------------------------------------------------
+# the benchmark configurations at full size, sampled rows
+# ---------------------------------------------------------------------------
+
+def sample_rows(w, n_random, seed):
+    """Row ids (b, i, h) from the first, last and diagonal tiles plus random rows."""
+    r = np.random.default_rng(seed)
+    B, Sq, Hq = w.batch, w.seqlen_q, w.heads_q
+    pos = [0, 1, 63, 127, 128, Sq // 2, Sq - 129, Sq - 128, Sq - 2, Sq - 1]
+    pos = [p for p in pos if 0 <= p < Sq]
+    b = np.concatenate([np.full(len(pos), B - 1), r.integers(0, B, n_random)])
+    i = np.concatenate([np.array(pos), r.integers(0, Sq, n_random)])
+    h = np.concatenate([np.arange(len(pos)) % Hq, r.integers(0, Hq, n_random)])
+    return b, i, h
+
+
+BENCH_CONFIGS = ["tiny", "mha8k", "causal1k", "causal2k", "causal4k", "causal8k", "causal16k", "causal32k", "gqa",
+                 "mqa", "asym"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", BENCH_CONFIGS)
+def test_bench_config_sampled(fa, name):
+    w = synthetic.workloads()[name]
+    q, k, v = w.generate()
+    o, lse = run_gpu(fa, w, q, k, v)
+    b, i, h = sample_rows(w, 600, seed=len(name))
+    rows = oracle.row_ids(b, i, h, w.seqlen_q, w.heads_q)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal=w.causal, scale=w.softmax_scale, rows=rows)
+    bi, ii, hi = (torch.from_numpy(x).cuda() for x in (b, i, h))
+    og = o[bi, ii, hi].float().cpu().numpy().astype(np.float64)
+    lg = lse[bi, hi, ii].cpu().numpy().astype(np.float64)
+    compare(og, lg, o_ref, lse_ref, name)
+    # properties that hold at any size: every output finite, every LSE finite
+    # (no empty rows in these configurations), |O| bounded by max|V|
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    vmax = float(np.abs(synthetic.bf16_bits_to_f32(v)).max())
+    assert float(o.float().abs().max()) <= vmax * (1 + 2 ** -7)
