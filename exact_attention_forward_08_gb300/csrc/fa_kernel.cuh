@@ -349,17 +349,20 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         }
         fence_proxy_async_smem();
         mbar_arrive(bar0 + 8 * L::bEpiFull);
+        bool stored = true;
         if (t == 0) {
-          if (!mbar_wait(bar0 + 8 * L::bEpiFull, chunks & 1u, wc, kSiteCorrEpiFull)) {
-            ++chunks;
-            goto out;
+          stored = mbar_wait(bar0 + 8 * L::bEpiFull, chunks & 1u, wc, kSiteCorrEpiFull);
+          if (stored) {
+            tma_store_5d(&p.tm_o, staging_s, c * 64, 0, tk.g, pos0, tk.b);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(bar0 + 8 * L::bStageFree);
           }
-          tma_store_5d(&p.tm_o, staging_s, c * 64, 0, tk.g, pos0, tk.b);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-          mbar_arrive(bar0 + 8 * L::bStageFree);
         }
+        // the whole warp leaves together (its later collectives need every lane)
+        stored = __all_sync(0xffffffffu, stored);
         ++chunks;
+        if (!stored) goto out;
       }
       const int pos = pos0 + t / pr.pack;
       if (p.lse != nullptr && pos < pr.Sq) {
