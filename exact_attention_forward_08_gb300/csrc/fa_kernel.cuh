@@ -22,12 +22,14 @@
 //
 // Hand-offs per stage s and K/V block j (mbarrier names follow the pages'
 // "Softmax, correction and barrier hand-off" section):
-//   s_full[s]   MMA commit after S_s = Q_s K_j^T             -> softmax
-//   corr_full[s] softmax wrote acc_scale (and, at the last
-//               block, row_sum and the reference)            -> correction
-//   p_full[s]   count 256: 128 softmax threads (P written) +
-//               128 correction threads (O rescaled or not)   -> PV MMA
-//   o_done[s]   MMA commit after O_s += P_s V_j              -> correction / epilogue
+//   s_full[s]    MMA commit after S_s = Q_s K_j^T            -> softmax
+//   corr_full[s] softmax posted acc_scale (right after the row
+//                max, before the exponentials)               -> correction
+//   fin_full[s]  last block only: row_sum and the reference
+//                posted for the epilogue                     -> correction
+//   p_full[s]    count 256: 128 softmax threads (P written) +
+//                128 correction threads (O rescaled or not)  -> PV MMA
+//   o_done[s]    MMA commit after O_s += P_s V_j             -> correction / epilogue
 // Every wait is bounded (see ptx.cuh); on a timeout the CTA records the
 // failing site in the status word, every role leaves its loop, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed.
@@ -91,7 +93,8 @@ struct Layout {
   static constexpr int bPFull = bSFull + 2;
   static constexpr int bODone = bPFull + 2;
   static constexpr int bCorrFull = bODone + 2;
-  static constexpr int bEpiFull = bCorrFull + 2;  // WG2: staging tile written (count 128)
+  static constexpr int bFinFull = bCorrFull + 2;  // final row_sum / reference posted (count 128)
+  static constexpr int bEpiFull = bFinFull + 2;  // WG2: staging tile written (count 128)
   static constexpr int bStageFree = bEpiFull + 1; // WG2: TMA store finished reading staging (count 1)
   static constexpr int bDrain = bStageFree + 1;   // MMA drain at exit
   static constexpr int kNumBars = bDrain + 1;
@@ -109,6 +112,7 @@ enum : unsigned int {
   kSiteCorrODone = 202,
   kSiteCorrEpiFull = 203,
   kSiteCorrStageFree = 204,
+  kSiteCorrFin = 205,
   kSiteMmaKv = 301,
   kSiteMmaQ = 302,
   kSiteMmaP = 303,
@@ -144,6 +148,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   const uint32_t bar_s = sbase + L::oBar + 8 * (L::bSFull + stage);
   const uint32_t bar_corr = sbase + L::oBar + 8 * (L::bCorrFull + stage);
   const uint32_t bar_p = sbase + L::oBar + 8 * (L::bPFull + stage);
+  const uint32_t bar_fin = sbase + L::oBar + 8 * (L::bFinFull + stage);
   float* mb_acc = mbox + (stage * 3 + 0) * 128;
   float* mb_sum = mbox + (stage * 3 + 1) * 128;
   float* mb_ref = mbox + (stage * 3 + 2) * 128;
@@ -188,15 +193,16 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
           if (c > lim) s[c] = -INFINITY;
       }
 
-      float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
+      // block maximum: three-input max, four independent chains
+      float m0 = fmaxf(s[0], s[1]), m1 = fmaxf(s[2], s[3]), m2 = fmaxf(s[4], s[5]), m3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        m0 = fmaxf(m0, s[c]);
-        m1 = fmaxf(m1, s[c + 1]);
-        m2 = fmaxf(m2, s[c + 2]);
-        m3 = fmaxf(m3, s[c + 3]);
+      for (int c = 8; c < 128; c += 8) {
+        m0 = fmax3(m0, s[c + 0], s[c + 1]);
+        m1 = fmax3(m1, s[c + 2], s[c + 3]);
+        m2 = fmax3(m2, s[c + 4], s[c + 5]);
+        m3 = fmax3(m3, s[c + 6], s[c + 7]);
       }
-      const float bmax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+      const float bmax = fmaxf(fmax3(m0, m1, m2), m3);
 
       // conditional rescaling: keep the reference unless the maximum grew by
       // more than tau (log2 units); the first visible block takes its own max
@@ -214,32 +220,48 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
       }
       ref = (row_max == -INFINITY) ? 0.f : row_max * sl2;
 
-      float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        s[c] = ex2_approx(fmaf(s[c], sl2, -ref));
-        s[c + 1] = ex2_approx(fmaf(s[c + 1], sl2, -ref));
-        l0 += s[c];
-        l1 += s[c + 1];
-      }
-      row_sum = row_sum * acc + (l0 + l1);
-
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-      tmem_st32(tS, pk);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[64 + 2 * i], s[64 + 2 * i + 1]);
-      tmem_st32(tS + 32, pk);
-      tmem_wait_st();
-
+      // post acc_scale now: the correction warps rescale O (when needed) while
+      // the exponentials below run, off the path to the PV MMA
       mb_acc[t] = acc;
-      if (j == n - 1) {
+      mbar_arrive(bar_corr);
+
+      // p = 2^(s * scale_log2 - ref): one packed FMA per pair, then ex2; the
+      // row sum is accumulated in packed pairs of fp32.  P goes to TMEM as
+      // packed bf16 pairs, 64 keys at a time.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t nrefx2 = f2_pack(-ref, -ref);
+      uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int c = 64 * half; c < 64 * half + 64; c += 4) {
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nrefx2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, nrefx2), x2, x3);
+          s[c] = ex2_approx(x0);
+          s[c + 1] = ex2_approx(x1);
+          s[c + 2] = ex2_approx(x2);
+          s[c + 3] = ex2_approx(x3);
+          sum_a = f2_add(sum_a, f2_pack(s[c], s[c + 1]));
+          sum_b = f2_add(sum_b, f2_pack(s[c + 2], s[c + 3]));
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
+        tmem_st32(tS + static_cast<uint32_t>(32 * half), pk);
+        tmem_wait_st();
+
+      }
+      float sa0, sa1;
+      f2_unpack(f2_add(sum_a, sum_b), sa0, sa1);
+      row_sum = row_sum * acc + (sa0 + sa1);
+
+      if (j == n - 1) {  // final statistics for the epilogue
         mb_sum[t] = row_sum;
         mb_ref[t] = ref;
+        mbar_arrive(bar_fin);
       }
       tc_fence_before();
-      mbar_arrive(bar_corr);
       if (!skip_p) mbar_arrive(bar_p);
     }
   }
@@ -259,6 +281,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   uint8_t* staging = smem + L::oStage;
   const uint32_t staging_s = sbase + L::oStage;
   uint32_t corr_phase[2] = {0u, 0u};
+  uint32_t fin_phase[2] = {0u, 0u};
   uint32_t pv_count[2] = {0u, 0u};  // PV MMAs of each stage released so far
   uint32_t chunks = 0;              // epilogue chunks stored so far
 
@@ -275,10 +298,6 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         if (!ok) goto out;
         corr_phase[s] ^= 1u;
         const float acc = mbox[(s * 3 + 0) * 128 + t];
-        if (j == tk.n[s] - 1) {
-          fin_sum[s] = mbox[(s * 3 + 1) * 128 + t];
-          fin_ref[s] = mbox[(s * 3 + 2) * 128 + t];
-        }
         // warp-uniform skip of the O round trip when no row moved its reference
         if (j > 0 && __any_sync(0xffffffffu, acc != 1.f)) {
           ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), (pv_count[s] - 1u) & 1u, wc,
@@ -295,6 +314,13 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
             tmem_st32(tO + c, r);
           }
           tmem_wait_st();
+        }
+        if (j == tk.n[s] - 1) {  // last block: the final row sum and reference
+          ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bFinFull + s), fin_phase[s], wc, kSiteCorrFin));
+          if (!ok) goto out;
+          fin_phase[s] ^= 1u;
+          fin_sum[s] = mbox[(s * 3 + 1) * 128 + t];
+          fin_ref[s] = mbox[(s * 3 + 2) * 128 + t];
         }
         tc_fence_before();
         mbar_arrive(bar0 + 8 * (L::bPFull + s));
@@ -382,29 +408,28 @@ out:
 // a 128-byte swizzled row; a new 16 KB chunk every 64 columns).  Descriptor
 // start addresses are in 16-byte units, so offsets are added to the low field.
 template <int DQ, int DV>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr, uint32_t leader) {
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128, false, false);
-  const uint64_t qd = smem_desc_sw128(q_addr, 16, 1024);
-  const uint64_t kd = smem_desc_sw128(k_addr, 16, 1024);
-#pragma unroll 1
-  for (int i = 0; i < DQ / 16; ++i) {
-    const uint32_t off = static_cast<uint32_t>((i >> 2) * (kChunkBytes >> 4) + (i & 3) * 2);
-    mma_ss(d_tmem, qd + off, kd + off, kIdesc, i != 0 ? 1u : 0u);
+#pragma unroll
+  for (int c = 0; c < DQ / 64; ++c) {
+    const uint32_t co = opaque_u32(static_cast<uint32_t>(c * kChunkBytes));
+    mma_ss_x4<2, 2>(d_tmem, smem_desc_sw128(q_addr + co, 16, 1024), smem_desc_sw128(k_addr + co, 16, 1024), kIdesc,
+                    c != 0 ? 1u : 0u, leader);
   }
 }
 
-// O (+)= P V: M = 128 rows, N = DV, K = 128 keys in steps of 16; P is read from
-// TMEM (8 columns of packed bf16 pairs per step), V from SMEM (MN-major: 16
-// key rows of 128 bytes per step; the second 64-column chunk is LBO away).
+// O (+)= P V for one half of the block (keys 64*half .. 64*half+63): M = 128
+// rows, N = DV, K in steps of 16; P is read from TMEM (8 columns of packed bf16
+// pairs per step), V from SMEM (MN-major: 16 key rows of 128 bytes per step;
+// the second 64-column chunk of V is LBO away).
 template <int DV>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, bool accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_addr, int half,
+                                              bool accumulate, uint32_t leader) {
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, DV, false, true);
-  const uint64_t vd = smem_desc_sw128(v_addr, kChunkBytes, 1024);
-#pragma unroll 1
-  for (int k = 0; k < kBN / 16; ++k) {
-    mma_ts(d_tmem, p_tmem + static_cast<uint32_t>(k * 8), vd + static_cast<uint32_t>(k * (16 * 128 >> 4)), kIdesc,
-           (accumulate || k > 0) ? 1u : 0u);
-  }
+  constexpr uint32_t kStep = 16 * 128 >> 4;  // 16 key rows, in 16-byte units
+  const uint32_t va = opaque_u32(v_addr + static_cast<uint32_t>(half * 64 * 128));
+  mma_ts_x4<kStep>(d_tmem, p_tmem + static_cast<uint32_t>(32 * half), smem_desc_sw128(va, kChunkBytes, 1024),
+                   kIdesc, accumulate ? 1u : 0u, leader);
 }
 
 template <int DQ, int DV>
@@ -418,6 +443,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   auto q_addr = [&](int s) { return sbase + L::oQ + static_cast<uint32_t>(s * L::kQBytes); };
   uint32_t q_phase[2] = {0u, 0u}, p_phase[2] = {0u, 0u};
   uint32_t kv_it = 0;  // K/V tiles consumed so far (ring order K0, V0, K1, V1, ...)
+  const uint32_t leader = (threadIdx.x & 31) == 0 ? 1u : 0u;  // the lane that issues MMAs and commits
+  // every lane waits; a timeout seen by any lane ends the role for the whole warp
+  auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
+    return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
+  };
 
   for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
     const Task tk = decode_task(pr, task);
@@ -426,57 +456,59 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
     // prologue: S_s = Q_s K_0^T for both stages
     {
       const uint32_t slot = kv_it % L::NS;
-      if (!mbar_wait(bar(L::bKvFull + slot), (kv_it / L::NS) & 1u, wc, kSiteMmaKv)) goto out;
+      if (!wait(bar(L::bKvFull + slot), (kv_it / L::NS) & 1u, kSiteMmaKv)) goto out;
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (tk.n[s] == 0) continue;
-        if (!mbar_wait(bar(L::bQFull + s), q_phase[s], wc, kSiteMmaQ)) goto out;
+        if (!wait(bar(L::bQFull + s), q_phase[s], kSiteMmaQ)) goto out;
         q_phase[s] ^= 1u;
         tc_fence_after();
-        issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(kv_it));
-        mma_commit(bar(L::bSFull + s));
-        if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s));
+        issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(kv_it), leader);
+        mma_commit(bar(L::bSFull + s), leader);
+        if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
       }
-      mma_commit(bar(L::bKvEmpty + slot));
+      mma_commit(bar(L::bKvEmpty + slot), leader);
       ++kv_it;
     }
 
     for (int j = 0; j < tk.nmax; ++j) {
       const uint32_t v_it = kv_it;
       const uint32_t vslot = v_it % L::NS;
-      if (!mbar_wait(bar(L::bKvFull + vslot), (v_it / L::NS) & 1u, wc, kSiteMmaKv)) goto out;
+      if (!wait(bar(L::bKvFull + vslot), (v_it / L::NS) & 1u, kSiteMmaKv)) goto out;
       const uint32_t k_it = kv_it + 1;  // K_{j+1}
       bool k_ready = false;
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (j >= tk.n[s]) continue;
-        if (!mbar_wait(bar(L::bPFull + s), p_phase[s], wc, kSiteMmaP)) goto out;
+        if (!wait(bar(L::bPFull + s), p_phase[s], kSiteMmaP)) goto out;
         p_phase[s] ^= 1u;
         tc_fence_after();
-        issue_pv<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
-                     slot_addr(v_it), j > 0);
-        mma_commit(bar(L::bODone + s));
+        issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
+                          slot_addr(v_it), 0, j > 0, leader);
+        issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
+                          slot_addr(v_it), 1, true, leader);
+        mma_commit(bar(L::bODone + s), leader);
         if (j + 1 < tk.n[s]) {
           if (!k_ready) {
-            if (!mbar_wait(bar(L::bKvFull + k_it % L::NS), (k_it / L::NS) & 1u, wc, kSiteMmaKv)) goto out;
+            if (!wait(bar(L::bKvFull + k_it % L::NS), (k_it / L::NS) & 1u, kSiteMmaKv)) goto out;
             k_ready = true;
           }
-          issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(k_it));
-          mma_commit(bar(L::bSFull + s));
-          if (j + 2 == tk.n[s]) mma_commit(bar(L::bQEmpty + s));
+          issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(k_it), leader);
+          mma_commit(bar(L::bSFull + s), leader);
+          if (j + 2 == tk.n[s]) mma_commit(bar(L::bQEmpty + s), leader);
         }
       }
-      mma_commit(bar(L::bKvEmpty + vslot));
+      mma_commit(bar(L::bKvEmpty + vslot), leader);
       ++kv_it;
       if (j + 1 < tk.nmax) {
-        mma_commit(bar(L::bKvEmpty + k_it % L::NS));
+        mma_commit(bar(L::bKvEmpty + k_it % L::NS), leader);
         ++kv_it;
       }
     }
   }
 out:
-  // every MMA issued by this thread has completed once the drain barrier fires
-  mma_commit(bar(L::bDrain));
+  // every MMA issued by the leader lane has completed once the drain barrier fires
+  mma_commit(bar(L::bDrain), leader);
   mbar_drain_wait(bar(L::bDrain), 0u, wc, kSiteMmaDrain);
 }
 
@@ -565,6 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(b + 8 * (L::bPFull + s), 256);
       mbar_init(b + 8 * (L::bODone + s), 1);
       mbar_init(b + 8 * (L::bCorrFull + s), 128);
+      mbar_init(b + 8 * (L::bFinFull + s), 128);
     }
     for (int i = 0; i < L::NS; ++i) {
       mbar_init(b + 8 * (L::bKvFull + i), 1);
@@ -596,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   } else {
     setmaxnreg_dec<56>();
     if (warp == 12) {
-      if (lane == 0) mma_role<DQ, DV>(p, tmem, sbase, wc);
+      mma_role<DQ, DV>(p, tmem, sbase, wc);
       __syncwarp();
     } else if (warp == 13) {
       if (lane == 0) load_role<DQ, DV>(p, sbase, wc);
