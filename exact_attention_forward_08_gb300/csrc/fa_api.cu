@@ -96,8 +96,8 @@ int init_device(int dev, DeviceState** out) {
 }
 
 // Per device and kernel: allow the large dynamic shared memory and check the
-// register count the warp-role split assumes (128 per thread at launch; the
-// roles then move registers with setmaxnreg, whose total must match).
+// register count the warp-role split assumes (the roles move registers with
+// setmaxnreg; their total must fit what the CTA is launched with).
 int prepare_kernel(DeviceState* st, int idx, const fa::KernelEntry& e) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (st->kernel_ready[idx]) return FA_OK;
@@ -106,7 +106,9 @@ int prepare_kernel(DeviceState* st, int idx, const fa::KernelEntry& e) {
     return FA_ERR_CUDA;
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, e.fn) != cudaSuccess) return FA_ERR_CUDA;
-  if (attr.numRegs != 128 || attr.maxThreadsPerBlock < fa::kThreads) return FA_ERR_UNSUPPORTED;
+  // setmaxnreg.inc would wait forever if the launch left fewer registers than the split needs
+  if (attr.numRegs * fa::kThreads < fa::kRegBudgetPerCta || attr.maxThreadsPerBlock < fa::kThreads)
+    return FA_ERR_UNSUPPORTED;
   st->kernel_ready[idx] = true;
   return FA_OK;
 }

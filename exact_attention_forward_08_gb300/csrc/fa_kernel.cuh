@@ -29,7 +29,8 @@
 //                posted for the epilogue                     -> correction
 //   p_full[s]    count 256: 128 softmax threads (P written) +
 //                128 correction threads (O rescaled or not)  -> PV MMA
-//   o_done[s]    MMA commit after O_s += P_s V_j             -> correction / epilogue
+//   o_done[s]    MMA commit after the stage's last P V of a
+//                task                                        -> epilogue
 // Every wait is bounded (see ptx.cuh); on a timeout the CTA records the
 // failing site in the status word, every role leaves its loop, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed.
@@ -42,6 +43,8 @@
 namespace fa {
 
 constexpr int kThreads = 512;
+// registers the setmaxnreg split needs: 128 x (176 + 176 + 104 + 56)
+constexpr int kRegBudgetPerCta = 128 * (176 + 176 + 104 + 56);
 constexpr int kChunkBytes = 128 * 64 * 2;  // 128 rows x 64 bf16: one 128B-swizzled TMA box
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.693147180559945309417f;
@@ -282,7 +285,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   const uint32_t staging_s = sbase + L::oStage;
   uint32_t corr_phase[2] = {0u, 0u};
   uint32_t fin_phase[2] = {0u, 0u};
-  uint32_t pv_count[2] = {0u, 0u};  // PV MMAs of each stage released so far
+  uint32_t od_count[2] = {0u, 0u};  // o_done phases consumed (one per task with blocks)
   uint32_t chunks = 0;              // epilogue chunks stored so far
 
   for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
@@ -298,11 +301,10 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         if (!ok) goto out;
         corr_phase[s] ^= 1u;
         const float acc = mbox[(s * 3 + 0) * 128 + t];
-        // warp-uniform skip of the O round trip when no row moved its reference
+        // warp-uniform skip of the O round trip when no row moved its
+        // reference.  The softmax posted acc_scale after S_j was ready, and S_j
+        // ready implies that P V_{j-1} completed, so O is final here.
         if (j > 0 && __any_sync(0xffffffffu, acc != 1.f)) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), (pv_count[s] - 1u) & 1u, wc,
-                                                 kSiteCorrODone));
-          if (!ok) goto out;
           tc_fence_after();
           const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(s * 128);
 #pragma unroll
@@ -324,7 +326,6 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         }
         tc_fence_before();
         mbar_arrive(bar0 + 8 * (L::bPFull + s));
-        ++pv_count[s];
       }
     }
 
@@ -334,10 +335,11 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
       const int pos0 = tk.pos0[s];
       if (pos0 >= pr.Sq) continue;  // tile past the end of the sequence
       const bool has = tk.n[s] > 0;
-      if (has) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), (pv_count[s] - 1u) & 1u,
-                                                          wc, kSiteCorrODone));
+      if (has) {  // o_done completes once per task: after the stage's last P V
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), od_count[s] & 1u, wc, kSiteCorrODone));
         if (!ok) goto out;
+        ++od_count[s];
         tc_fence_after();
       }
       float inv = 0.f, lse = -INFINITY;
@@ -432,6 +434,11 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
                    kIdesc, accumulate ? 1u : 0u, leader);
 }
 
+// K/V tiles are consumed in the order K0, V0, K1, V1, ...; a task starting
+// at ring tile `base` has K_j at base + 2j and V_j at base + 2j + 1.
+// o_done[s] is committed once per task, after the stage's last P V: inside a
+// task, "S_j ready" already implies that P V_{j-1} has completed (a commit
+// tracks every earlier MMA of the issuing thread).
 template <int DQ, int DV>
 __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                          const WaitCtx& wc) {
@@ -442,40 +449,42 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   auto slot_addr = [&](uint32_t it) { return sbase + L::oRing + (it % L::NS) * L::kSlotBytes; };
   auto q_addr = [&](int s) { return sbase + L::oQ + static_cast<uint32_t>(s * L::kQBytes); };
   uint32_t q_phase[2] = {0u, 0u}, p_phase[2] = {0u, 0u};
-  uint32_t kv_it = 0;  // K/V tiles consumed so far (ring order K0, V0, K1, V1, ...)
+  uint32_t kv_it = 0;  // first ring tile of the current task
   const uint32_t leader = (threadIdx.x & 31) == 0 ? 1u : 0u;  // the lane that issues MMAs and commits
   // every lane waits; a timeout seen by any lane ends the role for the whole warp
   auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
   };
+  // full / empty barriers of ring tile `it`
+  auto wait_tile = [&](uint32_t it) {
+    return wait(bar(L::bKvFull + static_cast<int>(it % L::NS)), (it / L::NS) & 1u, kSiteMmaKv);
+  };
+  auto release_tile = [&](uint32_t it) { mma_commit(bar(L::bKvEmpty + static_cast<int>(it % L::NS)), leader); };
 
   for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
     const Task tk = decode_task(pr, task);
+    const uint32_t base = kv_it;
+    kv_it += 2u * static_cast<uint32_t>(tk.nmax);
     if (tk.nmax == 0) continue;
 
     // prologue: S_s = Q_s K_0^T for both stages
-    {
-      const uint32_t slot = kv_it % L::NS;
-      if (!wait(bar(L::bKvFull + slot), (kv_it / L::NS) & 1u, kSiteMmaKv)) goto out;
+    if (!wait_tile(base)) goto out;
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        if (tk.n[s] == 0) continue;
-        if (!wait(bar(L::bQFull + s), q_phase[s], kSiteMmaQ)) goto out;
-        q_phase[s] ^= 1u;
-        tc_fence_after();
-        issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(kv_it), leader);
-        mma_commit(bar(L::bSFull + s), leader);
-        if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
-      }
-      mma_commit(bar(L::bKvEmpty + slot), leader);
-      ++kv_it;
+    for (int s = 0; s < 2; ++s) {
+      if (tk.n[s] == 0) continue;
+      if (!wait(bar(L::bQFull + s), q_phase[s], kSiteMmaQ)) goto out;
+      q_phase[s] ^= 1u;
+      tc_fence_after();
+      issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(base), leader);
+      mma_commit(bar(L::bSFull + s), leader);
+      if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
     }
+    release_tile(base);  // K_0, once both Q K^T have finished
 
     for (int j = 0; j < tk.nmax; ++j) {
-      const uint32_t v_it = kv_it;
-      const uint32_t vslot = v_it % L::NS;
-      if (!wait(bar(L::bKvFull + vslot), (v_it / L::NS) & 1u, kSiteMmaKv)) goto out;
-      const uint32_t k_it = kv_it + 1;  // K_{j+1}
+      const uint32_t v_it = base + 2u * static_cast<uint32_t>(j) + 1u;
+      const uint32_t k_it = v_it + 1u;  // K_{j+1}
+      if (!wait_tile(v_it)) goto out;
       bool k_ready = false;
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
@@ -487,10 +496,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
                           slot_addr(v_it), 0, j > 0, leader);
         issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
                           slot_addr(v_it), 1, true, leader);
-        mma_commit(bar(L::bODone + s), leader);
+        if (j + 1 == tk.n[s]) mma_commit(bar(L::bODone + s), leader);
         if (j + 1 < tk.n[s]) {
           if (!k_ready) {
-            if (!wait(bar(L::bKvFull + k_it % L::NS), (k_it / L::NS) & 1u, kSiteMmaKv)) goto out;
+            if (!wait_tile(k_it)) goto out;
             k_ready = true;
           }
           issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(k_it), leader);
@@ -498,12 +507,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
           if (j + 2 == tk.n[s]) mma_commit(bar(L::bQEmpty + s), leader);
         }
       }
-      mma_commit(bar(L::bKvEmpty + vslot), leader);
-      ++kv_it;
-      if (j + 1 < tk.nmax) {
-        mma_commit(bar(L::bKvEmpty + k_it % L::NS), leader);
-        ++kv_it;
-      }
+      // V_j, and K_{j+1} once its Q K^T have finished
+      release_tile(v_it);
+      if (j + 1 < tk.nmax) release_tile(k_it);
     }
   }
 out:
@@ -547,9 +553,9 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
       for (int which = 0; which < 2; ++which) {  // K_j then V_j
         const uint32_t slot = kv_it % L::NS;
         if (kv_it >= static_cast<uint32_t>(L::NS) &&
-            !mbar_wait(bar(L::bKvEmpty + slot), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
+            !mbar_wait(bar(L::bKvEmpty + static_cast<int>(slot)), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
           goto out;
-        const uint32_t fb = bar(L::bKvFull + slot);
+        const uint32_t fb = bar(L::bKvFull + static_cast<int>(slot));
         const uint32_t dst = sbase + L::oRing + slot * L::kSlotBytes;
         const int nch = which == 0 ? L::NQC : L::NVC;
         mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nch * kChunkBytes));
@@ -567,7 +573,7 @@ out:
     if (q_uses[s] > 0) mbar_drain_wait(bar(L::bQFull + s), (q_uses[s] - 1u) & 1u, wc, kSiteLoadDrain);
   for (uint32_t i = 0; i < static_cast<uint32_t>(L::NS) && i < kv_it; ++i) {
     const uint32_t uses = (kv_it - i + L::NS - 1) / L::NS;  // copies issued into slot i
-    mbar_drain_wait(bar(L::bKvFull + i), (uses - 1u) & 1u, wc, kSiteLoadDrain);
+    mbar_drain_wait(bar(L::bKvFull + static_cast<int>(i)), (uses - 1u) & 1u, wc, kSiteLoadDrain);
   }
 }
 
