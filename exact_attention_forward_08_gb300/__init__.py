@@ -20,7 +20,7 @@ import os
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_status_string", "fa_make_plan", "fa_plan_task",
+__all__ = ["fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan", "fa_plan_task",
            "fa_plan_block_masked", "fa_version", "FaOptions", "FaPlan", "FaTask", "attention_forward",
            "FaError", "load_library", "LIB_PATH", "STATUS"]
 
@@ -38,7 +38,7 @@ class FaError(RuntimeError):
 
 class FaOptions(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("pack", ctypes.c_int), ("grid", ctypes.c_int),
-                ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int)]
+                ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int), ("exp_emu", ctypes.c_int)]
 
 
 class FaPlan(ctypes.Structure):
@@ -86,6 +86,8 @@ def load_library(path: str | None = None):
     lib.fa_plan_task.restype = _I
     lib.fa_plan_block_masked.argtypes = [ctypes.POINTER(FaPlan), _I, _I]
     lib.fa_plan_block_masked.restype = _I
+    lib.fa_selftest_exp2.argtypes = [_P, _P, _P, _I, _P]
+    lib.fa_selftest_exp2.restype = _I
     if path is None:
         _lib = lib
     return lib
@@ -123,6 +125,11 @@ def fa_device_status(stream=None):
     if rc != FA_OK:
         raise FaError(rc, "fa_device_status")
     return out.value, tuple(detail)
+
+
+def fa_selftest_exp2(x, y_fma, y_mufu, n, stream) -> int:
+    """``fa_selftest_exp2``: device pointers as integers."""
+    return load_library().fa_selftest_exp2(x, y_fma, y_mufu, n, stream)
 
 
 def fa_status_string(code: int) -> str:

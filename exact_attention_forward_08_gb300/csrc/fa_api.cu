@@ -20,7 +20,7 @@ __device__ unsigned int g_fa_status[4];
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumKernels = 10;  // 5 (d_qk, d_v) pairs x {non-causal, causal}
+constexpr int kNumKernels = 20;  // 5 (d_qk, d_v) pairs x {non-causal, causal} x {MUFU, FMA-emulated exp}
 
 struct DeviceState {
   bool ready = false;
@@ -35,20 +35,20 @@ std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-int kernel_index(int dq, int dv, int causal) {
+int kernel_index(int dq, int dv, int causal, int emu) {
   int pair = -1;
   if (dq == 64 && dv == 64) pair = 0;
   if (dq == 128 && dv == 64) pair = 1;
   if (dq == 128 && dv == 128) pair = 2;
   if (dq == 192 && dv == 64) pair = 3;
   if (dq == 192 && dv == 128) pair = 4;
-  return pair < 0 ? -1 : pair * 2 + (causal ? 1 : 0);
+  return pair < 0 ? -1 : pair * 4 + (causal ? 2 : 0) + (emu ? 1 : 0);
 }
 
-bool get_entry(int dq, int dv, int causal, fa::KernelEntry* e) {
-  if (dq == 64) return fa::entry_d64(dv, causal, e);
-  if (dq == 128) return fa::entry_d128(dv, causal, e);
-  if (dq == 192) return fa::entry_d192(dv, causal, e);
+bool get_entry(int dq, int dv, int causal, int emu, fa::KernelEntry* e) {
+  if (dq == 64) return fa::entry_d64(dv, causal, emu, e);
+  if (dq == 128) return fa::entry_d128(dv, causal, emu, e);
+  if (dq == 192) return fa::entry_d192(dv, causal, emu, e);
   return false;
 }
 
@@ -145,6 +145,22 @@ int encode_kv(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
   return encode(m, base, 4, dims, strides, box);
 }
 
+// Test hook: y_fma[i] = the FMA-pipe 2^x above, y_mufu[i] = ex2.approx, for
+// comparing the two on the device.
+__global__ void exp2_selftest_kernel(const float* x, float* y_fma, float* y_mufu, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float a = x[i], b = (i + 1 < n) ? x[i + 1] : 0.f;
+  float ya, yb;
+  fa::ex2_fma_x2(fa::f2_pack(a, b), ya, yb);
+  y_fma[i] = ya;
+  y_mufu[i] = fa::ex2_approx(a);
+  if (i + 1 < n) {
+    y_fma[i + 1] = yb;
+    y_mufu[i + 1] = fa::ex2_approx(b);
+  }
+}
+
 __global__ void fill_f32(float* p, int64_t n, float v) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -156,8 +172,9 @@ int validate(const void* q, const void* k, const void* v, void* o, const float* 
   if (batch < 0 || seqlen_q < 0 || seqlen_k < 0 || heads_q < 1 || heads_kv < 1) return FA_ERR_INVALID_ARG;
   if (heads_q % heads_kv != 0) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale)) || scale < 0.f) return FA_ERR_INVALID_ARG;
-  if (kernel_index(d_qk, d_v, 0) < 0) return FA_ERR_UNSUPPORTED;
+  if (kernel_index(d_qk, d_v, 0, 0) < 0) return FA_ERR_UNSUPPORTED;
   if (opt.pack < 0 || opt.grid < 0 || (opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
+  if (opt.exp_emu != 0 && opt.exp_emu != 1) return FA_ERR_INVALID_ARG;
   // the kept reference may lag the row maximum by up to tau (log2 units), so
   // unnormalised weights reach 2^tau: keep them far inside the fp32 range
   if (!(opt.tau >= 0.f && opt.tau <= 64.f)) return FA_ERR_INVALID_ARG;
@@ -187,6 +204,7 @@ void fa_options_default(fa_options* opts) {
   opts->grid = 0;
   opts->timeout_s = 1.0;
   opts->debug_flags = 0;
+  opts->exp_emu = 0;
 }
 
 int fa_version(void) { return 100; }
@@ -244,9 +262,9 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     return FA_OK;
   }
 
-  const int idx = kernel_index(d_qk, d_v, causal);
+  const int idx = kernel_index(d_qk, d_v, causal, opt.exp_emu);
   fa::KernelEntry entry;
-  if (idx < 0 || !get_entry(d_qk, d_v, causal, &entry)) return FA_ERR_UNSUPPORTED;
+  if (idx < 0 || !get_entry(d_qk, d_v, causal, opt.exp_emu, &entry)) return FA_ERR_UNSUPPORTED;
   rc = prepare_kernel(st, idx, entry);
   if (rc != FA_OK) return rc;
 
@@ -300,12 +318,26 @@ int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]) {
   return FA_OK;
 }
 
+int fa_selftest_exp2(const float* x, float* y_fma, float* y_mufu, int n, fa_stream_t stream) {
+  if (n < 0 || (n > 0 && (x == nullptr || y_fma == nullptr || y_mufu == nullptr))) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* st = nullptr;
+  const int rc = init_device(dev, &st);
+  if (rc != FA_OK) return rc;
+  if (!is_device_ptr(x, dev) || !is_device_ptr(y_fma, dev) || !is_device_ptr(y_mufu, dev)) return FA_ERR_INVALID_ARG;
+  const int pairs = (n + 1) / 2;
+  exp2_selftest_kernel<<<(pairs + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y_fma, y_mufu, n);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal,
                  int64_t l2_bytes, int pack, fa_plan* out) {
   if (out == nullptr) return FA_ERR_INVALID_ARG;
   if (batch < 0 || seqlen_q < 0 || seqlen_k < 0 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv)
     return FA_ERR_INVALID_ARG;
-  if (kernel_index(d_qk, d_v, 0) < 0) return FA_ERR_UNSUPPORTED;
+  if (kernel_index(d_qk, d_v, 0, 0) < 0) return FA_ERR_UNSUPPORTED;
   if (pack < 0 || (pack > 0 && (fa::kBM % pack != 0 || (heads_q / heads_kv) % pack != 0))) return FA_ERR_INVALID_ARG;
   if (l2_bytes <= 0) l2_bytes = int64_t(64) << 20;
   const fa::Problem p =

@@ -3,13 +3,13 @@
 
 namespace fa {
 
-bool entry_d192(int dv, int causal, KernelEntry* out) {
+bool entry_d192(int dv, int causal, int emu, KernelEntry* out) {
   if (dv == 64) {
-    *out = causal ? make_entry<192, 64, true>() : make_entry<192, 64, false>();
+    *out = pick_entry<192, 64>(causal, emu);
     return true;
   }
   if (dv == 128) {
-    *out = causal ? make_entry<192, 128, true>() : make_entry<192, 128, false>();
+    *out = pick_entry<192, 128>(causal, emu);
     return true;
   }
   return false;

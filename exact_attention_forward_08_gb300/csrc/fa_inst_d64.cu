@@ -3,9 +3,9 @@
 
 namespace fa {
 
-bool entry_d64(int dv, int causal, KernelEntry* out) {
+bool entry_d64(int dv, int causal, int emu, KernelEntry* out) {
   if (dv == 64) {
-    *out = causal ? make_entry<64, 64, true>() : make_entry<64, 64, false>();
+    *out = pick_entry<64, 64>(causal, emu);
     return true;
   }
   return false;

@@ -37,6 +37,8 @@
 #pragma once
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "fa_schedule.h"
 #include "ptx.cuh"
 
@@ -139,9 +141,43 @@ __device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, c
 }
 
 // ---------------------------------------------------------------------------
+// 2^x on the FMA pipe ("FlashAttention-4 wiki", "Core methods": Cody-Waite
+// range reduction and a degree-3 Horner polynomial, the integer part added to
+// the exponent field).  x = j + f with j = rint(x) (adding 1.5 * 2^23 rounds
+// to an integer and leaves j in the low mantissa bits), f in [-1/2, 1/2];
+// 2^f from a polynomial fitted by exp2_poly.py (max relative error 7.5e-5,
+// below half a bf16 unit).  x is clamped at -126 so the exponent sum stays in
+// range; only unmasked blocks use it (a masked key must give exactly 0).
+// ---------------------------------------------------------------------------
+constexpr float kExp2C0 = 0.99992806f;
+constexpr float kExp2C1 = 0.69326097f;
+constexpr float kExp2C2 = 0.24261114f;
+constexpr float kExp2C3 = 0.055171628f;
+
+__device__ __forceinline__ void ex2_fma_x2(uint64_t x2, float& y0, float& y1) {
+  float a, b;
+  f2_unpack(x2, a, b);
+  const uint64_t xc = f2_pack(fmaxf(a, -126.f), fmaxf(b, -126.f));
+  const uint64_t t = f2_add(xc, f2_pack(12582912.f, 12582912.f));    // 1.5 * 2^23 + rint(x)
+  const uint64_t jf = f2_add(t, f2_pack(-12582912.f, -12582912.f));  // rint(x)
+  const uint64_t f = f2_fma(jf, f2_pack(-1.f, -1.f), xc);            // x - rint(x)
+  uint64_t q = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+  q = f2_fma(q, f, f2_pack(kExp2C1, kExp2C1));
+  q = f2_fma(q, f, f2_pack(kExp2C0, kExp2C0));
+  float t0, t1, q0, q1;
+  f2_unpack(t, t0, t1);
+  f2_unpack(q, q0, q1);
+  // the low bits of t hold rint(x); shifted by 23 they add to the exponent
+  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+}
+
+// ---------------------------------------------------------------------------
 // softmax (WG0 / WG1)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL>
+// EMU: one in four exponentials of unmasked blocks on the FMA pipe (an option;
+// its own instantiation, so the default kernel carries no extra code)
+template <int DQ, int DV, bool CAUSAL, bool EMU>
 __device__ __forceinline__ void softmax_role(const Params& p, const int stage, const uint32_t tmem,
                                              const uint32_t sbase, float* mbox, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
@@ -187,7 +223,8 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
 
-      if (block_needs_mask(pr, pos0, j)) {
+      const bool masked_block = block_needs_mask(pr, pos0, j);
+      if (masked_block) {
         // columns c <= lim are visible
         int64_t lim64 = last_key - static_cast<int64_t>(j) * kBN;
         const int lim = lim64 < -1 ? -1 : (lim64 > 127 ? 127 : static_cast<int>(lim64));
@@ -234,27 +271,40 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t nrefx2 = f2_pack(-ref, -ref);
       uint64_t sum_a = f2_pack(0.f, 0.f), sum_b = sum_a;
+      auto exps = [&](auto emu_tag) {
+        constexpr bool kFma = decltype(emu_tag)::value;  // one pair in four on the FMA pipe
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
-        for (int c = 64 * half; c < 64 * half + 64; c += 4) {
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nrefx2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, nrefx2), x2, x3);
-          s[c] = ex2_approx(x0);
-          s[c + 1] = ex2_approx(x1);
-          s[c + 2] = ex2_approx(x2);
-          s[c + 3] = ex2_approx(x3);
-          sum_a = f2_add(sum_a, f2_pack(s[c], s[c + 1]));
-          sum_b = f2_add(sum_b, f2_pack(s[c + 2], s[c + 3]));
+          for (int c = 64 * half; c < 64 * half + 64; c += 4) {
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nrefx2), x0, x1);
+            s[c] = ex2_approx(x0);
+            s[c + 1] = ex2_approx(x1);
+            const uint64_t xb = f2_fma(f2_pack(s[c + 2], s[c + 3]), sl2x2, nrefx2);
+            if (kFma && (c & 4)) {
+              ex2_fma_x2(xb, s[c + 2], s[c + 3]);
+            } else {
+              f2_unpack(xb, x2, x3);
+              s[c + 2] = ex2_approx(x2);
+              s[c + 3] = ex2_approx(x3);
+            }
+            sum_a = f2_add(sum_a, f2_pack(s[c], s[c + 1]));
+            sum_b = f2_add(sum_b, f2_pack(s[c + 2], s[c + 3]));
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
+          tmem_st32(tS + static_cast<uint32_t>(32 * half), pk);
         }
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]);
-        tmem_st32(tS + static_cast<uint32_t>(32 * half), pk);
-        tmem_wait_st();
-
+      };
+      if constexpr (EMU) {
+        if (!masked_block) exps(std::true_type{});
+        else exps(std::false_type{});
+      } else {
+        exps(std::false_type{});
       }
+      tmem_wait_st();
       float sa0, sa1;
       f2_unpack(f2_add(sum_a, sum_b), sa0, sa1);
       row_sum = row_sum * acc + (sa0 + sa1);
@@ -580,7 +630,7 @@ out:
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL>
+template <int DQ, int DV, bool CAUSAL, bool EMU>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = Layout<DQ, DV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -628,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   // register budget: 128 x (176 + 176 + 104 + 56) = 65536
   if (warp < 8) {
     setmaxnreg_inc<176>();
-    softmax_role<DQ, DV, CAUSAL>(p, warp >> 2, tmem, sbase, mbox, wc);
+    softmax_role<DQ, DV, CAUSAL, EMU>(p, warp >> 2, tmem, sbase, mbox, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
     correction_role<DQ, DV, CAUSAL>(p, tmem, sbase, smem, mbox, wc);

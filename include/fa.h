@@ -94,6 +94,10 @@ typedef struct fa_options {
   int debug_flags;    /* bit 0: the softmax warps never signal P ready, so the MMA warp's
                          bounded wait expires (tests the failure path; the output is not
                          valid).  Other bits must be 0. */
+  int exp_emu;        /* 1: compute one in four exponentials of unmasked blocks on the FMA
+                         pipe with a degree-3 polynomial instead of the MUFU ex2 unit
+                         ("FlashAttention-4 wiki", "Core methods": partial exp emulation);
+                         0 (default): MUFU only.  Any other value is rejected. */
 } fa_options;
 
 /* Fill `opts` with the defaults. */
@@ -103,6 +107,13 @@ void fa_options_default(fa_options* opts);
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
               int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
               const fa_options* opts, fa_stream_t stream);
+
+/*
+ * Test hook for the emulated exponential: for i < n, y_fma[i] = 2^x[i] by the
+ * FMA-pipe polynomial used with exp_emu = 1, y_mufu[i] = the hardware ex2
+ * (ex2.approx.ftz).  Device pointers, fp32; stream-ordered.
+ */
+int fa_selftest_exp2(const float* x, float* y_fma, float* y_mufu, int n, fa_stream_t stream);
 
 /*
  * Synchronise `stream`, then read and clear the current device's status

@@ -31,7 +31,8 @@ def _declared_functions():
 def test_header_declares_entry_points():
     names = _declared_functions()
     for required in ("fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_status_string", "fa_make_plan",
-                     "fa_plan_task", "fa_options_default", "fa_version", "fa_plan_block_masked"):
+                     "fa_plan_task", "fa_options_default", "fa_version", "fa_plan_block_masked",
+                     "fa_selftest_exp2"):
         assert required in names
 
 
@@ -81,7 +82,8 @@ def test_bad_options_rejected(fa):
     opts = fa.default_options()
     assert abs(opts.tau - 8.0) < 1e-7 and opts.pack == 0 and opts.grid == 0
     for field, value in (("pack", 3), ("pack", -1), ("grid", -2), ("debug_flags", 2), ("timeout_s", 1e9), ("tau", 65.0),
-                         ("tau", float("inf")), ("tau", float("nan"))):
+                         ("tau", float("inf")), ("tau", float("nan")), ("exp_emu", 2),
+                         ("exp_emu", -1)):
         o = fa.default_options()
         setattr(o, field, value)
         rc = fa.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 64, 128, 128, 0, 0.0, o, None)

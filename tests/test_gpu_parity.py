@@ -234,3 +234,31 @@ def test_bench_config_sampled(fa, name):
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
     vmax = float(np.abs(synthetic.bf16_bits_to_f32(v)).max())
     assert float(o.float().abs().max()) <= vmax * (1 + 2 ** -7)
+
+
+# ---------------------------------------------------------------------------
+# the optional FMA-pipe exponential
+# ---------------------------------------------------------------------------
+
+def test_exp2_fma_path_matches_mufu(fa):
+    x = torch.linspace(-126.0, 8.0, 1 << 20, device="cuda", dtype=torch.float32)
+    y_fma = torch.empty_like(x)
+    y_mufu = torch.empty_like(x)
+    assert fa.fa_selftest_exp2(x.data_ptr(), y_fma.data_ptr(), y_mufu.data_ptr(), x.numel(),
+                               torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    bf = lambda t: t.to(torch.bfloat16).view(torch.int16).to(torch.int32)
+    d = (bf(y_fma) - bf(y_mufu)).abs()
+    normal = x > -125.0  # ex2.approx.ftz flushes the subnormal results to zero
+    assert int(d[normal].max()) <= 1
+    assert float((d[normal] <= 1).float().mean()) >= 0.99
+
+
+@pytest.mark.parametrize("case", ["mha", "asym", "causal"])
+def test_exp2_fma_path_parity(fa, case):
+    w = {"mha": synthetic.Workload("emu_mha", 1, 4, 4, 600, 600, 128, 128, False, seed=71),
+         "asym": synthetic.Workload("emu_asym", 1, 4, 4, 700, 700, 192, 128, True, seed=72, q_mul=4.0, k_offset=12.0),
+         "causal": synthetic.Workload("emu_causal", 2, 8, 2, 520, 520, 64, 64, True, seed=73)}[case]
+    opts = fa.default_options()
+    opts.exp_emu = 1
+    full_check(fa, w, options=opts)
