@@ -7,10 +7,12 @@ library is missing or a call fails, an exception is raised.
 
     from exact_attention_forward_08_gb300 import attention_forward
     o, lse = attention_forward(q, k, v, causal=True)   # q [B,Sq,Hq,d] bf16 on cuda
+    o, lse = attention_forward_varlen(q, k, v, cu_q, cu_k)  # q [total_q,Hq,d], cu_q int32 [B+1]
 
-Raw entry points with the C names: ``fa_fwd``, ``fa_fwd_ex``,
-``fa_device_status``, ``fa_status_string``, ``fa_make_plan``,
-``fa_plan_task``, ``fa_plan_block_masked``, ``fa_version``.
+Raw entry points with the C names: ``fa_fwd``, ``fa_fwd_ex``, ``fa_fwd_varlen``,
+``fa_fwd_varlen_ex``, ``fa_varlen_workspace_size``, ``fa_varlen_plan_host``,
+``fa_device_status``, ``fa_status_string``, ``fa_make_plan``, ``fa_plan_task``,
+``fa_plan_block_masked``, ``fa_plan_first_masked_block``, ``fa_version``.
 """
 from __future__ import annotations
 
@@ -20,9 +22,11 @@ import os
 
 from . import _build
 
-__all__ = ["fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan", "fa_plan_task",
-           "fa_plan_block_masked", "fa_version", "FaOptions", "FaPlan", "FaTask", "attention_forward",
-           "FaError", "load_library", "LIB_PATH", "STATUS"]
+__all__ = ["fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_varlen_ex", "fa_varlen_workspace_size",
+           "fa_varlen_plan_host", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
+           "fa_plan_task", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
+           "FaTask", "FaVarlenTask", "attention_forward", "attention_forward_varlen", "FaError", "load_library",
+           "LIB_PATH", "STATUS", "VARLEN_HEADER_BYTES"]
 
 LIB_PATH = _build.LIB
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
@@ -38,19 +42,32 @@ class FaError(RuntimeError):
 
 class FaOptions(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("pack", ctypes.c_int), ("grid", ctypes.c_int),
-                ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int), ("exp_emu", ctypes.c_int)]
+                ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int), ("exp_emu", ctypes.c_int),
+                ("workspace", ctypes.c_void_p)]
+
+
+# bytes of the optional fixed-length scheduling workspace (fa_options.workspace)
+SCHED_WORKSPACE_BYTES = 16
 
 
 class FaPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("batch", "heads_q", "heads_kv", "seqlen_q", "seqlen_k", "causal",
                                             "pack", "groups", "pos_per_tile", "tiles", "mblocks", "kv_blocks",
-                                            "ratio", "section_units")] + [("num_tasks", ctypes.c_int64)]
+                                            "ratio", "section_units", "heavy_levels")] + [("num_tasks", ctypes.c_int64)]
 
 
 class FaTask(ctypes.Structure):
     _fields_ = [("b", ctypes.c_int), ("g", ctypes.c_int), ("mblock", ctypes.c_int), ("kv_head", ctypes.c_int),
                 ("pos0", ctypes.c_int * 2), ("n_blocks", ctypes.c_int * 2)]
 
+
+class FaVarlenTask(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("b", "g", "mblock", "reserved", "q_row0", "seqlen_q", "k_row0",
+                                            "seqlen_k")]
+
+
+# a varlen workspace holds the task count at byte 0 and the task records from this offset
+VARLEN_HEADER_BYTES = 256
 
 _lib = None
 
@@ -88,6 +105,19 @@ def load_library(path: str | None = None):
     lib.fa_plan_block_masked.restype = _I
     lib.fa_selftest_exp2.argtypes = [_P, _P, _P, _I, _P]
     lib.fa_selftest_exp2.restype = _I
+    lib.fa_plan_first_masked_block.argtypes = [ctypes.POINTER(FaPlan), _I]
+    lib.fa_plan_first_masked_block.restype = _I
+    lib.fa_varlen_workspace_size.argtypes = [_I, _I, ctypes.c_int64]
+    lib.fa_varlen_workspace_size.restype = ctypes.c_size_t
+    vl = [_P, _P, _P, _P, _P, _P, _P, _I, ctypes.c_int64, ctypes.c_int64, _I, _I, _I, _I, _I, ctypes.c_float, _P,
+          ctypes.c_size_t]
+    lib.fa_fwd_varlen.argtypes = vl + [_P]
+    lib.fa_fwd_varlen.restype = _I
+    lib.fa_fwd_varlen_ex.argtypes = vl + [ctypes.POINTER(FaOptions), _P]
+    lib.fa_fwd_varlen_ex.restype = _I
+    lib.fa_varlen_plan_host.argtypes = [_P, _P] + [_I] * 6 + [ctypes.c_int64, _I, ctypes.POINTER(FaVarlenTask),
+                                                             ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
+    lib.fa_varlen_plan_host.restype = _I
     if path is None:
         _lib = lib
     return lib
@@ -161,19 +191,68 @@ def fa_plan_block_masked(plan: FaPlan, pos0: int, j: int) -> bool:
     return bool(load_library().fa_plan_block_masked(ctypes.byref(plan), pos0, j))
 
 
+def fa_plan_first_masked_block(plan: FaPlan, pos0: int) -> int:
+    return load_library().fa_plan_first_masked_block(ctypes.byref(plan), pos0)
+
+
+def fa_varlen_workspace_size(batch: int, heads_q: int, total_q: int) -> int:
+    return load_library().fa_varlen_workspace_size(batch, heads_q, total_q)
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv, d_qk, d_v, causal, scale,
+                  workspace, workspace_bytes, stream) -> int:
+    """``fa_fwd_varlen`` of include/fa.h; pointer arguments are integers (device addresses)."""
+    return load_library().fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv, d_qk,
+                                        d_v, int(causal), float(scale), workspace, workspace_bytes, stream)
+
+
+def fa_fwd_varlen_ex(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv, d_qk, d_v, causal,
+                     scale, workspace, workspace_bytes, opts, stream) -> int:
+    return load_library().fa_fwd_varlen_ex(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv,
+                                           d_qk, d_v, int(causal), float(scale), workspace, workspace_bytes,
+                                           ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def fa_varlen_plan_host(cu_q, cu_k, heads_q, heads_kv, d_qk, d_v, causal, l2_bytes=0, pack=0):
+    """Host copy of the planning kernel's task list for int sequences ``cu_q``, ``cu_k`` (length B + 1)."""
+    batch = len(cu_q) - 1
+    cq = (ctypes.c_int * len(cu_q))(*[int(x) for x in cu_q])
+    ck = (ctypes.c_int * len(cu_k))(*[int(x) for x in cu_k])
+    n = ctypes.c_int64(0)
+    lib = load_library()
+    rc = lib.fa_varlen_plan_host(cq, ck, batch, heads_q, heads_kv, d_qk, d_v, int(causal), l2_bytes, pack, None, 0,
+                                 ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_varlen_plan_host")
+    out = (FaVarlenTask * max(n.value, 1))()
+    rc = lib.fa_varlen_plan_host(cq, ck, batch, heads_q, heads_kv, d_qk, d_v, int(causal), l2_bytes, pack, out,
+                                 n.value, ctypes.byref(n))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_varlen_plan_host")
+    return list(out)[: n.value]
+
+
 # ---------------------------------------------------------------------------
 # torch convenience wrapper (allocation and argument marshalling only)
 # ---------------------------------------------------------------------------
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-                      return_lse: bool = True, stream=None, options: FaOptions | None = None):
+                      return_lse: bool = True, stream=None, options: FaOptions | None = None, workspace=None):
     """O (and LSE) for bf16 CUDA tensors q [B,Sq,Hq,dqk], k [B,Sk,Hkv,dqk], v [B,Sk,Hkv,dv].
 
     Allocates ``out`` [B,Sq,Hq,dv] bf16 and ``lse`` [B,Hq,Sq] fp32 when not given.
-    Launches on ``stream`` (default: torch's current stream).  Raises FaError on
-    any non-OK status.
+    ``workspace`` (a CUDA tensor of at least SCHED_WORKSPACE_BYTES bytes) selects
+    dynamic task assignment (``fa_options.workspace``).  Launches on ``stream``
+    (default: torch's current stream).  Raises FaError on any non-OK status.
     """
     import torch
+
+    if workspace is not None:
+        if not workspace.is_cuda or workspace.numel() * workspace.element_size() < SCHED_WORKSPACE_BYTES:
+            raise FaError(FA_ERR_INVALID_ARG, f"workspace must be a CUDA tensor of >= {SCHED_WORKSPACE_BYTES} bytes")
+        base = options if options is not None else default_options()
+        options = FaOptions.from_buffer_copy(base)
+        options.workspace = workspace.data_ptr()
 
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
@@ -193,6 +272,50 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
                    lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Sq, Sk, dqk, dv, causal, s, options, sptr)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+    return (out, lse) if return_lse else out
+
+
+def attention_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool = False, scale: float | None = None,
+                             out=None, lse=None, return_lse: bool = True, workspace=None, stream=None,
+                             options: FaOptions | None = None):
+    """O (and LSE) of a variable-length batch: q [total_q,Hq,dqk], k [total_k,Hkv,dqk], v [total_k,Hkv,dv]
+    bf16 CUDA tensors, cu_seqlens_q / cu_seqlens_k int32 CUDA tensors [B+1].
+
+    Allocates ``out`` [total_q,Hq,dv] bf16, ``lse`` [Hq,total_q] fp32 and the
+    planning workspace (uint8) when not given.  Bad cu_seqlens are detected on
+    the device and reported by ``fa_device_status``.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 3-D bf16 CUDA tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.dim() != 1:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 1-D int32 CUDA tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise FaError(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both hold batch + 1 offsets")
+    batch = cu_seqlens_q.numel() - 1
+    total_q, Hq, dqk = q.shape
+    total_k, Hkv, _ = k.shape
+    dv = v.shape[2]
+    if out is None:
+        out = torch.empty((total_q, Hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    need = fa_varlen_workspace_size(batch, Hq, total_q)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    s = 0.0 if scale is None else float(scale)
+    rc = fa_fwd_varlen_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else None, cu_seqlens_q.data_ptr(),
+                          cu_seqlens_k.data_ptr(), batch, total_q, total_k, Hq, Hkv, dqk, dv, causal, s,
+                          workspace.data_ptr(), workspace.numel(), options, sptr)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_varlen")
     return (out, lse) if return_lse else out
 
 

@@ -5,10 +5,13 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "fa.h"
 #include "fa_dispatch.h"
@@ -20,7 +23,20 @@ __device__ unsigned int g_fa_status[4];
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumKernels = 20;  // 5 (d_qk, d_v) pairs x {non-causal, causal} x {MUFU, FMA-emulated exp}
+// 5 (d_qk, d_v) pairs x {non-causal, causal} x {fixed-length, fixed-length with the FMA-pipe exp2, varlen,
+// fixed-length with dynamic task assignment}
+constexpr int kVariants = 4;
+constexpr int kNumKernels = 5 * 2 * kVariants;
+constexpr int kVariantFixed = 0, kVariantEmu = 1, kVariantVarlen = 2, kVariantDyn = 3;
+
+// variable-length batches: workspace = [task count (int) at byte 0, task counter (uint) at byte 16,
+// padding to 256 B][VarlenTask records]
+constexpr size_t kVarlenHeaderBytes = 256;
+constexpr size_t kVarlenCounterOffset = 16;
+constexpr int kVarlenMaxBatch = 16384;  // sequences one planning CTA sorts in shared memory
+constexpr int kPlanThreads = 1024;
+constexpr unsigned int kSiteVarlenSeqlens = 501;  // a cu_seqlens entry is out of order or out of range
+constexpr unsigned int kSiteVarlenCapacity = 502; // more tasks than the workspace holds
 
 struct DeviceState {
   bool ready = false;
@@ -29,26 +45,27 @@ struct DeviceState {
   int smem_optin = 0;
   unsigned int* status = nullptr;
   bool kernel_ready[kNumKernels] = {};
+  bool plan_ready = false;
 };
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-int kernel_index(int dq, int dv, int causal, int emu) {
+int kernel_index(int dq, int dv, int causal, int variant) {
   int pair = -1;
   if (dq == 64 && dv == 64) pair = 0;
   if (dq == 128 && dv == 64) pair = 1;
   if (dq == 128 && dv == 128) pair = 2;
   if (dq == 192 && dv == 64) pair = 3;
   if (dq == 192 && dv == 128) pair = 4;
-  return pair < 0 ? -1 : pair * 4 + (causal ? 2 : 0) + (emu ? 1 : 0);
+  return pair < 0 ? -1 : (pair * 2 + (causal ? 1 : 0)) * kVariants + variant;
 }
 
-bool get_entry(int dq, int dv, int causal, int emu, fa::KernelEntry* e) {
-  if (dq == 64) return fa::entry_d64(dv, causal, emu, e);
-  if (dq == 128) return fa::entry_d128(dv, causal, emu, e);
-  if (dq == 192) return fa::entry_d192(dv, causal, emu, e);
+bool get_entry(int dq, int dv, int causal, int variant, fa::KernelEntry* e) {
+  if (dq == 64) return fa::entry_d64(dv, causal, variant, e);
+  if (dq == 128) return fa::entry_d128(dv, causal, variant, e);
+  if (dq == 192) return fa::entry_d192(dv, causal, variant, e);
   return false;
 }
 
@@ -129,8 +146,10 @@ int encode_q_like(CUtensorMap* m, const void* base, int B, int S, int H, int d, 
   const cuuint64_t e = 2;
   cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(pack), static_cast<cuuint64_t>(H / pack),
                         static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  // with one batch (varlen) the batch stride is never used: keep it small so
+  // that the encoder's stride limit does not depend on the sequence length
   cuuint64_t strides[4] = {d * e, static_cast<cuuint64_t>(pack) * d * e, static_cast<cuuint64_t>(H) * d * e,
-                           static_cast<cuuint64_t>(S) * H * d * e};
+                           static_cast<cuuint64_t>(B > 1 ? S : 1) * H * d * e};
   cuuint32_t box[5] = {64, static_cast<cuuint32_t>(pack), 1, static_cast<cuuint32_t>(fa::kBM / pack), 1};
   return encode(m, base, 5, dims, strides, box);
 }
@@ -140,7 +159,8 @@ int encode_kv(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
   const cuuint64_t e = 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(H) * d * e, static_cast<cuuint64_t>(S) * H * d * e};
+  cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(H) * d * e,
+                           static_cast<cuuint64_t>(B > 1 ? S : 1) * H * d * e};
   cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(fa::kBN), 1};
   return encode(m, base, 4, dims, strides, box);
 }
@@ -167,9 +187,139 @@ __global__ void fill_f32(float* p, int64_t n, float v) {
     p[i] = v;
 }
 
-int validate(const void* q, const void* k, const void* v, void* o, const float* lse, int batch, int heads_q,
-             int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, float scale, const fa_options& opt) {
-  if (batch < 0 || seqlen_q < 0 || seqlen_k < 0 || heads_q < 1 || heads_kv < 1) return FA_ERR_INVALID_ARG;
+// ---------------------------------------------------------------------------
+// variable-length batches: the planning kernel
+// ---------------------------------------------------------------------------
+// One CTA.  Checks cu_seqlens, sorts the sequences by the K/V blocks of their
+// heaviest tile (longest first, ties by index; "FlashAttention-4 wiki", "Core
+// methods": LPT scheduling with a preprocessing kernel for varlen), then
+// writes every sequence's tasks in that order.  Shared memory: the sort values
+// (a power of two >= batch) and the first task of each sorted position.
+size_t plan_smem_bytes(int batch) {
+  int npow2 = 1;
+  while (npow2 < batch) npow2 <<= 1;
+  return static_cast<size_t>(npow2) * sizeof(uint64_t) + static_cast<size_t>(batch + 1) * sizeof(int);
+}
+
+__device__ void plan_error(unsigned int* status, int* count, unsigned int site, int index) {
+  *count = 0;
+  if (atomicCAS(&status[0], 0u, static_cast<unsigned int>(FA_ERR_INVALID_ARG)) == 0u) {
+    status[1] = site;
+    status[2] = static_cast<unsigned int>(index);
+  }
+}
+
+__global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(
+    const int* cu_q, const int* cu_k, int batch, int64_t total_q, int64_t total_k, fa::Problem base, int d_qk,
+    int d_v, int64_t l2_budget, fa::VarlenTask* tasks, int* count, unsigned int* sched_next, int64_t capacity,
+    unsigned int* status) {
+  extern __shared__ __align__(16) uint8_t plan_smem[];
+  __shared__ int bad_index;
+  __shared__ long long warp_sums[kPlanThreads / 32];
+  int npow2 = 1;
+  while (npow2 < batch) npow2 <<= 1;
+  uint64_t* vals = reinterpret_cast<uint64_t*>(plan_smem);
+  int* start = reinterpret_cast<int*>(vals + npow2);
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    bad_index = INT_MAX;
+    *sched_next = 0;  // the attention kernel's dynamic task counter
+  }
+  __syncthreads();
+  for (int i = tid; i < npow2; i += kPlanThreads) {
+    uint64_t v = 0;  // padding sorts after every sequence
+    if (i < batch) {
+      const int q0 = cu_q[i], q1 = cu_q[i + 1], k0 = cu_k[i], k1 = cu_k[i + 1];
+      if (q0 < 0 || q1 < q0 || q1 > total_q || k0 < 0 || k1 < k0 || k1 > total_k) atomicMin(&bad_index, i);
+      v = fa::varlen_sort_value(fa::varlen_key(q1 - q0, k1 - k0), i);
+    }
+    vals[i] = v;
+  }
+  __syncthreads();
+  if (bad_index != INT_MAX) {
+    if (tid == 0) plan_error(status, count, kSiteVarlenSeqlens, bad_index);
+    return;
+  }
+
+  // bitonic sort, descending
+  for (int k = 2; k <= npow2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < npow2; i += kPlanThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t a = vals[i], b = vals[l];
+          if (((i & k) == 0) ? (a < b) : (a > b)) {
+            vals[i] = b;
+            vals[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // tasks per sorted position, exclusive scan: thread tid owns positions [lo, hi)
+  const int per = (batch + kPlanThreads - 1) / kPlanThreads;
+  const int lo = tid * per < batch ? tid * per : batch;
+  const int hi = lo + per < batch ? lo + per : batch;
+  auto tasks_at = [&](int pos) -> long long {
+    const int b = fa::varlen_sort_index(vals[pos]);
+    const int sq = cu_q[b + 1] - cu_q[b], sk = cu_k[b + 1] - cu_k[b];
+    if (sq == 0) return 0;
+    return fa::varlen_sequence_problem(base, sq, sk, d_qk, d_v, l2_budget).num_tasks;
+  };
+  long long mine = 0;
+  for (int i = lo; i < hi; ++i) mine += tasks_at(i);
+  long long incl = mine;  // inclusive scan inside the warp
+  const int lane = tid & 31, warp = tid >> 5;
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = warp_sums[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const long long total = warp_sums[kPlanThreads / 32 - 1];
+  if (total > capacity) {
+    if (tid == 0) plan_error(status, count, kSiteVarlenCapacity, 0);
+    return;
+  }
+  long long run = (warp > 0 ? warp_sums[warp - 1] : 0) + incl - mine;
+  for (int i = lo; i < hi; ++i) {
+    start[i] = static_cast<int>(run);
+    run += tasks_at(i);
+  }
+  if (tid == 0) start[batch] = static_cast<int>(total);
+  __syncthreads();
+
+  // emit: task t belongs to the last sorted position whose first task is <= t
+  for (int t = tid; t < static_cast<int>(total); t += kPlanThreads) {
+    int a = 0, z = batch - 1;
+    while (a < z) {
+      const int mid = (a + z + 1) >> 1;
+      if (start[mid] <= t) a = mid;
+      else z = mid - 1;
+    }
+    const int b = fa::varlen_sort_index(vals[a]);
+    const int q0 = cu_q[b], k0 = cu_k[b];
+    const fa::Problem seq = fa::varlen_sequence_problem(base, cu_q[b + 1] - q0, cu_k[b + 1] - k0, d_qk, d_v, l2_budget);
+    tasks[t] = fa::varlen_record(seq, b, q0, k0, t - start[a]);
+  }
+  if (tid == 0) *count = static_cast<int>(total);
+}
+
+// Options, heads, head dims and scale (shared by the fixed-length and varlen calls).
+int validate_common(int heads_q, int heads_kv, int d_qk, int d_v, float scale, const fa_options& opt) {
+  if (heads_q < 1 || heads_kv < 1) return FA_ERR_INVALID_ARG;
   if (heads_q % heads_kv != 0) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale)) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (kernel_index(d_qk, d_v, 0, 0) < 0) return FA_ERR_UNSUPPORTED;
@@ -183,9 +333,18 @@ int validate(const void* q, const void* k, const void* v, void* o, const float* 
     const int ratio = heads_q / heads_kv;
     if (fa::kBM % opt.pack != 0 || ratio % opt.pack != 0) return FA_ERR_INVALID_ARG;
   }
+  return FA_OK;
+}
+
+int validate(const void* q, const void* k, const void* v, void* o, const float* lse, int batch, int heads_q,
+             int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, float scale, const fa_options& opt) {
+  if (batch < 0 || seqlen_q < 0 || seqlen_k < 0) return FA_ERR_INVALID_ARG;
+  const int rc = validate_common(heads_q, heads_kv, d_qk, d_v, scale, opt);
+  if (rc != FA_OK) return rc;
   if (batch == 0 || seqlen_q == 0) return FA_OK;  // nothing to compute; pointers unused
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(opt.workspace))
     return FA_ERR_INVALID_ARG;
   // every TMA extent and index must fit in 32 bits
   const int64_t big = int64_t(1) << 31;
@@ -205,6 +364,7 @@ void fa_options_default(fa_options* opts) {
   opts->timeout_s = 1.0;
   opts->debug_flags = 0;
   opts->exp_emu = 0;
+  opts->workspace = nullptr;
 }
 
 int fa_version(void) { return 100; }
@@ -238,6 +398,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
 
   int rc = validate(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, scale, opt);
   if (rc != FA_OK) return rc;
+  if (opt.workspace != nullptr && opt.exp_emu) return FA_ERR_UNSUPPORTED;  // one or the other
   if (batch == 0 || seqlen_q == 0) return FA_OK;
   if (scale == 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d_qk));
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -248,7 +409,8 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   rc = init_device(dev, &st);
   if (rc != FA_OK) return rc;
   if (!is_device_ptr(q, dev) || !is_device_ptr(k, dev) || !is_device_ptr(v, dev) || !is_device_ptr(o, dev) ||
-      (lse != nullptr && !is_device_ptr(lse, dev)))
+      (lse != nullptr && !is_device_ptr(lse, dev)) ||
+      (opt.workspace != nullptr && !is_device_ptr(opt.workspace, dev)))
     return FA_ERR_INVALID_ARG;
 
   if (seqlen_k == 0) {  // no key anywhere: O = 0, lse = -inf
@@ -262,9 +424,10 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     return FA_OK;
   }
 
-  const int idx = kernel_index(d_qk, d_v, causal, opt.exp_emu);
+  const int variant = opt.workspace != nullptr ? kVariantDyn : (opt.exp_emu ? kVariantEmu : kVariantFixed);
+  const int idx = kernel_index(d_qk, d_v, causal, variant);
   fa::KernelEntry entry;
-  if (idx < 0 || !get_entry(d_qk, d_v, causal, opt.exp_emu, &entry)) return FA_ERR_UNSUPPORTED;
+  if (idx < 0 || !get_entry(d_qk, d_v, causal, variant, &entry)) return FA_ERR_UNSUPPORTED;
   rc = prepare_kernel(st, idx, entry);
   if (rc != FA_OK) return rc;
 
@@ -278,6 +441,10 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (encode_kv(&p.tm_v, v, batch, seqlen_k, heads_kv, d_v) != FA_OK) return FA_ERR_CUDA;
   if (encode_q_like(&p.tm_o, o, batch, seqlen_q, heads_q, d_v, p.prob.pack) != FA_OK) return FA_ERR_CUDA;
   p.lse = lse;
+  p.lse_hstride = seqlen_q;
+  p.lse_bstride = static_cast<int64_t>(heads_q) * seqlen_q;
+  p.o = static_cast<uint16_t*>(o);
+  p.o_row_stride = static_cast<int64_t>(heads_q) * d_v;
   p.status = st->status;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.tau = opt.tau;
@@ -287,6 +454,10 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   int64_t grid = opt.grid > 0 ? opt.grid : st->sms;
   if (grid > p.prob.num_tasks) grid = p.prob.num_tasks;
   if (grid < 1) return FA_OK;
+  if (opt.workspace != nullptr) {  // dynamic assignment: the counter starts at 0 for this launch
+    p.sched_next = static_cast<unsigned int*>(opt.workspace);
+    if (cudaMemsetAsync(opt.workspace, 0, FA_SCHED_WORKSPACE_BYTES, stream) != cudaSuccess) return FA_ERR_CUDA;
+  }
   if (entry.launch(p, static_cast<int>(grid), stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -295,6 +466,166 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale, fa_stream_t stream) {
   return fa_fwd_ex(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale, nullptr,
                    stream);
+}
+
+size_t fa_varlen_workspace_size(int batch, int heads_q, int64_t total_q) {
+  if (batch < 0 || heads_q < 1 || total_q < 0) return 0;
+  return kVarlenHeaderBytes + sizeof(fa::VarlenTask) * static_cast<size_t>(fa::varlen_max_tasks(batch, heads_q, total_q));
+}
+
+int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, int batch, int64_t total_q, int64_t total_k, int heads_q,
+                     int heads_kv, int d_qk, int d_v, int causal, float scale, void* workspace,
+                     size_t workspace_bytes, const fa_options* opts, fa_stream_t stream_) {
+  fa_options opt;
+  fa_options_default(&opt);
+  if (opts) opt = *opts;
+  if (opt.tau < 0.f) opt.tau = 8.0f;
+  if (opt.timeout_s <= 0.0) opt.timeout_s = 1.0;
+  causal = causal ? 1 : 0;
+
+  if (batch < 0 || batch > kVarlenMaxBatch || total_q < 0 || total_k < 0) return FA_ERR_INVALID_ARG;
+  int rc = validate_common(heads_q, heads_kv, d_qk, d_v, scale, opt);
+  if (rc != FA_OK) return rc;
+  if (opt.exp_emu != 0) return FA_ERR_UNSUPPORTED;  // the FMA-pipe exp2 is built for fixed-length batches only
+  if (opt.workspace != nullptr) return FA_ERR_INVALID_ARG;  // varlen calls take their workspace as an argument
+  if (batch == 0 || total_q == 0) return FA_OK;
+  // TMA coordinates (row + 128) and the task count stay inside 32 bits
+  const int64_t big = int64_t(1) << 31;
+  if (total_q + total_k + 4 * fa::kBM >= big) return FA_ERR_INVALID_ARG;
+  const int64_t max_tasks = fa::varlen_max_tasks(batch, heads_q, total_q);
+  if (max_tasks >= big) return FA_ERR_INVALID_ARG;
+  if (q == nullptr || o == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || workspace == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (total_k > 0 && (k == nullptr || v == nullptr)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace) ||
+      (total_k > 0 && (!aligned16(k) || !aligned16(v))))
+    return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+    return FA_ERR_INVALID_ARG;
+  if (workspace_bytes < fa_varlen_workspace_size(batch, heads_q, total_q)) return FA_ERR_INVALID_ARG;
+  if (scale == 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d_qk));
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* st = nullptr;
+  rc = init_device(dev, &st);
+  if (rc != FA_OK) return rc;
+  if (!is_device_ptr(q, dev) || !is_device_ptr(o, dev) || !is_device_ptr(cu_seqlens_q, dev) ||
+      !is_device_ptr(cu_seqlens_k, dev) || !is_device_ptr(workspace, dev) ||
+      (total_k > 0 && (!is_device_ptr(k, dev) || !is_device_ptr(v, dev))) ||
+      (lse != nullptr && !is_device_ptr(lse, dev)))
+    return FA_ERR_INVALID_ARG;
+
+  if (total_k == 0) {  // no key in any sequence: O = 0, lse = -inf
+    if (cudaMemsetAsync(o, 0, static_cast<size_t>(total_q) * heads_q * d_v * 2, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (lse) {
+      fill_f32<<<st->sms * 4, 256, 0, stream>>>(lse, static_cast<int64_t>(heads_q) * total_q, -INFINITY);
+      if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return FA_OK;
+  }
+
+  const int idx = kernel_index(d_qk, d_v, causal, kVariantVarlen);
+  fa::KernelEntry entry;
+  if (idx < 0 || !get_entry(d_qk, d_v, causal, kVariantVarlen, &entry)) return FA_ERR_UNSUPPORTED;
+  rc = prepare_kernel(st, idx, entry);
+  if (rc != FA_OK) return rc;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!st->plan_ready) {
+      if (cudaFuncSetAttribute(varlen_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(plan_smem_bytes(kVarlenMaxBatch))) != cudaSuccess)
+        return FA_ERR_CUDA;
+      st->plan_ready = true;
+    }
+  }
+
+  fa::Params p;
+  std::memset(&p, 0, sizeof(p));
+  // the fields every sequence shares; lengths travel with each task
+  p.prob = fa::make_problem(1, heads_q, heads_kv, 1, 1, d_qk, d_v, causal, st->l2_bytes / 2, opt.pack);
+  const int tq = static_cast<int>(total_q), tk = static_cast<int>(total_k);
+  if (encode_q_like(&p.tm_q, q, 1, tq, heads_q, d_qk, p.prob.pack) != FA_OK) return FA_ERR_CUDA;
+  if (encode_kv(&p.tm_k, k, 1, tk, heads_kv, d_qk) != FA_OK) return FA_ERR_CUDA;
+  if (encode_kv(&p.tm_v, v, 1, tk, heads_kv, d_v) != FA_OK) return FA_ERR_CUDA;
+  if (encode_q_like(&p.tm_o, o, 1, tq, heads_q, d_v, p.prob.pack) != FA_OK) return FA_ERR_CUDA;
+  p.lse = lse;
+  p.lse_hstride = total_q;
+  p.lse_bstride = 0;
+  p.o = static_cast<uint16_t*>(o);
+  p.o_row_stride = static_cast<int64_t>(heads_q) * d_v;
+  int* count = static_cast<int*>(workspace);
+  fa::VarlenTask* tasks =
+      reinterpret_cast<fa::VarlenTask*>(static_cast<uint8_t*>(workspace) + kVarlenHeaderBytes);
+  p.vtasks = tasks;
+  p.vtask_count = count;
+  p.sched_next = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) + kVarlenCounterOffset);
+  p.status = st->status;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.tau = opt.tau;
+  p.timeout_ns = static_cast<unsigned long long>(opt.timeout_s * 1e9);
+  p.debug_flags = opt.debug_flags;
+
+  const int64_t capacity = static_cast<int64_t>((workspace_bytes - kVarlenHeaderBytes) / sizeof(fa::VarlenTask));
+  varlen_plan_kernel<<<1, kPlanThreads, plan_smem_bytes(batch), stream>>>(
+      cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, p.prob, d_qk, d_v, st->l2_bytes / 2, tasks, count,
+      p.sched_next, capacity < max_tasks ? capacity : max_tasks, st->status);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+
+  int64_t grid = opt.grid > 0 ? opt.grid : st->sms;
+  if (grid > max_tasks) grid = max_tasks;
+  if (entry.launch(p, static_cast<int>(grid), stream) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int batch, int64_t total_q, int64_t total_k, int heads_q, int heads_kv,
+                  int d_qk, int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
+                  fa_stream_t stream) {
+  return fa_fwd_varlen_ex(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, heads_q, heads_kv,
+                          d_qk, d_v, causal, scale, workspace, workspace_bytes, nullptr, stream);
+}
+
+int fa_varlen_plan_host(const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int heads_q, int heads_kv,
+                        int d_qk, int d_v, int causal, int64_t l2_bytes, int pack, fa_varlen_task* out,
+                        int64_t capacity, int64_t* count) {
+  if (count == nullptr || batch < 0 || batch > kVarlenMaxBatch || capacity < 0) return FA_ERR_INVALID_ARG;
+  if (batch > 0 && (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)) return FA_ERR_INVALID_ARG;
+  fa_options opt;
+  fa_options_default(&opt);
+  opt.pack = pack;
+  const int rc = validate_common(heads_q, heads_kv, d_qk, d_v, 1.f, opt);
+  if (rc != FA_OK) return rc;
+  if (l2_bytes <= 0) l2_bytes = int64_t(64) << 20;
+  for (int i = 0; i < batch; ++i)
+    if (cu_seqlens_q[i] < 0 || cu_seqlens_q[i + 1] < cu_seqlens_q[i] || cu_seqlens_k[i] < 0 ||
+        cu_seqlens_k[i + 1] < cu_seqlens_k[i])
+      return FA_ERR_INVALID_ARG;
+  const fa::Problem base = fa::make_problem(1, heads_q, heads_kv, 1, 1, d_qk, d_v, causal ? 1 : 0, l2_bytes, pack);
+  std::vector<uint64_t> vals(static_cast<size_t>(batch));
+  for (int i = 0; i < batch; ++i)
+    vals[i] = fa::varlen_sort_value(
+        fa::varlen_key(cu_seqlens_q[i + 1] - cu_seqlens_q[i], cu_seqlens_k[i + 1] - cu_seqlens_k[i]), i);
+  std::sort(vals.begin(), vals.end(), [](uint64_t a, uint64_t b) { return a > b; });
+  int64_t n = 0;
+  for (int pos = 0; pos < batch; ++pos) {
+    const int b = fa::varlen_sort_index(vals[pos]);
+    const int q0 = cu_seqlens_q[b], k0 = cu_seqlens_k[b];
+    const int sq = cu_seqlens_q[b + 1] - q0, sk = cu_seqlens_k[b + 1] - k0;
+    if (sq == 0) continue;
+    const fa::Problem seq = fa::varlen_sequence_problem(base, sq, sk, d_qk, d_v, l2_bytes);
+    for (int64_t i = 0; i < seq.num_tasks; ++i, ++n) {
+      if (out == nullptr || n >= capacity) continue;
+      const fa::VarlenTask r = fa::varlen_record(seq, b, q0, k0, static_cast<int>(i));
+      out[n].b = r.b, out[n].g = r.g, out[n].mblock = r.mb, out[n].reserved = 0;
+      out[n].q_row0 = r.q_row0, out[n].seqlen_q = r.sq, out[n].k_row0 = r.k_row0, out[n].seqlen_k = r.sk;
+    }
+  }
+  *count = n;
+  return FA_OK;
 }
 
 int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]) {
@@ -345,7 +676,7 @@ int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_
   out->batch = p.B, out->heads_q = p.Hq, out->heads_kv = p.Hkv, out->seqlen_q = p.Sq, out->seqlen_k = p.Sk;
   out->causal = p.causal, out->pack = p.pack, out->groups = p.groups, out->pos_per_tile = p.pos_per_tile;
   out->tiles = p.tiles, out->mblocks = p.mblocks, out->kv_blocks = p.kv_blocks, out->ratio = p.ratio;
-  out->section_units = p.section_units, out->num_tasks = p.num_tasks;
+  out->section_units = p.section_units, out->heavy_levels = p.heavy_levels, out->num_tasks = p.num_tasks;
   return FA_OK;
 }
 
@@ -354,7 +685,7 @@ static fa::Problem problem_of(const fa_plan* pl) {
   p.B = pl->batch, p.Hq = pl->heads_q, p.Hkv = pl->heads_kv, p.Sq = pl->seqlen_q, p.Sk = pl->seqlen_k;
   p.causal = pl->causal, p.pack = pl->pack, p.groups = pl->groups, p.pos_per_tile = pl->pos_per_tile;
   p.tiles = pl->tiles, p.mblocks = pl->mblocks, p.kv_blocks = pl->kv_blocks, p.ratio = pl->ratio;
-  p.section_units = pl->section_units, p.num_tasks = pl->num_tasks;
+  p.section_units = pl->section_units, p.heavy_levels = pl->heavy_levels, p.num_tasks = pl->num_tasks;
   return p;
 }
 
@@ -369,6 +700,11 @@ int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out) {
 int fa_plan_block_masked(const fa_plan* plan, int pos0, int j) {
   if (plan == nullptr) return 0;
   return fa::block_needs_mask(problem_of(plan), pos0, j) ? 1 : 0;
+}
+
+int fa_plan_first_masked_block(const fa_plan* plan, int pos0) {
+  if (plan == nullptr) return 0;
+  return fa::first_masked_block(plan->seqlen_q, plan->seqlen_k, plan->causal, pos0);
 }
 
 }  // extern "C"

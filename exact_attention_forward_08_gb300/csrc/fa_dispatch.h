@@ -1,4 +1,7 @@
-// Kernel table: one entry per (d_qk, d_v, causal) instantiation.  Each head
+// Kernel table: one entry per (d_qk, d_v, causal, variant) instantiation; the
+// variants are fixed-length, fixed-length with the FMA-pipe exp2, varlen (its
+// tasks always assigned dynamically), and fixed-length with dynamic task
+// assignment.  Each head
 // dimension lives in its own translation unit so the build compiles them in
 // parallel.
 #pragma once
@@ -16,27 +19,36 @@ struct KernelEntry {
   LaunchFn launch;
 };
 
-template <int DQ, int DV, bool CAUSAL, bool EMU>
+template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
 cudaError_t launch_kernel(const Params& p, int grid, cudaStream_t stream) {
-  fa_fwd_kernel<DQ, DV, CAUSAL, EMU><<<grid, kThreads, Layout<DQ, DV>::kDynSmem, stream>>>(p);
+  fa_fwd_kernel<DQ, DV, CAUSAL, EMU, VARLEN, DYN><<<grid, kThreads, Layout<DQ, DV>::kDynSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int DQ, int DV, bool CAUSAL, bool EMU>
+template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
 KernelEntry make_entry() {
-  return KernelEntry{reinterpret_cast<const void*>(&fa_fwd_kernel<DQ, DV, CAUSAL, EMU>), Layout<DQ, DV>::kDynSmem,
-                     &launch_kernel<DQ, DV, CAUSAL, EMU>};
+  return KernelEntry{reinterpret_cast<const void*>(&fa_fwd_kernel<DQ, DV, CAUSAL, EMU, VARLEN, DYN>),
+                     Layout<DQ, DV>::kDynSmem, &launch_kernel<DQ, DV, CAUSAL, EMU, VARLEN, DYN>};
+}
+
+// variant: 0 fixed-length, 1 fixed-length with the FMA-pipe exp2, 2 varlen,
+// 3 fixed-length with dynamic task assignment
+template <int DQ, int DV, bool CAUSAL>
+KernelEntry pick_variant(int variant) {
+  if (variant == 3) return make_entry<DQ, DV, CAUSAL, false, false, true>();
+  if (variant == 2) return make_entry<DQ, DV, CAUSAL, false, true, true>();
+  if (variant == 1) return make_entry<DQ, DV, CAUSAL, true, false, false>();
+  return make_entry<DQ, DV, CAUSAL, false, false, false>();
 }
 
 template <int DQ, int DV>
-KernelEntry pick_entry(int causal, int emu) {
-  if (causal) return emu ? make_entry<DQ, DV, true, true>() : make_entry<DQ, DV, true, false>();
-  return emu ? make_entry<DQ, DV, false, true>() : make_entry<DQ, DV, false, false>();
+KernelEntry pick_entry(int causal, int variant) {
+  return causal ? pick_variant<DQ, DV, true>(variant) : pick_variant<DQ, DV, false>(variant);
 }
 
 // defined in fa_inst_d{64,128,192}.cu; false when (dq, dv) is not built
-bool entry_d64(int dv, int causal, int emu, KernelEntry* out);
-bool entry_d128(int dv, int causal, int emu, KernelEntry* out);
-bool entry_d192(int dv, int causal, int emu, KernelEntry* out);
+bool entry_d64(int dv, int causal, int variant, KernelEntry* out);
+bool entry_d128(int dv, int causal, int variant, KernelEntry* out);
+bool entry_d192(int dv, int causal, int variant, KernelEntry* out);
 
 }  // namespace fa

@@ -3,13 +3,13 @@
 
 namespace fa {
 
-bool entry_d192(int dv, int causal, int emu, KernelEntry* out) {
+bool entry_d192(int dv, int causal, int variant, KernelEntry* out) {
   if (dv == 64) {
-    *out = pick_entry<192, 64>(causal, emu);
+    *out = pick_entry<192, 64>(causal, variant);
     return true;
   }
   if (dv == 128) {
-    *out = pick_entry<192, 128>(causal, emu);
+    *out = pick_entry<192, 128>(causal, variant);
     return true;
   }
   return false;

@@ -3,9 +3,9 @@
 
 namespace fa {
 
-bool entry_d64(int dv, int causal, int emu, KernelEntry* out) {
+bool entry_d64(int dv, int causal, int variant, KernelEntry* out) {
   if (dv == 64) {
-    *out = pick_entry<64, 64>(causal, emu);
+    *out = pick_entry<64, 64>(causal, variant);
     return true;
   }
   return false;

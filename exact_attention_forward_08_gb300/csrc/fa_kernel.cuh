@@ -13,7 +13,10 @@
 //   warp 12                tcgen05.mma issue (one thread) + TMEM alloc/free.
 //   warp 13                TMA loads (one thread): Q stages, K/V ring.
 // Each task covers two Q tiles (stages) that stream the same K/V blocks, so
-// one stage's softmax overlaps the other stage's MMAs.
+// one stage's softmax overlaps the other stage's MMAs.  With VARLEN the
+// sequences are packed back to back (rows cu_seqlens[b] ..) and the tasks
+// come from a list written by the planning kernel; each task carries its
+// sequence's lengths and row offsets.
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DV),
 // O1 [384,384+DV).  P_s overwrites the first 64 columns of S_s as packed bf16
@@ -31,6 +34,13 @@
 //                128 correction threads (O rescaled or not)  -> PV MMA
 //   o_done[s]    MMA commit after the stage's last P V of a
 //                task                                        -> epilogue
+//   task_full[r] / task_empty[r]  (DYN only) the TMA thread takes the next
+//                task index from a global counter (atomicAdd) and posts it in
+//                ring slot r; every other warp reads it and frees the slot.
+// Task assignment: static round-robin (task = blockIdx.x + k * gridDim.x), or
+// with DYN dynamic, in list order, to whichever CTA asks next, so no CTA sits
+// on a long tail of heavy tasks while others idle (the counter is caller
+// scratch, cleared on the stream before each launch).
 // Every wait is bounded (see ptx.cuh); on a timeout the CTA records the
 // failing site in the status word, every role leaves its loop, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed.
@@ -50,18 +60,26 @@ constexpr int kRegBudgetPerCta = 128 * (176 + 176 + 104 + 56);
 constexpr int kChunkBytes = 128 * 64 * 2;  // 128 rows x 64 bf16: one 128B-swizzled TMA box
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.693147180559945309417f;
+constexpr int kTaskRing = 4;     // task indices the TMA thread may post ahead (DYN)
+constexpr int kTaskReaders = 13; // arrivals that free a ring slot: MMA warp + 12 softmax/correction warps
 
 // debug_flags bits
 constexpr int kDebugSkipPArrive = 1;  // softmax never arrives on p_full: exercises the bounded waits
 
 struct Params {
-  CUtensorMap tm_q;  // 5-D view (d, pack, groups, Sq, B) of q
-  CUtensorMap tm_k;  // 4-D view (d, Hkv, Sk, B) of k
+  CUtensorMap tm_q;  // 5-D view (d, pack, groups, Sq, B) of q (varlen: S = total_q rows, B = 1)
+  CUtensorMap tm_k;  // 4-D view (d, Hkv, Sk, B) of k (varlen: S = total_k rows, B = 1)
   CUtensorMap tm_v;  // 4-D view (dv, Hkv, Sk, B) of v
   CUtensorMap tm_o;  // 5-D view (dv, pack, groups, Sq, B) of o
-  float* lse;        // [B, Hq, Sq] or null
+  float* lse;        // [B, Hq, Sq] (varlen: [Hq, total_q]) or null
+  int64_t lse_bstride, lse_hstride;  // element strides of lse per batch and per head
+  uint16_t* o;                       // o (bf16 bits): direct stores of ragged varlen tiles
+  int64_t o_row_stride;              // elements between consecutive positions of o (Hq * dv)
+  const VarlenTask* vtasks;          // varlen: the planned task list
+  const int* vtask_count;            // varlen: its length
+  unsigned int* sched_next;          // DYN: next task index (cleared before the launch)
   unsigned int* status;
-  Problem prob;
+  Problem prob;  // varlen: the shared fields (heads, pack, causal); lengths come per task
   float scale_log2;  // scale * log2(e)
   float tau;         // conditional-rescale threshold, log2 units
   unsigned long long timeout_ns;
@@ -102,10 +120,13 @@ struct Layout {
   static constexpr int bEpiFull = bFinFull + 2;  // WG2: staging tile written (count 128)
   static constexpr int bStageFree = bEpiFull + 1; // WG2: TMA store finished reading staging (count 1)
   static constexpr int bDrain = bStageFree + 1;   // MMA drain at exit
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bTaskFull = bDrain + 1;               // [kTaskRing] (DYN) count 1
+  static constexpr int bTaskEmpty = bTaskFull + kTaskRing;   // [kTaskRing] (DYN) count kTaskReaders
+  static constexpr int kNumBars = bTaskEmpty + kTaskRing;
 
   static constexpr int oMisc = oBar + kNumBars * 8;  // [0] TMEM base, [1] abort flag
-  static constexpr int kBytes = oMisc + 16;
+  static constexpr int oTaskRing = oMisc + 16;       // int[kTaskRing] (DYN)
+  static constexpr int kBytes = oTaskRing + 4 * kTaskRing;
   static constexpr int kDynSmem = kBytes + 1024;     // slack to align the base to 1024 B
   static_assert(kDynSmem <= kMaxSmem, "shared memory budget");
 };
@@ -113,19 +134,98 @@ struct Layout {
 // Wait-site codes recorded in status[1] on a timeout: role * 100 + barrier.
 enum : unsigned int {
   kSiteSoftmaxS = 101,
+  kSiteSoftmaxTask = 102,
   kSiteCorrCorr = 201,
   kSiteCorrODone = 202,
   kSiteCorrEpiFull = 203,
   kSiteCorrStageFree = 204,
   kSiteCorrFin = 205,
+  kSiteCorrTask = 206,
   kSiteMmaKv = 301,
   kSiteMmaQ = 302,
   kSiteMmaP = 303,
   kSiteMmaDrain = 304,
+  kSiteMmaTask = 305,
   kSiteLoadQ = 401,
   kSiteLoadKv = 402,
   kSiteLoadDrain = 403,
+  kSiteLoadTask = 404,
 };
+
+// The tasks a CTA walks: decoded from the fixed-length problem, or read from
+// the list the varlen planning kernel wrote (every role reads the same list).
+// An int the compiler cannot see through (keeps a re-read from being merged
+// with an earlier one, so the earlier value need not stay live).
+__device__ __forceinline__ int opaque_i32(int x) {
+  asm volatile("" : "+r"(x));
+  return x;
+}
+template <bool VARLEN>
+__device__ __forceinline__ int task_count(const Params& p) {
+  if constexpr (VARLEN) return *p.vtask_count;
+  else return static_cast<int>(p.prob.num_tasks);
+}
+
+template <bool VARLEN>
+__device__ __forceinline__ Task get_task(const Params& p, int t) {
+  if constexpr (VARLEN) {
+    const int4* r = reinterpret_cast<const int4*>(p.vtasks + t);
+    const int4 a = r[0], b = r[1];
+    VarlenTask rec;
+    rec.b = a.x, rec.g = a.y, rec.mb = a.z, rec.reserved = a.w;
+    rec.q_row0 = b.x, rec.sq = b.y, rec.k_row0 = b.z, rec.sk = b.w;
+    return task_from_record(p.prob, rec);
+  } else {
+    return decode_task(p.prob, t);
+  }
+}
+
+// Task k of this CTA for a reading warp (softmax, correction, MMA): the
+// static index, or (DYN) the index the TMA thread posted in ring slot
+// k % kTaskRing.  Returns -1 when no task is left, -2 on an abort.  Called by
+// every lane of the warp.
+template <int DQ, int DV, bool DYN>
+__device__ __forceinline__ int read_task(int k, int num_tasks, uint32_t bar0, const volatile int* ring,
+                                         const WaitCtx& wc, unsigned site) {
+  using L = Layout<DQ, DV>;
+  if constexpr (!DYN) {
+    const int t = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    return t < num_tasks ? t : -1;
+  } else {
+    const int slot = k % kTaskRing;
+    const uint32_t parity = static_cast<uint32_t>(k / kTaskRing) & 1u;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (L::bTaskFull + slot), parity, wc, site))) return -2;
+    const int t = ring[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar0 + 8u * (L::bTaskEmpty + slot));
+    return t;
+  }
+}
+
+// The TMA thread's side (DYN): take the next task index from the global
+// counter and post it in ring slot k % kTaskRing once every reader freed the
+// slot's previous use.  Returns the index, -1 when none is left, -2 on an
+// abort.  Static assignment needs no posting.
+template <int DQ, int DV, bool DYN>
+__device__ __forceinline__ int post_task(const Params& p, int k, int num_tasks, uint32_t bar0, volatile int* ring,
+                                         const WaitCtx& wc) {
+  using L = Layout<DQ, DV>;
+  if constexpr (!DYN) {
+    const int t = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    return t < num_tasks ? t : -1;
+  } else {
+    const int slot = k % kTaskRing;
+    if (k >= kTaskRing &&
+        !mbar_wait(bar0 + 8u * (L::bTaskEmpty + slot), static_cast<uint32_t>(k / kTaskRing - 1) & 1u, wc,
+                   kSiteLoadTask))
+      return -2;
+    const unsigned int got = atomicAdd(p.sched_next, 1u);
+    const int t = got < static_cast<unsigned int>(num_tasks) ? static_cast<int>(got) : -1;
+    ring[slot] = t;
+    mbar_arrive(bar0 + 8u * (L::bTaskFull + slot));
+    return t;
+  }
+}
 
 // A wait that ignores the abort flag (used to drain in-flight async work
 // before TMEM is freed); still bounded by the time limit.
@@ -177,9 +277,10 @@ __device__ __forceinline__ void ex2_fma_x2(uint64_t x2, float& y0, float& y1) {
 // ---------------------------------------------------------------------------
 // EMU: one in four exponentials of unmasked blocks on the FMA pipe (an option;
 // its own instantiation, so the default kernel carries no extra code)
-template <int DQ, int DV, bool CAUSAL, bool EMU>
+template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
 __device__ __forceinline__ void softmax_role(const Params& p, const int stage, const uint32_t tmem,
-                                             const uint32_t sbase, float* mbox, const WaitCtx& wc) {
+                                             const uint32_t sbase, float* mbox, const volatile int* ring,
+                                             const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
   const Problem& pr = p.prob;
   const int t = threadIdx.x - stage * 128;  // row of the Q tile == TMEM lane
@@ -195,18 +296,24 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   const float neg_tau = -p.tau;
   const bool skip_p = (p.debug_flags & kDebugSkipPArrive) != 0;
   uint32_t phase = 0;
+  const int num_tasks = task_count<VARLEN>(p);
 
-  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
-    const Task tk = decode_task(pr, task);
+  for (int kt = 0;; ++kt) {
+    const int task = read_task<DQ, DV, DYN>(kt, num_tasks, sbase + L::oBar, ring, wc, kSiteSoftmaxTask);
+    if (task < 0) break;  // no task left, or an abort
+    const Task tk = get_task<VARLEN>(p, task);
     const int n = stage ? tk.n[1] : tk.n[0];
     if (n == 0) continue;
     const int pos0 = stage ? tk.pos0[1] : tk.pos0[0];
-    // last key visible to this row (inclusive); keys >= Sk are never visible
-    int64_t last_key = static_cast<int64_t>(pr.Sk) - 1;
+    // last key visible to this row (inclusive; keys >= sk are never visible;
+    // (pos - sq) + sk stays inside 32 bits for the sizes the host accepts),
+    // and the first block that needs the element mask
+    int last_key = tk.sk - 1;
     if (CAUSAL) {
-      const int64_t c = static_cast<int64_t>(pos0 + t / pr.pack) + pr.Sk - pr.Sq;
+      const int c = (pos0 + t / pr.pack - tk.sq) + tk.sk;
       if (c < last_key) last_key = c;
     }
+    const int j_mask = first_masked_block(tk.sq, tk.sk, CAUSAL, pos0);
     float row_max = -INFINITY;  // kept reference, raw score units
     float row_sum = 0.f;
     float ref = 0.f;            // row_max * scale_log2 (0 while the row is empty)
@@ -223,11 +330,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(r[c]);
 
-      const bool masked_block = block_needs_mask(pr, pos0, j);
+      const bool masked_block = j >= j_mask;
       if (masked_block) {
         // columns c <= lim are visible
-        int64_t lim64 = last_key - static_cast<int64_t>(j) * kBN;
-        const int lim = lim64 < -1 ? -1 : (lim64 > 127 ? 127 : static_cast<int>(lim64));
+        const int lim = max(-1, min(127, last_key - j * kBN));
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) s[c] = -INFINITY;
@@ -323,9 +429,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 // ---------------------------------------------------------------------------
 // correction + epilogue (WG2)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN>
 __device__ __forceinline__ void correction_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
-                                                uint8_t* smem, float* mbox, const WaitCtx& wc) {
+                                                uint8_t* smem, float* mbox, const volatile int* ring,
+                                                const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
   const Problem& pr = p.prob;
   const int t = threadIdx.x - 256;  // row == TMEM lane
@@ -336,10 +443,13 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   uint32_t corr_phase[2] = {0u, 0u};
   uint32_t fin_phase[2] = {0u, 0u};
   uint32_t od_count[2] = {0u, 0u};  // o_done phases consumed (one per task with blocks)
-  uint32_t chunks = 0;              // epilogue chunks stored so far
+  uint32_t chunks = 0;              // epilogue chunks stored through the staging tile so far
+  const int num_tasks = task_count<VARLEN>(p);
 
-  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
-    const Task tk = decode_task(pr, task);
+  for (int kt = 0;; ++kt) {
+    const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteCorrTask);
+    if (task < 0) break;  // no task left, or an abort
+    Task tk = get_task<VARLEN>(p, task);
     float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
 
     for (int j = 0; j < tk.nmax; ++j) {
@@ -379,12 +489,20 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
       }
     }
 
-    // epilogue: O / row_sum -> bf16 -> staging -> TMA store; LSE
+    // epilogue: O / row_sum -> bf16 -> staging -> TMA store; LSE.  A varlen
+    // task record is read again here rather than kept in registers across
+    // the K/V loop (this role runs at 104 registers).
+    if constexpr (VARLEN) tk = get_task<VARLEN>(p, opaque_i32(task));
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int pos0 = tk.pos0[s];
-      if (pos0 >= pr.Sq) continue;  // tile past the end of the sequence
+      if (pos0 >= tk.sq) continue;  // tile past the end of the sequence
       const bool has = tk.n[s] > 0;
+      // a varlen tile that runs past its sequence is stored row by row: a TMA
+      // store would write the next sequence's rows
+      const bool direct = VARLEN && pos0 + pr.pos_per_tile > tk.sq;
+      const int pos = pos0 + t / pr.pack;
+      const int head = tk.g * pr.pack + t % pr.pack;
       if (has) {  // o_done completes once per task: after the stage's last P V
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), od_count[s] & 1u, wc, kSiteCorrODone));
@@ -398,9 +516,13 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         lse = (fin_ref[s] + __log2f(fin_sum[s])) * kLn2;
       }
       const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(s * 128);
+      uint4* out_row = nullptr;
+      if (direct && pos < tk.sq)
+        out_row = reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(tk.q_row0) + pos) * p.o_row_stride +
+                                           static_cast<int64_t>(head) * DV);
 #pragma unroll 1
       for (int c = 0; c < L::NVC; ++c) {
-        if (chunks > 0) {
+        if (!direct && chunks > 0) {
           const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * L::bStageFree, (chunks - 1u) & 1u, wc,
                                                             kSiteCorrStageFree));
           if (!ok) goto out;
@@ -422,16 +544,21 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
             v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
             v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
             v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
-            row[(half * 4 + q) ^ (t & 7)] = v;  // 128-byte swizzle of the TMA box
+            if (direct) {
+              if (out_row != nullptr) out_row[c * 8 + half * 4 + q] = v;
+            } else {
+              row[(half * 4 + q) ^ (t & 7)] = v;  // 128-byte swizzle of the TMA box
+            }
           }
         }
+        if (direct) continue;
         fence_proxy_async_smem();
         mbar_arrive(bar0 + 8 * L::bEpiFull);
         bool stored = true;
         if (t == 0) {
           stored = mbar_wait(bar0 + 8 * L::bEpiFull, chunks & 1u, wc, kSiteCorrEpiFull);
           if (stored) {
-            tma_store_5d(&p.tm_o, staging_s, c * 64, 0, tk.g, pos0, tk.b);
+            tma_store_5d(&p.tm_o, staging_s, c * 64, 0, tk.g, tk.q_row0 + pos0, tk.bc);
             bulk_commit_group();
             bulk_wait_group_read0();
             mbar_arrive(bar0 + 8 * L::bStageFree);
@@ -442,11 +569,8 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         ++chunks;
         if (!stored) goto out;
       }
-      const int pos = pos0 + t / pr.pack;
-      if (p.lse != nullptr && pos < pr.Sq) {
-        const int head = tk.g * pr.pack + t % pr.pack;
-        p.lse[(static_cast<int64_t>(tk.b) * pr.Hq + head) * pr.Sq + pos] = lse;
-      }
+      if (p.lse != nullptr && pos < tk.sq)
+        p.lse[tk.b * p.lse_bstride + head * p.lse_hstride + tk.q_row0 + pos] = lse;
     }
   }
 out:
@@ -489,9 +613,9 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // o_done[s] is committed once per task, after the stage's last P V: inside a
 // task, "S_j ready" already implies that P V_{j-1} has completed (a commit
 // tracks every earlier MMA of the issuing thread).
-template <int DQ, int DV>
+template <int DQ, int DV, bool VARLEN, bool DYN>
 __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
-                                         const WaitCtx& wc) {
+                                         const volatile int* ring, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
   const Problem& pr = p.prob;
   const uint32_t bar0 = sbase + L::oBar;
@@ -511,8 +635,11 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   };
   auto release_tile = [&](uint32_t it) { mma_commit(bar(L::bKvEmpty + static_cast<int>(it % L::NS)), leader); };
 
-  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
-    const Task tk = decode_task(pr, task);
+  const int num_tasks = task_count<VARLEN>(p);
+  for (int kt = 0;; ++kt) {
+    const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteMmaTask);
+    if (task < 0) break;  // no task left, or an abort
+    const Task tk = get_task<VARLEN>(p, task);
     const uint32_t base = kv_it;
     kv_it += 2u * static_cast<uint32_t>(tk.nmax);
     if (tk.nmax == 0) continue;
@@ -571,8 +698,9 @@ out:
 // ---------------------------------------------------------------------------
 // TMA loads (warp 13, one thread)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV>
-__device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase, const WaitCtx& wc) {
+template <int DQ, int DV, bool VARLEN, bool DYN>
+__device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase, volatile int* ring,
+                                          const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
   const Problem& pr = p.prob;
   const uint32_t bar0 = sbase + L::oBar;
@@ -584,8 +712,11 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
   tma_prefetch_desc(&p.tm_k);
   tma_prefetch_desc(&p.tm_v);
 
-  for (int task = blockIdx.x; task < static_cast<int>(pr.num_tasks); task += gridDim.x) {
-    const Task tk = decode_task(pr, task);
+  const int num_tasks = task_count<VARLEN>(p);
+  for (int kt = 0;; ++kt) {
+    const int task = post_task<DQ, DV, DYN>(p, kt, num_tasks, bar0, ring, wc);
+    if (task < 0) break;  // no task left, or an abort
+    const Task tk = get_task<VARLEN>(p, task);
     if (tk.nmax == 0) continue;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -595,7 +726,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
       mbar_arrive_expect_tx(qb, L::NQC * kChunkBytes);
       const uint32_t dst = sbase + L::oQ + static_cast<uint32_t>(s * L::kQBytes);
       for (int c = 0; c < L::NQC; ++c)
-        tma_load_5d(dst + c * kChunkBytes, &p.tm_q, qb, c * 64, 0, tk.g, tk.pos0[s], tk.b);
+        tma_load_5d(dst + c * kChunkBytes, &p.tm_q, qb, c * 64, 0, tk.g, tk.q_row0 + tk.pos0[s], tk.bc);
       ++q_uses[s];
     }
     for (int j = 0; j < tk.nmax; ++j) {
@@ -611,7 +742,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
         mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nch * kChunkBytes));
         for (int c = 0; c < nch; ++c)
           tma_load_4d(dst + c * kChunkBytes, which == 0 ? static_cast<const void*>(&p.tm_k) : &p.tm_v, fb,
-                      c * 64, tk.kvh, j * kBN, tk.b);
+                      c * 64, tk.kvh, tk.k_row0 + j * kBN, tk.bc);
         ++kv_it;
       }
     }
@@ -630,7 +761,7 @@ out:
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL, bool EMU>
+template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = Layout<DQ, DV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -640,6 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
   float* mbox = reinterpret_cast<float*>(smem + L::oMbox);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::oTaskRing);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -662,6 +794,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     mbar_init(b + 8 * L::bEpiFull, 128);
     mbar_init(b + 8 * L::bStageFree, 1);
     mbar_init(b + 8 * L::bDrain, 1);
+    for (int r = 0; r < kTaskRing; ++r) {
+      mbar_init(b + 8 * (L::bTaskFull + r), 1);
+      mbar_init(b + 8 * (L::bTaskEmpty + r), kTaskReaders);
+    }
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -678,17 +814,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   // register budget: 128 x (176 + 176 + 104 + 56) = 65536
   if (warp < 8) {
     setmaxnreg_inc<176>();
-    softmax_role<DQ, DV, CAUSAL, EMU>(p, warp >> 2, tmem, sbase, mbox, wc);
+    softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
-    correction_role<DQ, DV, CAUSAL>(p, tmem, sbase, smem, mbox, wc);
+    correction_role<DQ, DV, CAUSAL, VARLEN, DYN>(p, tmem, sbase, smem, mbox, ring, wc);
   } else {
     setmaxnreg_dec<56>();
     if (warp == 12) {
-      mma_role<DQ, DV>(p, tmem, sbase, wc);
+      mma_role<DQ, DV, VARLEN, DYN>(p, tmem, sbase, ring, wc);
       __syncwarp();
     } else if (warp == 13) {
-      if (lane == 0) load_role<DQ, DV>(p, sbase, wc);
+      if (lane == 0) load_role<DQ, DV, VARLEN, DYN>(p, sbase, ring, wc);
       __syncwarp();
     }
   }

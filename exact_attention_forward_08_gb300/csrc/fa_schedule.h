@@ -17,9 +17,22 @@
 //  * n_blocks(stage) is the number of 128-key blocks the tile visits: all of
 //    them without a mask; under the bottom-right causal mask only blocks that
 //    hold a key j <= pos_last + Sk - Sq (future blocks are skipped).
-//  * Task order: linear for the non-causal case (uniform cost); for the causal
-//    case longest-processing-time first (m_blocks in decreasing order) inside
-//    sections of `section_units` (b, g) units whose K/V fit in L2 together.
+//  * Task order: linear for the non-causal case (uniform cost).  For the
+//    causal case longest-processing-time first: the heavier half of the
+//    m_blocks (m >= M - ceil(M/2)) in decreasing order inside sections of
+//    `section_units` (b, g) units whose K/V fit in L2 together, then the
+//    lighter half level by level (m decreasing, all units per level).  Light
+//    tasks read only the first half of a unit's K/V, and ending the list with
+//    the cheapest tasks keeps the last CTAs from finishing late (a static
+//    round-robin over "heaviest first per section" alone left the busiest CTA
+//    with 11-29 % more work than the average; this order halves that, and a
+//    dynamic assignment over it comes within about 1 %).
+//  * Variable-length batches (sequences packed back to back, offsets in
+//    cu_seqlens): a planning kernel sorts the sequences by the cost of their
+//    heaviest tile, longest first ("FlashAttention-4 wiki", "Core methods",
+//    LPT scheduling: varlen batches are ordered by a preprocessing kernel),
+//    and lists every sequence's tasks in the order above, one sequence after
+//    the other.  The persistent CTAs then walk that list.
 #pragma once
 #include <cstdint>
 
@@ -45,6 +58,7 @@ struct Problem {
   int kv_blocks;      // ceil(Sk / kBN)
   int ratio;          // Hq / Hkv
   int section_units;  // causal task order: (b, g) units per L2 section
+  int heavy_levels;   // causal task order: m_blocks M-1 .. M-heavy_levels go by sections
   int64_t num_tasks;  // B * groups * mblocks
 };
 
@@ -54,6 +68,17 @@ struct Task {
   int pos0[2];   // first sequence position of each stage's tile
   int n[2];      // K/V blocks each stage visits (0: nothing to do)
   int nmax;      // max(n[0], n[1])
+  int sq, sk;    // query and key count of this task's sequence
+  int q_row0;    // row of position 0 in the Q/O view (varlen: cu_seqlens_q[b]; else 0)
+  int k_row0;    // row of key 0 in the K/V view (varlen: cu_seqlens_k[b]; else 0)
+  int bc;        // batch coordinate in the TMA views (varlen: 0; else b)
+};
+
+// One task of a variable-length batch as the planning kernel writes it
+// (32 bytes, read with two 16-byte loads).
+struct alignas(16) VarlenTask {
+  int b, g, mb, reserved;
+  int q_row0, sq, k_row0, sk;
 };
 
 FA_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -85,19 +110,25 @@ FA_HD Problem make_problem(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int
   if (su < 1) su = 1;
   if (su > units) su = units > 0 ? units : 1;
   p.section_units = static_cast<int>(su);
+  p.heavy_levels = (p.mblocks + 1) / 2;
   return p;
 }
 
-// K/V blocks a Q tile starting at pos0 visits.
-FA_HD int tile_blocks(const Problem& p, int pos0) {
-  if (pos0 >= p.Sq || p.kv_blocks == 0) return 0;
-  if (!p.causal) return p.kv_blocks;
-  int last = pos0 + p.pos_per_tile;
-  if (last > p.Sq) last = p.Sq;
-  const int64_t max_key = static_cast<int64_t>(last - 1) + p.Sk - p.Sq;
+// K/V blocks a Q tile starting at pos0 visits, in a sequence of sq queries
+// and sk keys (kvb = ceil(sk / kBN) blocks), ppt positions per tile.
+FA_HD int tile_blocks_len(int sq, int sk, int kvb, int causal, int ppt, int pos0) {
+  if (pos0 >= sq || kvb == 0) return 0;
+  if (!causal) return kvb;
+  int last = pos0 + ppt;
+  if (last > sq) last = sq;
+  const int64_t max_key = static_cast<int64_t>(last - 1) + sk - sq;
   if (max_key < 0) return 0;
   const int64_t n = max_key / kBN + 1;
-  return n < p.kv_blocks ? static_cast<int>(n) : p.kv_blocks;
+  return n < kvb ? static_cast<int>(n) : kvb;
+}
+
+FA_HD int tile_blocks(const Problem& p, int pos0) {
+  return tile_blocks_len(p.Sq, p.Sk, p.kv_blocks, p.causal, p.pos_per_tile, pos0);
 }
 
 // Task t (0 <= t < num_tasks < 2^31; the host refuses larger problems).
@@ -109,21 +140,30 @@ FA_HD Task decode_task(const Problem& p, int t) {
     unit = t / M;
     mb = t - unit * M;
   } else {
-    const int su = p.section_units;
     const int units = p.B * p.groups;
-    const int section = t / (su * M);
-    const int first_unit = section * su;
-    int in_section = units - first_unit;
-    if (in_section > su) in_section = su;
-    const int idx = t - section * su * M;
-    const int q = idx / in_section;
-    mb = M - 1 - q;  // heaviest m_block first
-    unit = first_unit + (idx - q * in_section);
+    const int Mh = p.heavy_levels;
+    if (t < units * Mh) {  // heavier half: L2 sections, m_block decreasing inside each
+      const int su = p.section_units;
+      const int section = t / (su * Mh);
+      const int first_unit = section * su;
+      int in_section = units - first_unit;
+      if (in_section > su) in_section = su;
+      const int idx = t - section * su * Mh;
+      const int q = idx / in_section;
+      mb = M - 1 - q;
+      unit = first_unit + (idx - q * in_section);
+    } else {  // lighter half: one level (m_block) at a time over all units
+      const int idx = t - units * Mh;
+      const int q = idx / units;
+      mb = M - 1 - Mh - q;
+      unit = idx - q * units;
+    }
   }
   k.b = unit / p.groups;
   k.g = unit - k.b * p.groups;
   k.mb = mb;
   k.kvh = (k.g * p.pack) / p.ratio;
+  k.sq = p.Sq, k.sk = p.Sk, k.q_row0 = 0, k.k_row0 = 0, k.bc = k.b;
   k.nmax = 0;
   for (int s = 0; s < 2; ++s) {
     k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
@@ -135,10 +175,82 @@ FA_HD Task decode_task(const Problem& p, int t) {
 
 // Does K/V block j need the element mask for a tile starting at pos0?  (the
 // sequence tail, or the causal diagonal)
-FA_HD bool block_needs_mask(const Problem& p, int pos0, int j) {
+FA_HD bool block_needs_mask_len(int sq, int sk, int causal, int pos0, int j) {
   const int64_t key_hi = static_cast<int64_t>(j) * kBN + kBN - 1;
-  if (key_hi >= p.Sk) return true;
-  return p.causal && key_hi > static_cast<int64_t>(pos0) + p.Sk - p.Sq;
+  if (key_hi >= sk) return true;
+  return causal && key_hi > static_cast<int64_t>(pos0) + sk - sq;
+}
+
+FA_HD bool block_needs_mask(const Problem& p, int pos0, int j) {
+  return block_needs_mask_len(p.Sq, p.Sk, p.causal, pos0, j);
+}
+
+// The first K/V block that needs the mask (every later one needs it too):
+// the tail starts at block sk / kBN; under the causal mask block j hides a
+// key of the tile once j * kBN + kBN - 1 > pos0 + sk - sq.
+FA_HD int first_masked_block(int sq, int sk, int causal, int pos0) {
+  int j = sk / kBN;
+  if (causal) {
+    const int64_t c1 = static_cast<int64_t>(pos0) + sk - sq + 1;
+    const int jc = c1 > 0 ? static_cast<int>(c1 / kBN) : 0;
+    if (jc < j) j = jc;
+  }
+  return j;
+}
+
+// ---------------------------------------------------------------------------
+// variable-length batches
+// ---------------------------------------------------------------------------
+// Upper bound on the tasks of any variable-length batch of `batch` sequences
+// holding total_q queries: a sequence of sq queries has groups * ceil(sq * pack
+// / 256) tasks, at most Hq * (sq / 256 + 1) whatever the pack.
+FA_HD int64_t varlen_max_tasks(int batch, int heads_q, int64_t total_q) {
+  return static_cast<int64_t>(heads_q) * ((total_q + 2 * kBM - 1) / (2 * kBM) + batch);
+}
+
+// Sort key of a sequence for the longest-first order: the K/V blocks of its
+// heaviest tile.  Every tile of a non-causal sequence, and the last tile of a
+// causal one (its last query sees key sk - 1), visits all ceil(sk / 128)
+// blocks.  Sequences without queries have no tasks and sort last.
+FA_HD int varlen_key(int sq, int sk) { return sq > 0 ? ceil_div(sk, kBN) : -1; }
+
+// Sequence a comes before sequence b: larger key first, then lower index.
+// Packed into one unsigned 64-bit value so that a descending sort of the
+// values gives this order (index i is stored as ~i).
+FA_HD uint64_t varlen_sort_value(int key, int index) {
+  return (static_cast<uint64_t>(static_cast<uint32_t>(key + 1)) << 32) | static_cast<uint32_t>(~index);
+}
+FA_HD int varlen_sort_index(uint64_t value) { return static_cast<int>(~static_cast<uint32_t>(value)); }
+
+// Tasks of one sequence: the fixed-length decomposition of a batch of one.
+FA_HD Problem varlen_sequence_problem(const Problem& base, int sq, int sk, int d_qk, int d_v,
+                                      int64_t l2_budget_bytes) {
+  return make_problem(1, base.Hq, base.Hkv, sq, sk, d_qk, d_v, base.causal, l2_budget_bytes, base.pack);
+}
+
+// Record of the i-th task of sequence b (rows q_row0.., k_row0.. of the packed views).
+FA_HD VarlenTask varlen_record(const Problem& seq, int b, int q_row0, int k_row0, int i) {
+  const Task t = decode_task(seq, i);
+  VarlenTask r;
+  r.b = b, r.g = t.g, r.mb = t.mb, r.reserved = 0;
+  r.q_row0 = q_row0, r.sq = seq.Sq, r.k_row0 = k_row0, r.sk = seq.Sk;
+  return r;
+}
+
+// The task the kernel runs for a record.
+FA_HD Task task_from_record(const Problem& p, const VarlenTask& r) {
+  Task k;
+  k.b = r.b, k.g = r.g, k.mb = r.mb;
+  k.kvh = (k.g * p.pack) / p.ratio;
+  k.sq = r.sq, k.sk = r.sk, k.q_row0 = r.q_row0, k.k_row0 = r.k_row0, k.bc = 0;
+  const int kvb = ceil_div(r.sk, kBN);
+  k.nmax = 0;
+  for (int s = 0; s < 2; ++s) {
+    k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
+    k.n[s] = tile_blocks_len(r.sq, r.sk, kvb, p.causal, p.pos_per_tile, k.pos0[s]);
+    if (k.n[s] > k.nmax) k.nmax = k.n[s];
+  }
+  return k;
 }
 
 }  // namespace fa

@@ -47,6 +47,7 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -98,7 +99,17 @@ typedef struct fa_options {
                          pipe with a degree-3 polynomial instead of the MUFU ex2 unit
                          ("FlashAttention-4 wiki", "Core methods": partial exp emulation);
                          0 (default): MUFU only.  Any other value is rejected. */
+  void* workspace;    /* fixed-length calls: NULL (default) assigns tasks to the persistent
+                         CTAs round-robin; a device buffer of FA_SCHED_WORKSPACE_BYTES,
+                         16-byte aligned, assigns them dynamically (each CTA takes the next
+                         task from a counter in it, which the call clears on the stream first;
+                         the pages' persistent scheduler with a task counter, "Flash Attention
+                         4 on Blackwell", "Scheduling").  Calls that may overlap on different
+                         streams need different buffers.  Not combinable with exp_emu; must
+                         be NULL for the varlen calls (they take their own workspace). */
 } fa_options;
+
+#define FA_SCHED_WORKSPACE_BYTES 16
 
 /* Fill `opts` with the defaults. */
 void fa_options_default(fa_options* opts);
@@ -116,9 +127,72 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
 int fa_selftest_exp2(const float* x, float* y_fma, float* y_mufu, int n, fa_stream_t stream);
 
 /*
+ * Variable-length batches: `batch` sequences of different lengths packed back
+ * to back ("FlashAttention-4 wiki", "Core methods" and "Limitations": varlen
+ * is supported, with a preprocessing kernel that orders the batch longest
+ * first).  Sequence b holds queries cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and
+ * keys cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1; each sequence is an independent
+ * attention problem with the same heads, head dims, scale and mask rule as
+ * fa_fwd (causal = bottom-right inside each sequence).
+ *
+ * Layouts (dense, contiguous):
+ *   q   [total_q, heads_q,  d_qk]  bf16
+ *   k   [total_k, heads_kv, d_qk]  bf16
+ *   v   [total_k, heads_kv, d_v ]  bf16
+ *   o   [total_q, heads_q,  d_v ]  bf16 (rows of the sequences written; other rows untouched)
+ *   lse [heads_q, total_q]         fp32, natural log (may be NULL)
+ *   cu_seqlens_q, cu_seqlens_k     int32 [batch + 1], device memory
+ * The offsets must satisfy 0 <= cu[b] <= cu[b+1] <= total.  They live on the
+ * device, so they are checked there: on a violation nothing is computed and
+ * the status word (fa_device_status) reports FA_ERR_INVALID_ARG with site 501
+ * and the first bad sequence index.  q rows past the end of a sequence may be
+ * read (and ignored), never written.
+ *
+ * workspace: caller-owned device memory, 16-byte aligned, at least
+ * fa_varlen_workspace_size(batch, heads_q, total_q) bytes.  Each call writes
+ * its task list there (an int task count at byte 0, fa_varlen_task records
+ * from byte 256) with a one-block planning kernel and the attention kernel
+ * reads it, both on `stream`; calls ordered on one stream may share a
+ * workspace, concurrent calls may not.
+ *
+ * batch <= 16384; total_q + total_k < 2^31 - 512.  total_k == 0 writes O = 0
+ * and lse = -inf for every query row.  fa_options.exp_emu must be 0
+ * (FA_ERR_UNSUPPORTED otherwise).  Other arguments as for fa_fwd_ex.
+ */
+typedef struct fa_varlen_task {
+  int b, g, mblock, reserved;   /* sequence, head group, m_block (as fa_task) */
+  int q_row0, seqlen_q;         /* cu_seqlens_q[b], its query count */
+  int k_row0, seqlen_k;         /* cu_seqlens_k[b], its key count */
+} fa_varlen_task;
+
+size_t fa_varlen_workspace_size(int batch, int heads_q, int64_t total_q);
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int batch, int64_t total_q, int64_t total_k, int heads_q,
+                  int heads_kv, int d_qk, int d_v, int causal, float scale, void* workspace,
+                  size_t workspace_bytes, fa_stream_t stream);
+
+int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int64_t total_q,
+                     int64_t total_k, int heads_q, int heads_kv, int d_qk, int d_v, int causal, float scale,
+                     void* workspace, size_t workspace_bytes, const fa_options* opts, fa_stream_t stream);
+
+/*
+ * Host-only copy of the planning kernel's task list (no CUDA call): the same
+ * records in the same order, for host cu_seqlens arrays.  l2_bytes is the L2
+ * budget of the causal sections (0 selects 64 MiB; the kernel uses half the
+ * device's L2).  Writes min(count, capacity) records to `out` (may be NULL)
+ * and the task count to *count.
+ */
+int fa_varlen_plan_host(const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int heads_q, int heads_kv,
+                        int d_qk, int d_v, int causal, int64_t l2_bytes, int pack, fa_varlen_task* out,
+                        int64_t capacity, int64_t* count);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status
- * word.  *out receives FA_OK or FA_ERR_DEVICE_TIMEOUT; detail (may be NULL)
- * receives {code, wait site, block index}.  Returns FA_OK or FA_ERR_CUDA.
+ * word.  *out receives FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_INVALID_ARG (a
+ * varlen call found bad cu_seqlens); detail (may be NULL) receives
+ * {code, site, block or sequence index}.  Returns FA_OK or FA_ERR_CUDA.
  */
 int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]);
 
@@ -133,7 +207,9 @@ int fa_version(void);
  * A task is (batch b, head group g, m_block): two consecutive 128-row Q tiles
  * ("stages") that stream the same K/V blocks ("Flash Attention 4 on
  * Blackwell", section "Scheduling": tasks (batch, kv_head, m_block), each
- * m_block holding two Q stages; causal tasks run longest first).
+ * m_block holding two Q stages; causal tasks run longest first).  Causal
+ * order: the heavier half of the m_blocks in L2 sections (decreasing m inside
+ * a section), then the lighter half one m_block level at a time.
  */
 typedef struct fa_plan {
   int batch, heads_q, heads_kv, seqlen_q, seqlen_k, causal;
@@ -145,6 +221,8 @@ typedef struct fa_plan {
   int kv_blocks;       /* ceil(seqlen_k / 128) */
   int ratio;           /* heads_q / heads_kv */
   int section_units;   /* causal order: (b, g) units per L2 section */
+  int heavy_levels;    /* causal order: the top heavy_levels m_blocks go section by section,
+                          the rest level by level over all units */
   int64_t num_tasks;
 } fa_plan;
 
@@ -161,6 +239,10 @@ int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out);
 
 /* Does block j need the element mask for a tile starting at pos0? (host view) */
 int fa_plan_block_masked(const fa_plan* plan, int pos0, int j);
+
+/* The first block that needs it; the kernel masks exactly the blocks j >= this
+   index (the tail and the causal diagonal only grow with j). */
+int fa_plan_first_masked_block(const fa_plan* plan, int pos0);
 
 #ifdef __cplusplus
 }

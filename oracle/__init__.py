@@ -118,3 +118,52 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, rows=Non
 def row_ids(b, i, h, Sq: int, Hq: int) -> np.ndarray:
     """Linear row ids r = (b*Sq + i)*Hq + h."""
     return (np.asarray(b, dtype=np.int64) * Sq + np.asarray(i, dtype=np.int64)) * Hq + np.asarray(h, dtype=np.int64)
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool = False, scale: float | None = None,
+                    rows=None, threads: int | None = None, lib=None):
+    """Reference attention forward of a variable-length batch.
+
+    Sequence b holds queries cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of
+    q [total_q, Hq, dqk] and keys cu_seqlens_k[b] .. of k [total_k, Hkv, dqk],
+    v [total_k, Hkv, dv]; each sequence is its own attention problem (its own
+    softmax rows and, with ``causal``, its own bottom-right mask), so this is
+    ``attn_fwd`` on every sequence as a batch of one.
+
+    rows=None: returns (O [total_q, Hq, dv], LSE [Hq, total_q]) as float64; query
+    rows outside every sequence are NaN.  rows = int64 array of (t, h) pairs
+    (shape [n, 2], t a packed query row): returns (O [n, dv], LSE [n]).
+    """
+    cu_q = [int(x) for x in cu_seqlens_q]
+    cu_k = [int(x) for x in cu_seqlens_k]
+    total_q, Hq, _ = q.shape
+    dv = v.shape[2]
+    seq_of = np.full(total_q, -1, dtype=np.int64)
+    for b in range(len(cu_q) - 1):
+        seq_of[cu_q[b]:cu_q[b + 1]] = b
+    if rows is None:
+        o = np.full((total_q, Hq, dv), np.nan)
+        lse = np.full((Hq, total_q), np.nan)
+        for b in range(len(cu_q) - 1):
+            q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+            if q1 == q0:
+                continue
+            ob, lb = attn_fwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], causal, scale, threads=threads, lib=lib)
+            o[q0:q1] = ob[0]
+            lse[:, q0:q1] = lb[0]
+        return o, lse
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 2)
+    o = np.empty((rows.shape[0], dv))
+    lse = np.empty(rows.shape[0])
+    seqs = seq_of[rows[:, 0]]
+    if (seqs < 0).any():
+        raise ValueError("a requested row lies outside every sequence")
+    for b in np.unique(seqs):
+        sel = np.nonzero(seqs == b)[0]
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        ids = row_ids(0, rows[sel, 0] - q0, rows[sel, 1], q1 - q0, Hq)
+        ob, lb = attn_fwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], causal, scale, rows=ids, threads=threads,
+                          lib=lib)
+        o[sel] = ob
+        lse[sel] = lb
+    return o, lse

@@ -184,3 +184,98 @@ def workloads() -> dict:
                          k_offset=12.0,
                          notes="B2 H16 S16384 d_qk192 d_v128 causal, Q=4N(0,1), K=N(0,1)+0..12")
     return w
+
+
+# ---------------------------------------------------------------------------
+# variable-length batches (sequences packed back to back)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class VarlenWorkload:
+    """A variable-length batch: per-sequence query and key counts, the shared
+    heads / head dims / mask, and the input recipe (N(0,1) bf16 from seed)."""
+    name: str
+    seqlens_q: tuple
+    seqlens_k: tuple
+    heads_q: int
+    heads_kv: int
+    d_qk: int
+    d_v: int
+    causal: bool
+    seed: int
+    scale: float | None = None
+    notes: str = ""
+
+    @property
+    def batch(self) -> int:
+        return len(self.seqlens_q)
+
+    @property
+    def cu_seqlens_q(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.seqlens_q)]).astype(np.int32)
+
+    @property
+    def cu_seqlens_k(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.seqlens_k)]).astype(np.int32)
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.seqlens_q))
+
+    @property
+    def total_k(self) -> int:
+        return int(sum(self.seqlens_k))
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / float(np.sqrt(self.d_qk))
+
+    @property
+    def shapes(self):
+        return dict(q=(self.total_q, self.heads_q, self.d_qk), k=(self.total_k, self.heads_kv, self.d_qk),
+                    v=(self.total_k, self.heads_kv, self.d_v), o=(self.total_q, self.heads_q, self.d_v),
+                    lse=(self.heads_q, self.total_q))
+
+    def flops(self) -> float:
+        """Sum over sequences of 2*Hq*sq*sk*(d_qk + d_v), halved for causal."""
+        f = sum(2.0 * self.heads_q * sq * sk * (self.d_qk + self.d_v) for sq, sk in zip(self.seqlens_q,
+                                                                                        self.seqlens_k))
+        return f / 2 if self.causal else f
+
+    def algorithmic_bytes(self) -> int:
+        s = self.shapes
+        n = lambda t: int(np.prod(t))
+        return 2 * (n(s["q"]) + n(s["k"]) + n(s["v"]) + n(s["o"])) + 4 * n(s["lse"])
+
+    def generate(self):
+        """(q, k, v) bf16 bit arrays, packed [total, heads, d]."""
+        s = self.shapes
+        return (normal_bf16(s["q"], self.seed, STREAM_Q, 1.0), normal_bf16(s["k"], self.seed, STREAM_K, 1.0),
+                normal_bf16(s["v"], self.seed, STREAM_V, 1.0))
+
+
+def loguniform_lengths(total: int, lo: int, hi: int, seed: int) -> tuple:
+    """Sequence lengths drawn log-uniformly in [lo, hi] (numpy PCG64, seeded)
+    until they hold `total` tokens; the last one is cut to fit exactly."""
+    rng = np.random.default_rng(seed)
+    out, left = [], total
+    while left > 0:
+        n = int(round(float(np.exp(rng.uniform(np.log(lo), np.log(hi))))))
+        n = min(max(n, lo), hi, left)
+        out.append(n)
+        left -= n
+    return tuple(out)
+
+
+def varlen_workloads() -> dict:
+    """Variable-length batches at the benchmark grid's 32k total tokens, 16
+    heads of 128 (lengths 128..8192, log-uniform), causal and non-causal."""
+    lens = loguniform_lengths(32768, 128, 8192, seed=41)
+    w = {}
+    w["varlen32k"] = VarlenWorkload("varlen32k", lens, lens, 16, 16, 128, 128, True, seed=41,
+                                    notes=f"{len(lens)} sequences, 32768 tokens, lengths 128..8192 log-uniform, "
+                                          "H16 d128 causal")
+    w["varlen32k_nc"] = VarlenWorkload("varlen32k_nc", lens, lens, 16, 16, 128, 128, False, seed=42,
+                                       notes=f"{len(lens)} sequences, 32768 tokens, lengths 128..8192 "
+                                             "log-uniform, H16 d128 non-causal")
+    return w

@@ -32,7 +32,8 @@ def test_header_declares_entry_points():
     names = _declared_functions()
     for required in ("fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_status_string", "fa_make_plan",
                      "fa_plan_task", "fa_options_default", "fa_version", "fa_plan_block_masked",
-                     "fa_selftest_exp2"):
+                     "fa_selftest_exp2", "fa_plan_first_masked_block", "fa_fwd_varlen", "fa_fwd_varlen_ex",
+                     "fa_varlen_workspace_size", "fa_varlen_plan_host"):
         assert required in names
 
 
@@ -88,6 +89,59 @@ def test_bad_options_rejected(fa):
         setattr(o, field, value)
         rc = fa.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 64, 128, 128, 0, 0.0, o, None)
         assert rc == 1, (field, value)
+
+
+VBASE = dict(batch=2, total_q=300, total_k=400, heads_q=4, heads_kv=2, d_qk=128, d_v=128, causal=1, scale=0.0)
+
+
+def _vcall(fa, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, cu_q=FAKE, cu_k=FAKE, ws=FAKE, ws_bytes=None, opts=None,
+           **kw):
+    a = dict(VBASE)
+    a.update(kw)
+    if ws_bytes is None:
+        ws_bytes = fa.fa_varlen_workspace_size(max(a["batch"], 0), max(a["heads_q"], 1), max(a["total_q"], 0))
+    return fa.fa_fwd_varlen_ex(q, k, v, o, lse, cu_q, cu_k, a["batch"], a["total_q"], a["total_k"], a["heads_q"],
+                               a["heads_kv"], a["d_qk"], a["d_v"], a["causal"], a["scale"], ws, ws_bytes, opts, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(k=None), 1), (dict(cu_q=None), 1), (dict(cu_k=None), 1),
+    (dict(ws=None), 1), (dict(ws=FAKE + 8), 1), (dict(cu_q=FAKE + 2), 1), (dict(q=FAKE + 8), 1),
+    (dict(batch=-1), 1), (dict(batch=16385), 1), (dict(total_q=-1), 1), (dict(total_k=-3), 1),
+    (dict(total_q=2 ** 30, total_k=2 ** 30), 1), (dict(heads_q=6, heads_kv=4), 1), (dict(scale=-1.0), 1),
+    (dict(d_qk=96, d_v=96), 2), (dict(d_qk=64, d_v=128), 2),
+])
+def test_varlen_invalid_arguments_rejected_before_cuda(fa, kw, code):
+    assert _vcall(fa, **kw) == code
+
+
+def test_sched_workspace_options(fa):
+    o = fa.default_options()
+    assert o.workspace is None
+    o.workspace = FAKE + 8  # misaligned
+    assert fa.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 64, 128, 128, 1, 0.0, o, None) == 1
+    o.workspace = FAKE
+    o.exp_emu = 1  # one or the other
+    assert fa.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 64, 128, 128, 1, 0.0, o, None) == 2
+    o = fa.default_options()
+    o.workspace = FAKE  # varlen calls take their own workspace
+    assert _vcall(fa, opts=o) == 1
+
+
+def test_varlen_workspace_too_small_and_exp_emu(fa):
+    need = fa.fa_varlen_workspace_size(2, 4, 300)
+    assert need == 256 + 32 * 4 * ((300 + 255) // 256 + 2)
+    assert _vcall(fa, ws_bytes=need - 1) == 1
+    o = fa.default_options()
+    o.exp_emu = 1
+    assert _vcall(fa, opts=o) == 2
+    assert fa.fa_varlen_workspace_size(-1, 4, 10) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(batch=0), dict(total_q=0)])
+def test_varlen_empty_is_ok_without_launch(fa, kw):
+    assert _vcall(fa, q=None, k=None, v=None, o=None, lse=None, cu_q=None, cu_k=None, ws=None, ws_bytes=0,
+                  **kw) == 0
 
 
 # ---------------------------------------------------------------------------
@@ -147,11 +201,19 @@ def test_plan_covers_every_row_once_with_exact_block_counts(fa, case):
         costs.append(nmax)
     assert np.all(seen == 1)
     if causal:
-        # longest first inside each L2 section
-        per_section = plan.section_units * plan.mblocks
-        for s0 in range(0, len(costs), per_section):
-            c = costs[s0:s0 + per_section]
+        # longest first: inside each L2 section of the heavier half, then over
+        # the whole lighter half; every heavy task costs at least every light one
+        units = B * plan.groups
+        nh = units * plan.heavy_levels
+        assert plan.heavy_levels == (plan.mblocks + 1) // 2
+        per_section = plan.section_units * plan.heavy_levels
+        for s0 in range(0, nh, per_section):
+            c = costs[s0:min(s0 + per_section, nh)]
             assert all(a >= b for a, b in zip(c, c[1:]))
+        light = costs[nh:]
+        assert all(a >= b for a, b in zip(light, light[1:]))
+        if light:
+            assert min(costs[:nh]) >= max(light)
 
 
 def test_plan_sections_follow_l2_budget(fa):

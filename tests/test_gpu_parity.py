@@ -262,3 +262,47 @@ def test_exp2_fma_path_parity(fa, case):
     opts = fa.default_options()
     opts.exp_emu = 1
     full_check(fa, w, options=opts)
+
+
+DYN_CASES = ["ragged", "causal384", "causal_empty_rows", "gqa4", "ratio3", "d128_v64", "many_tasks", "asym_offset"]
+
+
+@pytest.mark.parametrize("name", DYN_CASES)
+def test_dynamic_assignment_matches_static_bitwise(fa, name):
+    """With a scheduling workspace the CTAs take tasks from a counter instead
+    of round-robin; every task computes the same tiles, so O and LSE must be
+    bit-identical.  The workspace is reused (the call clears the counter) and
+    small grids are covered."""
+    case = next(c for c in SMALL if c[0] == name)
+    _, B, Hq, Hkv, Sq, Sk, dq, dv, causal, extra = case
+    w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, seed=zlib.crc32(name.encode()) % 1000, **extra)
+    q, k, v = (to_dev(a) for a in w.generate())
+    o_s, l_s = fa.attention_forward(q, k, v, causal=causal, scale=w.softmax_scale)
+    ws = torch.full((fa.SCHED_WORKSPACE_BYTES,), 0x7F, dtype=torch.uint8, device="cuda")  # stale contents
+    for grid in (0, 0, 3, 1):
+        opts = fa.default_options()
+        opts.grid = grid
+        o_d, l_d = fa.attention_forward(q, k, v, causal=causal, scale=w.softmax_scale, options=opts, workspace=ws)
+        torch.cuda.synchronize()
+        code, detail = fa.fa_device_status()
+        assert code == 0, detail
+        assert torch.equal(o_d, o_s) and torch.equal(l_d, l_s), (name, grid)
+
+
+@pytest.mark.slow
+def test_dynamic_assignment_full_size_sampled(fa):
+    w = synthetic.workloads()["causal8k"]
+    q, k, v = w.generate()
+    ws = torch.zeros(fa.SCHED_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    o, lse = fa.attention_forward(to_dev(q), to_dev(k), to_dev(v), causal=True, scale=w.softmax_scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    r = np.random.default_rng(8)
+    b = r.integers(0, w.batch, 300)
+    i = np.concatenate([r.integers(0, w.seqlen_q, 280), np.arange(20) * 401 % w.seqlen_q])
+    h = r.integers(0, w.heads_q, 300)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, causal=True, scale=w.softmax_scale,
+                                   rows=oracle.row_ids(b, i, h, w.seqlen_q, w.heads_q))
+    og = o.float().cpu().numpy().astype(np.float64)[b, i, h]
+    lg = lse.cpu().numpy().astype(np.float64)[b, h, i]
+    compare(og, lg, o_ref, l_ref, "causal8k dynamic")
