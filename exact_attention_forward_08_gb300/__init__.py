@@ -23,7 +23,7 @@ import os
 from . import _build
 
 __all__ = ["fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_varlen_ex", "fa_varlen_workspace_size",
-           "fa_varlen_plan_host", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
+           "fa_varlen_plan_host", "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
            "fa_plan_task", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
            "FaTask", "FaVarlenTask", "attention_forward", "attention_forward_varlen", "FaError", "load_library",
            "LIB_PATH", "STATUS", "VARLEN_HEADER_BYTES"]
@@ -115,6 +115,10 @@ def load_library(path: str | None = None):
     lib.fa_fwd_varlen.restype = _I
     lib.fa_fwd_varlen_ex.argtypes = vl + [ctypes.POINTER(FaOptions), _P]
     lib.fa_fwd_varlen_ex.restype = _I
+    lib.fa_fwd_varlen_noalloc.argtypes = vl[:16] + [_P]
+    lib.fa_fwd_varlen_noalloc.restype = _I
+    lib.fa_noalloc_scratch_bytes.argtypes = []
+    lib.fa_noalloc_scratch_bytes.restype = ctypes.c_size_t
     lib.fa_varlen_plan_host.argtypes = [_P, _P] + [_I] * 6 + [ctypes.c_int64, _I, ctypes.POINTER(FaVarlenTask),
                                                              ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]
     lib.fa_varlen_plan_host.restype = _I
@@ -211,6 +215,17 @@ def fa_fwd_varlen_ex(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads
     return load_library().fa_fwd_varlen_ex(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv,
                                            d_qk, d_v, int(causal), float(scale), workspace, workspace_bytes,
                                            ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def fa_fwd_varlen_noalloc(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv, d_qk, d_v,
+                          causal, scale, stream) -> int:
+    """``fa_fwd_varlen_noalloc``: the varlen call with the library's static scratch (no workspace)."""
+    return load_library().fa_fwd_varlen_noalloc(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q,
+                                                heads_kv, d_qk, d_v, int(causal), float(scale), stream)
+
+
+def fa_noalloc_scratch_bytes() -> int:
+    return load_library().fa_noalloc_scratch_bytes()
 
 
 def fa_varlen_plan_host(cu_q, cu_k, heads_q, heads_kv, d_qk, d_v, causal, l2_bytes=0, pack=0):

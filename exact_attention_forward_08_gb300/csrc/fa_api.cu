@@ -20,6 +20,12 @@
 // {code, wait site, block} of the first device-side failure since the last read
 __device__ unsigned int g_fa_status[4];
 
+// Scratch of fa_fwd_varlen_noalloc: the varlen planning workspace (task count,
+// task counter, task records) as a file-scope device array, one per device.
+// 1 MiB holds (2^20 - 256) / 32 = 32 760 task records.
+constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
+__device__ __align__(256) unsigned char g_fa_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -44,6 +50,7 @@ struct DeviceState {
   int64_t l2_bytes = 0;
   int smem_optin = 0;
   unsigned int* status = nullptr;
+  void* noalloc_scratch = nullptr;  // g_fa_noalloc_scratch on this device
   bool kernel_ready[kNumKernels] = {};
   bool plan_ready = false;
 };
@@ -97,6 +104,11 @@ int init_device(int dev, DeviceState** out) {
     if (cudaGetSymbolAddress(&sym, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
     st.status = static_cast<unsigned int*>(sym);
     if (cudaMemset(st.status, 0, sizeof(unsigned int) * 4) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaGetSymbolAddress(&sym, g_fa_noalloc_scratch) != cudaSuccess) return FA_ERR_CUDA;
+    st.noalloc_scratch = sym;
+    // the header (task count, task counter) starts cleared; every call's
+    // planning kernel rewrites both before the attention kernel reads them
+    if (cudaMemset(st.noalloc_scratch, 0, kVarlenHeaderBytes) != cudaSuccess) return FA_ERR_CUDA;
     if (g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -473,10 +485,12 @@ size_t fa_varlen_workspace_size(int batch, int heads_q, int64_t total_q) {
   return kVarlenHeaderBytes + sizeof(fa::VarlenTask) * static_cast<size_t>(fa::varlen_max_tasks(batch, heads_q, total_q));
 }
 
-int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
-                     const int* cu_seqlens_k, int batch, int64_t total_q, int64_t total_k, int heads_q,
-                     int heads_kv, int d_qk, int d_v, int causal, float scale, void* workspace,
-                     size_t workspace_bytes, const fa_options* opts, fa_stream_t stream_) {
+// The varlen forward; noalloc = true takes the workspace from the library's
+// static scratch instead of the caller (workspace arguments ignored).
+static int varlen_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                      const int* cu_seqlens_k, int batch, int64_t total_q, int64_t total_k, int heads_q,
+                      int heads_kv, int d_qk, int d_v, int causal, float scale, void* workspace,
+                      size_t workspace_bytes, bool noalloc, const fa_options* opts, fa_stream_t stream_) {
   fa_options opt;
   fa_options_default(&opt);
   if (opts) opt = *opts;
@@ -495,7 +509,13 @@ int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float
   if (total_q + total_k + 4 * fa::kBM >= big) return FA_ERR_INVALID_ARG;
   const int64_t max_tasks = fa::varlen_max_tasks(batch, heads_q, total_q);
   if (max_tasks >= big) return FA_ERR_INVALID_ARG;
-  if (q == nullptr || o == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || workspace == nullptr)
+  if (noalloc) {  // the static scratch must hold this call's task list
+    if (fa_varlen_workspace_size(batch, heads_q, total_q) > kNoAllocScratchBytes) return FA_ERR_INVALID_ARG;
+    workspace = nullptr;
+    workspace_bytes = 0;
+  }
+  if (q == nullptr || o == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr ||
+      (!noalloc && workspace == nullptr))
     return FA_ERR_INVALID_ARG;
   if (total_k > 0 && (k == nullptr || v == nullptr)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace) ||
@@ -503,7 +523,7 @@ int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float
     return FA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
     return FA_ERR_INVALID_ARG;
-  if (workspace_bytes < fa_varlen_workspace_size(batch, heads_q, total_q)) return FA_ERR_INVALID_ARG;
+  if (!noalloc && workspace_bytes < fa_varlen_workspace_size(batch, heads_q, total_q)) return FA_ERR_INVALID_ARG;
   if (scale == 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d_qk));
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
@@ -512,6 +532,10 @@ int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float
   DeviceState* st = nullptr;
   rc = init_device(dev, &st);
   if (rc != FA_OK) return rc;
+  if (noalloc) {
+    workspace = st->noalloc_scratch;
+    workspace_bytes = kNoAllocScratchBytes;
+  }
   if (!is_device_ptr(q, dev) || !is_device_ptr(o, dev) || !is_device_ptr(cu_seqlens_q, dev) ||
       !is_device_ptr(cu_seqlens_k, dev) || !is_device_ptr(workspace, dev) ||
       (total_k > 0 && (!is_device_ptr(k, dev) || !is_device_ptr(v, dev))) ||
@@ -580,6 +604,24 @@ int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float
   if (entry.launch(p, static_cast<int>(grid), stream) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
+
+int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, int batch, int64_t total_q, int64_t total_k, int heads_q,
+                     int heads_kv, int d_qk, int d_v, int causal, float scale, void* workspace,
+                     size_t workspace_bytes, const fa_options* opts, fa_stream_t stream) {
+  return varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, heads_q, heads_kv, d_qk,
+                    d_v, causal, scale, workspace, workspace_bytes, false, opts, stream);
+}
+
+int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int64_t total_q,
+                          int64_t total_k, int heads_q, int heads_kv, int d_qk, int d_v, int causal, float scale,
+                          fa_stream_t stream) {
+  return varlen_fwd(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, heads_q, heads_kv, d_qk,
+                    d_v, causal, scale, nullptr, 0, true, nullptr, stream);
+}
+
+size_t fa_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_seqlens_q,
                   const int* cu_seqlens_k, int batch, int64_t total_q, int64_t total_k, int heads_q, int heads_kv,

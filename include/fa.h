@@ -178,6 +178,33 @@ int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float
                      void* workspace, size_t workspace_bytes, const fa_options* opts, fa_stream_t stream);
 
 /*
+ * fa_fwd_varlen without a caller workspace: the planning workspace lives in a
+ * file-scope device array of the library (fa_noalloc_scratch_bytes() bytes,
+ * 1 MiB, one per device; its address is looked up once per device at set-up).
+ * The pages have no counterpart: this is a convenience of this library for
+ * callers that cannot hand it scratch memory.  Nothing is allocated.
+ *
+ * A call whose task list needs more than the array holds
+ * (fa_varlen_workspace_size(batch, heads_q, total_q) > 1 MiB, about 32 760
+ * tasks) is rejected with FA_ERR_INVALID_ARG before any CUDA call.  Other
+ * arguments, errors and outputs as for fa_fwd_varlen.
+ *
+ * Race: every call on a device shares the one array.  Two calls that overlap
+ * in time (different streams without ordering between them, or host threads
+ * issuing concurrently to different streams) overwrite each other's task
+ * list and task counter, and their outputs are then undefined.  Calls
+ * ordered on one stream are safe; otherwise order them (events or
+ * synchronisation) or use fa_fwd_varlen with one workspace per stream.
+ */
+int fa_fwd_varlen_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int* cu_seqlens_q, const int* cu_seqlens_k, int batch, int64_t total_q,
+                          int64_t total_k, int heads_q, int heads_kv, int d_qk, int d_v, int causal,
+                          float scale, fa_stream_t stream);
+
+/* Bytes of the static scratch array used by fa_fwd_varlen_noalloc. */
+size_t fa_noalloc_scratch_bytes(void);
+
+/*
  * Host-only copy of the planning kernel's task list (no CUDA call): the same
  * records in the same order, for host cu_seqlens arrays.  l2_bytes is the L2
  * budget of the causal sections (0 selects 64 MiB; the kernel uses half the
