@@ -1,11 +1,13 @@
 """Benchmark: attention forward TFLOP/s on GB300 (BF16) and fraction of the
 dense BF16 tensor peak.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config mha8k] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config mha8k] [--impl ours|reference] [--dynamic]
 
 A step is one exact attention forward (the whole hot path) over the chosen
 workload, default the MHA non-causal configuration B4 H16 S8192 d128 (32k
-tokens).  Inputs are synthetic (seeded N(0,1) bf16) and resident in HBM when
+tokens); --config also takes the other fixed-length configurations and the
+variable-length batches (varlen32k, varlen32k_nc).  Inputs are synthetic
+(seeded N(0,1) bf16) and resident in HBM when
 the timed region starts; Q, K, V and O together (514 MiB) are larger than L2,
 so no flush is needed between steps.  Prints one JSON line (rank 0).
 
@@ -48,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--dynamic", action="store_true",
+                    help="fixed-length workloads: assign tasks dynamically (scheduling workspace)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -215,6 +219,56 @@ def rank_batch_seed(base_seed: int, rank: int) -> int:
 
 
 # ---------------------------------------------------------------------------
+# workloads: fixed-length (synthetic.workloads) and varlen (synthetic.varlen_workloads)
+# ---------------------------------------------------------------------------
+
+def get_workload(config: str):
+    import synthetic
+    fixed, varlen = synthetic.workloads(), synthetic.varlen_workloads()
+    if config in fixed:
+        return fixed[config]
+    if config in varlen:
+        return varlen[config]
+    raise SystemExit(f"unknown --config {config!r}; choose from {sorted(fixed) + sorted(varlen)}")
+
+
+def is_varlen(w) -> bool:
+    return hasattr(w, "cu_seqlens_q")
+
+
+def total_rows(w) -> int:
+    return w.total_q * w.heads_q if is_varlen(w) else w.batch * w.seqlen_q * w.heads_q
+
+
+def oracle_sample(w, q, k, v, n, rng, threads):
+    """Run the oracle on n uniformly drawn output rows; returns seconds."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    if is_varlen(w):
+        rows = np.stack([rng.integers(0, w.total_q, n), rng.integers(0, w.heads_q, n)], axis=1)
+        oracle.attn_fwd_varlen(q, k, v, w.cu_seqlens_q, w.cu_seqlens_k, causal=w.causal, scale=w.softmax_scale,
+                               rows=rows, threads=threads)
+    else:
+        rows = rng.integers(0, total_rows(w), size=n, dtype=np.int64)
+        oracle.attn_fwd(q, k, v, causal=w.causal, scale=w.softmax_scale, rows=rows, threads=threads)
+    return time.perf_counter() - t0
+
+
+def config_of(w, world: int, flops: float, dynamic: bool) -> dict:
+    common = {"heads_q": w.heads_q, "heads_kv": w.heads_kv, "d_qk": w.d_qk, "d_v": w.d_v, "causal": w.causal,
+              "flops_per_step_per_gpu": flops,
+              "l2": "inputs larger than L2 (Q+K+V+O %.0f MiB per GPU), no flush" % (w.algorithmic_bytes() / 2 ** 20),
+              "parallelism": f"weak x{world} (independent batches, no collective)",
+              "task_assignment": "dynamic (task counter)" if dynamic or is_varlen(w) else "static round-robin"}
+    if is_varlen(w):
+        return {"workload": f"{w.name}: {w.notes}", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
+                "total_tokens": w.total_q, "seq_len": max(w.seqlens_q), **common}
+    return {"workload": f"{w.name}: {w.notes}", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
+            "seq_len": w.seqlen_q, **common}
+
+
+# ---------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle on a bounded sample of the workload
 # ---------------------------------------------------------------------------
 
@@ -226,22 +280,15 @@ def cpu_baseline(w, q, k, v, seconds: float):
     import oracle
 
     threads = oracle.default_threads()
-    total_rows = w.batch * w.seqlen_q * w.heads_q
-    per_row = w.flops() / total_rows
+    rows_all = total_rows(w)
+    per_row = w.flops() / rows_all
     rng = np.random.default_rng(12345)
-
-    def run(n):
-        rows = rng.integers(0, total_rows, size=n, dtype=np.int64)
-        t0 = time.perf_counter()
-        oracle.attn_fwd(q, k, v, causal=w.causal, scale=w.softmax_scale, rows=rows, threads=threads)
-        return time.perf_counter() - t0
-
     n0 = max(threads * 4, 64)
-    dt0 = run(n0)  # calibration
-    n = int(min(total_rows, max(n0, n0 * seconds / max(dt0, 1e-3))))
-    dt = run(n)
+    dt0 = oracle_sample(w, q, k, v, n0, rng, threads)  # calibration
+    n = int(min(rows_all, max(n0, n0 * seconds / max(dt0, 1e-3))))
+    dt = oracle_sample(w, q, k, v, n, rng, threads)
     return {"value": n * per_row / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} of {total_rows} rows of {w.name} drawn uniformly (fp64 C oracle, {threads} threads, "
+            "sample": f"{n} of {rows_all} rows of {w.name} drawn uniformly (fp64 C oracle, {threads} threads, "
                       f"{dt:.1f} s)", "seconds": round(dt, 2), "rows": n}
 
 
@@ -250,11 +297,12 @@ def cpu_baseline(w, q, k, v, seconds: float):
 # ---------------------------------------------------------------------------
 
 def run_ours(args):
+    import dataclasses
+
     import numpy as np
     import torch
 
     import exact_attention_forward_08_gb300 as fa
-    import synthetic
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -262,8 +310,9 @@ def run_ours(args):
     dist_init("nccl" if world > 1 else "gloo")
     fa.load_library()
 
-    w0 = synthetic.workloads()[args.config]
-    w = synthetic.Workload(**{**w0.__dict__, "seed": rank_batch_seed(w0.seed, rank)})
+    w0 = get_workload(args.config)
+    w = dataclasses.replace(w0, seed=rank_batch_seed(w0.seed, rank))
+    varlen = is_varlen(w)
     qb, kb, vb = w.generate()
     to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
     qh, kh, vh = (to_t(a).pin_memory() for a in (qb, kb, vb))
@@ -273,12 +322,38 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     scale = w.softmax_scale
+    host_inputs, dev_inputs = [qh, kh, vh], [qd, kd, vd]
 
-    def step():
-        rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), w.batch,
-                       w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, sp)
-        if rc != 0:
-            raise fa.FaError(rc, "fa_fwd")
+    if varlen:
+        cqh = torch.from_numpy(w.cu_seqlens_q).pin_memory()
+        ckh = torch.from_numpy(w.cu_seqlens_k).pin_memory()
+        cqd, ckd = cqh.to(dev), ckh.to(dev)
+        host_inputs += [cqh, ckh]
+        dev_inputs += [cqd, ckd]
+        ws_bytes = fa.fa_varlen_workspace_size(w.batch, w.heads_q, w.total_q)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        launches_per_step = 2  # planning kernel + attention kernel
+
+        def step():
+            rc = fa.fa_fwd_varlen(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  cqd.data_ptr(), ckd.data_ptr(), w.batch, w.total_q, w.total_k, w.heads_q,
+                                  w.heads_kv, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, sp)
+            if rc != 0:
+                raise fa.FaError(rc, "fa_fwd_varlen")
+    else:
+        opts = None
+        if args.dynamic:
+            ws = torch.zeros(fa.SCHED_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+            opts = fa.default_options()
+            opts.workspace = ws.data_ptr()
+        launches_per_step = 1
+
+        def step():
+            rc = fa.fa_fwd_ex(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), w.batch,
+                              w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale,
+                              opts, sp)
+            if rc != 0:
+                raise fa.FaError(rc, "fa_fwd")
 
     for _ in range(args.warmup):
         step()
@@ -317,9 +392,8 @@ def run_ours(args):
     lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
 
     def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
+        for d_, h_ in zip(dev_inputs, host_inputs):
+            d_.copy_(h_, non_blocking=True)
         step()
         oh.copy_(o, non_blocking=True)
         lh.copy_(lse, non_blocking=True)
@@ -333,25 +407,20 @@ def run_ours(args):
         e2e_step()
     torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev) / args.e2e_steps
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
 
     peak, peak_src = load_peak()
     achieved = flops / (ms_step * 1e-3) / 1e12
-    traffic = stored_traffic(args.config)
+    traffic = stored_traffic(args.config) if not args.dynamic else None
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.notes}", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
-                   "heads_q": w.heads_q, "heads_kv": w.heads_kv, "seq_len": w.seqlen_q, "d_qk": w.d_qk,
-                   "d_v": w.d_v, "causal": w.causal, "flops_per_step_per_gpu": flops,
-                   "l2": "inputs larger than L2 (Q+K+V+O %.0f MiB per GPU), no flush" %
-                         (w.algorithmic_bytes() / 2 ** 20),
-                   "parallelism": f"weak x{world} (independent batches, no collective)"},
+        "config": config_of(w, world, flops, args.dynamic),
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_src} (bf16 dense, burst)",
@@ -375,41 +444,35 @@ def run_reference(args):
     minutes.  Rank 0 alone runs; other ranks exit without work."""
     import numpy as np
     import oracle
-    import synthetic
 
     rank, world, _ = dist_env()
     if rank != 0:
         return rank, None
-    w = synthetic.workloads()[args.config]
+    w = get_workload(args.config)
     q, k, v = w.generate()
     threads = oracle.default_threads()
-    total_rows = w.batch * w.seqlen_q * w.heads_q
-    per_row = w.flops() / total_rows
+    rows_all = total_rows(w)
+    per_row = w.flops() / rows_all
     rng = np.random.default_rng(777)
 
-    def one(n):
-        rows = rng.integers(0, total_rows, size=n, dtype=np.int64)
-        t0 = time.perf_counter()
-        oracle.attn_fwd(q, k, v, causal=w.causal, scale=w.softmax_scale, rows=rows, threads=threads)
-        return time.perf_counter() - t0
-
     n_cal = max(4 * threads, 64)
-    rate = n_cal / max(one(n_cal), 1e-3)  # rows per second
+    rate = n_cal / max(oracle_sample(w, q, k, v, n_cal, rng, threads), 1e-3)  # rows per second
     per_step_s = min(10.0, 120.0 / (args.steps + args.warmup))
-    n = int(max(threads, min(total_rows, rate * per_step_s)))
+    n = int(max(threads, min(rows_all, rate * per_step_s)))
     for _ in range(args.warmup):
-        one(n)
-    times = [one(n) for _ in range(args.steps)]
+        oracle_sample(w, q, k, v, n, rng, threads)
+    times = [oracle_sample(w, q, k, v, n, rng, threads) for _ in range(args.steps)]
     s_step = sum(times) / len(times)
     value = n * per_row / s_step / 1e12
-    sample = (f"{n} of {total_rows} rows of {w.name} per step, drawn uniformly; fp64 C oracle on {threads} "
+    sample = (f"{n} of {rows_all} rows of {w.name} per step, drawn uniformly; fp64 C oracle on {threads} "
               f"host threads")
+    cfg = config_of(w, 1, w.flops(), False)
+    cfg["rows_per_step"] = n
     result = {
         "metric": METRIC, "impl": "reference", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.notes}", "batch_per_gpu": w.batch, "global_batch": w.batch,
-                   "seq_len": w.seqlen_q, "rows_per_step": n},
+        "config": cfg,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
