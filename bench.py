@@ -5,8 +5,9 @@ dense BF16 tensor peak.
 
 A step is one exact attention forward (the whole hot path) over the chosen
 workload, default the MHA non-causal configuration B4 H16 S8192 d128 (32k
-tokens); --config also takes the other fixed-length configurations and the
-variable-length batches (varlen32k, varlen32k_nc).  Inputs are synthetic
+tokens); --config also takes the other fixed-length configurations, the
+variable-length batches (varlen32k, varlen32k_nc) and the decode problems
+(decode32k, decode_mqa, specdec: split-KV, HBM roofline).  Inputs are synthetic
 (seeded N(0,1) bf16) and resident in HBM when
 the timed region starts; Q, K, V and O together (514 MiB) are larger than L2,
 so no flush is needed between steps.  Prints one JSON line (rank 0).
@@ -36,6 +37,7 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 (BF16) and % of dense BF16 tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0  # burst bf16 of one earlier GB300 measurement
+FALLBACK_HBM_GBS = 6800.0      # copy bandwidth of one earlier GB300 measurement
 KERNEL_NAME = "fa_fwd_kernel"
 
 
@@ -52,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--dynamic", action="store_true",
                     help="fixed-length workloads: assign tasks dynamically (scheduling workspace)")
+    ap.add_argument("--splitkv", type=int, default=0,
+                    help="split-KV ranges for fixed-length workloads (decode workloads always split; 0 = auto there)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -64,15 +68,16 @@ def parse_args(argv=None):
 # peaks, clocks, ncu traffic
 # ---------------------------------------------------------------------------
 
-def load_peak():
-    """(TFLOP/s, source): the measured burst bf16 GEMM rate, else the fallback."""
+def load_peak(key: str = "bf16_tflops"):
+    """(value, source): the measured burst bf16 GEMM rate (TFLOP/s) or copy
+    bandwidth (hbm_gbs, GB/s), else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["bf16_tflops"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_PEAK_TFLOPS, "fallback"
+        return (FALLBACK_PEAK_TFLOPS if key == "bf16_tflops" else FALLBACK_HBM_GBS), "fallback"
 
 
 class ClockSampler:
@@ -224,12 +229,16 @@ def rank_batch_seed(base_seed: int, rank: int) -> int:
 
 def get_workload(config: str):
     import synthetic
-    fixed, varlen = synthetic.workloads(), synthetic.varlen_workloads()
-    if config in fixed:
-        return fixed[config]
-    if config in varlen:
-        return varlen[config]
-    raise SystemExit(f"unknown --config {config!r}; choose from {sorted(fixed) + sorted(varlen)}")
+    fixed, varlen, decode = synthetic.workloads(), synthetic.varlen_workloads(), synthetic.decode_workloads()
+    for table in (fixed, varlen, decode):
+        if config in table:
+            return table[config]
+    raise SystemExit(f"unknown --config {config!r}; choose from {sorted(fixed) + sorted(varlen) + sorted(decode)}")
+
+
+def is_decode(config: str) -> bool:
+    import synthetic
+    return config in synthetic.decode_workloads()
 
 
 def is_varlen(w) -> bool:
@@ -255,12 +264,14 @@ def oracle_sample(w, q, k, v, n, rng, threads):
     return time.perf_counter() - t0
 
 
-def config_of(w, world: int, flops: float, dynamic: bool) -> dict:
+def config_of(w, world: int, flops: float, dynamic: bool, splits: int = 1) -> dict:
     common = {"heads_q": w.heads_q, "heads_kv": w.heads_kv, "d_qk": w.d_qk, "d_v": w.d_v, "causal": w.causal,
               "flops_per_step_per_gpu": flops,
               "l2": "inputs larger than L2 (Q+K+V+O %.0f MiB per GPU), no flush" % (w.algorithmic_bytes() / 2 ** 20),
               "parallelism": f"weak x{world} (independent batches, no collective)",
               "task_assignment": "dynamic (task counter)" if dynamic or is_varlen(w) else "static round-robin"}
+    if splits > 1:
+        common["split_kv"] = f"{splits} key ranges per task + merge kernel"
     if is_varlen(w):
         return {"workload": f"{w.name}: {w.notes}", "batch_per_gpu": w.batch, "global_batch": w.batch * world,
                 "total_tokens": w.total_q, "seq_len": max(w.seqlens_q), **common}
@@ -309,6 +320,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     dist_init("nccl" if world > 1 else "gloo")
     fa.load_library()
+    splits = 1
 
     w0 = get_workload(args.config)
     w = dataclasses.replace(w0, seed=rank_batch_seed(w0.seed, rank))
@@ -340,6 +352,20 @@ def run_ours(args):
                                   w.heads_kv, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, sp)
             if rc != 0:
                 raise fa.FaError(rc, "fa_fwd_varlen")
+    elif is_decode(args.config) or args.splitkv > 0:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        splits = args.splitkv if args.splitkv > 0 else fa.fa_splitkv_num_splits(
+            w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, w.causal, sms)
+        ws_bytes = max(fa.fa_splitkv_workspace_size(w.batch, w.heads_q, w.seqlen_q, w.d_v, splits), 16)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        launches_per_step = 2 if splits > 1 else 1  # attention kernel + merge kernel
+
+        def step():
+            rc = fa.fa_fwd_splitkv(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                   w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v,
+                                   int(w.causal), scale, splits, ws.data_ptr(), ws_bytes, sp)
+            if rc != 0:
+                raise fa.FaError(rc, "fa_fwd_splitkv")
     else:
         opts = None
         if args.dynamic:
@@ -410,20 +436,26 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in host_inputs)
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
 
-    peak, peak_src = load_peak()
-    achieved = flops / (ms_step * 1e-3) / 1e12
+    hbm_bound = is_decode(args.config)  # K/V read once: bytes, not flops, bound it
+    if hbm_bound:
+        peak, peak_src = load_peak("hbm_gbs")
+        achieved = w.algorithmic_bytes() / (ms_step * 1e-3) / 1e9
+    else:
+        peak, peak_src = load_peak()
+        achieved = flops / (ms_step * 1e-3) / 1e12
     traffic = stored_traffic(args.config) if not args.dynamic else None
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, world, flops, args.dynamic),
+        "config": config_of(w, world, flops, args.dynamic, splits),
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
         "gpu_launches": args.steps * launches_per_step,
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_src} (bf16 dense, burst)",
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'copy bandwidth' if hbm_bound else 'bf16 dense, burst'})",
                      "algorithmic_bytes": w.algorithmic_bytes()},
         "clocks": clk,
     }

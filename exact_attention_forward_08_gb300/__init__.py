@@ -23,7 +23,8 @@ import os
 from . import _build
 
 __all__ = ["fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_varlen_ex", "fa_varlen_workspace_size",
-           "fa_varlen_plan_host", "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
+           "fa_varlen_plan_host", "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_num_splits",
+           "attention_forward_splitkv", "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
            "fa_plan_task", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
            "FaTask", "FaVarlenTask", "attention_forward", "attention_forward_varlen", "FaError", "load_library",
            "LIB_PATH", "STATUS", "VARLEN_HEADER_BYTES"]
@@ -115,6 +116,14 @@ def load_library(path: str | None = None):
     lib.fa_fwd_varlen.restype = _I
     lib.fa_fwd_varlen_ex.argtypes = vl + [ctypes.POINTER(FaOptions), _P]
     lib.fa_fwd_varlen_ex.restype = _I
+    lib.fa_fwd_splitkv.argtypes = _FWD_ARGS + [_I, _P, ctypes.c_size_t, _P]
+    lib.fa_fwd_splitkv.restype = _I
+    lib.fa_fwd_splitkv_ex.argtypes = _FWD_ARGS + [_I, _P, ctypes.c_size_t, ctypes.POINTER(FaOptions), _P]
+    lib.fa_fwd_splitkv_ex.restype = _I
+    lib.fa_splitkv_workspace_size.argtypes = [_I] * 5
+    lib.fa_splitkv_workspace_size.restype = ctypes.c_size_t
+    lib.fa_splitkv_num_splits.argtypes = [_I] * 10
+    lib.fa_splitkv_num_splits.restype = _I
     lib.fa_fwd_varlen_noalloc.argtypes = vl[:16] + [_P]
     lib.fa_fwd_varlen_noalloc.restype = _I
     lib.fa_noalloc_scratch_bytes.argtypes = []
@@ -215,6 +224,62 @@ def fa_fwd_varlen_ex(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads
     return load_library().fa_fwd_varlen_ex(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv,
                                            d_qk, d_v, int(causal), float(scale), workspace, workspace_bytes,
                                            ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale,
+                   num_splits, workspace, workspace_bytes, stream, opts=None) -> int:
+    """``fa_fwd_splitkv_ex`` (``opts`` None: defaults); pointers as integers."""
+    return load_library().fa_fwd_splitkv_ex(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v,
+                                            int(causal), float(scale), num_splits, workspace, workspace_bytes,
+                                            ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def fa_splitkv_workspace_size(batch, heads_q, seqlen_q, d_v, num_splits) -> int:
+    return load_library().fa_splitkv_workspace_size(batch, heads_q, seqlen_q, d_v, num_splits)
+
+
+def fa_splitkv_num_splits(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, num_sms, pack=0) -> int:
+    return load_library().fa_splitkv_num_splits(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, int(causal),
+                                                pack, num_sms)
+
+
+def attention_forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0,
+                              out=None, lse=None, workspace=None, stream=None, options: FaOptions | None = None):
+    """Split-KV forward (decode / short Q): same tensors as ``attention_forward``.
+
+    ``num_splits`` 0 lets the library choose; the workspace (uint8) is
+    allocated for the count the call will use when not given.  Returns (O, LSE).
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    B, Sq, Hq, dqk = q.shape
+    _, Sk, Hkv, _ = k.shape
+    dv = v.shape[3]
+    if out is None:
+        out = torch.empty((B, Sq, Hq, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    splits = num_splits
+    if splits == 0:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        splits = fa_splitkv_num_splits(B, Hq, Hkv, Sq, Sk, dqk, dv, causal, sms,
+                                       options.pack if options is not None else 0)
+    need = fa_splitkv_workspace_size(B, Hq, Sq, dv, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    s = 0.0 if scale is None else float(scale)
+    rc = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, Sk,
+                        dqk, dv, causal, s, num_splits, workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), sptr, options)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
+    return out, lse
 
 
 def fa_fwd_varlen_noalloc(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv, d_qk, d_v,

@@ -29,11 +29,12 @@ __device__ __align__(256) unsigned char g_fa_noalloc_scratch[kNoAllocScratchByte
 namespace {
 
 constexpr int kMaxDevices = 64;
-// 5 (d_qk, d_v) pairs x {non-causal, causal} x {fixed-length, fixed-length with the FMA-pipe exp2, varlen,
-// fixed-length with dynamic task assignment}
-constexpr int kVariants = 4;
+// 5 (d_qk, d_v) pairs x {non-causal, causal} x the kernel modes (fixed-length, FMA-pipe exp2, varlen,
+// dynamic assignment, split-KV)
+constexpr int kVariants = fa::kNumModes;
 constexpr int kNumKernels = 5 * 2 * kVariants;
-constexpr int kVariantFixed = 0, kVariantEmu = 1, kVariantVarlen = 2, kVariantDyn = 3;
+constexpr int kVariantFixed = fa::kModeFixed, kVariantEmu = fa::kModeEmu, kVariantVarlen = fa::kModeVarlen,
+              kVariantDyn = fa::kModeDyn, kVariantSplit = fa::kModeSplit;
 
 // variable-length batches: workspace = [task count (int) at byte 0, task counter (uint) at byte 16,
 // padding to 256 B][VarlenTask records]
@@ -329,6 +330,74 @@ __global__ void __launch_bounds__(kPlanThreads) varlen_plan_kernel(
   if (tid == 0) *count = static_cast<int>(total);
 }
 
+// ---------------------------------------------------------------------------
+// split-KV: the merge kernel
+// ---------------------------------------------------------------------------
+constexpr int kMaxSplits = 1024;
+
+// One warp per output row (b, pos, head), each lane DV / 32 columns.  The
+// ranges' states combine exactly after rescaling to a common base ("Infra:
+// Flash Attention", "How softmax is computed in pieces"; "Prefill and decode":
+// segments computed apart and merged): with O_s = U_s / l_s and
+// LSE_s = m_s + log l_s per range s,
+//   LSE = log sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+// A range without a visible key has LSE_s = -inf and weight 0; a row with none
+// at all gets O = 0, LSE = -inf.
+template <int DV>
+__global__ void __launch_bounds__(256) splitkv_merge_kernel(const float* __restrict__ opart,
+                                                            const float* __restrict__ lpart,
+                                                            uint16_t* __restrict__ o, float* __restrict__ lse,
+                                                            int B, int Sq, int Hq, int splits) {
+  constexpr int kPer = DV / 32;
+  static_assert(kPer == 2 || kPer == 4, "d_v 64 or 128");
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = static_cast<int64_t>(B) * Sq * Hq;
+  const int64_t lstride = rows;          // per range in lpart ([B, Hq, Sq] per range)
+  const int64_t ostride = rows * DV;     // per range in opart ([B, Sq, Hq, DV] per range)
+  const int64_t step = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += step) {
+    const int64_t bs = row / Hq;  // b * Sq + pos
+    const int head = static_cast<int>(row - bs * Hq);
+    const int64_t b = bs / Sq;
+    const int pos = static_cast<int>(bs - b * Sq);
+    const int64_t li = (b * Hq + head) * Sq + pos;
+    float m = -INFINITY;
+    for (int s = 0; s < splits; ++s) m = fmaxf(m, lpart[s * lstride + li]);
+    float acc[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < splits; ++s) {
+        const float l = lpart[s * lstride + li];
+        if (l == -INFINITY) continue;
+        const float w = expf(l - m);
+        wsum += w;
+        const float* src = opart + s * ostride + row * DV + lane * kPer;
+        if constexpr (kPer == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src);
+          acc[0] += w * x.x, acc[1] += w * x.y, acc[2] += w * x.z, acc[3] += w * x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(src);
+          acc[0] += w * x.x, acc[1] += w * x.y;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint32_t packed[kPer / 2];
+#pragma unroll
+    for (int i = 0; i < kPer / 2; ++i) packed[i] = fa::pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    uint16_t* dst = o + row * DV + lane * kPer;
+    if constexpr (kPer == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    }
+    if (lane == 0 && lse != nullptr) lse[li] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+  }
+}
+
 // Options, heads, head dims and scale (shared by the fixed-length and varlen calls).
 int validate_common(int heads_q, int heads_kv, int d_qk, int d_v, float scale, const fa_options& opt) {
   if (heads_q < 1 || heads_kv < 1) return FA_ERR_INVALID_ARG;
@@ -398,9 +467,14 @@ const char* fa_status_string(int status) {
   }
 }
 
-int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
-              int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
-              const fa_options* opts, fa_stream_t stream_) {
+// The fixed-length forward.  num_splits < 0: the plain call (fa_fwd_ex);
+// num_splits >= 0: split-KV (0 = choose), partial results in split_ws and a
+// merge kernel after the attention kernel; a problem that needs no split runs
+// the plain kernel.
+static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+                     int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+                     int num_splits, void* split_ws, size_t split_ws_bytes, const fa_options* opts,
+                     fa_stream_t stream_) {
   fa_options opt;
   fa_options_default(&opt);
   if (opts) opt = *opts;
@@ -411,6 +485,10 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   int rc = validate(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, scale, opt);
   if (rc != FA_OK) return rc;
   if (opt.workspace != nullptr && opt.exp_emu) return FA_ERR_UNSUPPORTED;  // one or the other
+  const bool split_api = num_splits >= 0;
+  if (split_api && (opt.workspace != nullptr || opt.exp_emu)) return FA_ERR_UNSUPPORTED;
+  if (split_api && num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (split_api && !aligned16(split_ws)) return FA_ERR_INVALID_ARG;
   if (batch == 0 || seqlen_q == 0) return FA_OK;
   if (scale == 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d_qk));
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -436,7 +514,20 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     return FA_OK;
   }
 
-  const int variant = opt.workspace != nullptr ? kVariantDyn : (opt.exp_emu ? kVariantEmu : kVariantFixed);
+  fa::Problem prob = fa::make_problem(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal,
+                                      st->l2_bytes / 2, opt.pack);
+  if (split_api) {
+    fa::set_splits(prob, num_splits > 0 ? num_splits : fa::choose_splits(prob, st->sms));
+    if (prob.splits > 1) {
+      if (split_ws == nullptr || split_ws_bytes < fa_splitkv_workspace_size(batch, heads_q, seqlen_q, d_v,
+                                                                           prob.splits) ||
+          !is_device_ptr(split_ws, dev))
+        return FA_ERR_INVALID_ARG;
+    }
+  }
+  const bool split = split_api && prob.splits > 1;
+  const int variant = split ? kVariantSplit
+                            : (opt.workspace != nullptr ? kVariantDyn : (opt.exp_emu ? kVariantEmu : kVariantFixed));
   const int idx = kernel_index(d_qk, d_v, causal, variant);
   fa::KernelEntry entry;
   if (idx < 0 || !get_entry(d_qk, d_v, causal, variant, &entry)) return FA_ERR_UNSUPPORTED;
@@ -445,8 +536,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
 
   fa::Params p;
   std::memset(&p, 0, sizeof(p));
-  p.prob = fa::make_problem(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, st->l2_bytes / 2,
-                            opt.pack);
+  p.prob = prob;
   if (p.prob.num_tasks >= (int64_t(1) << 31)) return FA_ERR_INVALID_ARG;  // the device decodes tasks in 32 bits
   if (encode_q_like(&p.tm_q, q, batch, seqlen_q, heads_q, d_qk, p.prob.pack) != FA_OK) return FA_ERR_CUDA;
   if (encode_kv(&p.tm_k, k, batch, seqlen_k, heads_kv, d_qk) != FA_OK) return FA_ERR_CUDA;
@@ -470,8 +560,66 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.sched_next = static_cast<unsigned int*>(opt.workspace);
     if (cudaMemsetAsync(opt.workspace, 0, FA_SCHED_WORKSPACE_BYTES, stream) != cudaSuccess) return FA_ERR_CUDA;
   }
+  const int64_t rows = static_cast<int64_t>(batch) * seqlen_q * heads_q;
+  if (split) {
+    p.opart = static_cast<float*>(split_ws);
+    p.lpart = p.opart + static_cast<int64_t>(prob.splits) * rows * d_v;
+  }
   if (entry.launch(p, static_cast<int>(grid), stream) != cudaSuccess) return FA_ERR_CUDA;
+  if (split) {
+    const int warps_per_block = 8;
+    int64_t blocks = (rows + warps_per_block - 1) / warps_per_block;
+    if (blocks > static_cast<int64_t>(st->sms) * 16) blocks = static_cast<int64_t>(st->sms) * 16;
+    if (d_v == 128)
+      splitkv_merge_kernel<128><<<static_cast<int>(blocks), 32 * warps_per_block, 0, stream>>>(
+          p.opart, p.lpart, static_cast<uint16_t*>(o), lse, batch, seqlen_q, heads_q, prob.splits);
+    else
+      splitkv_merge_kernel<64><<<static_cast<int>(blocks), 32 * warps_per_block, 0, stream>>>(
+          p.opart, p.lpart, static_cast<uint16_t*>(o), lse, batch, seqlen_q, heads_q, prob.splits);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  }
   return FA_OK;
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+              int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+              const fa_options* opts, fa_stream_t stream) {
+  return fixed_fwd(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale, -1,
+                   nullptr, 0, opts, stream);
+}
+
+size_t fa_splitkv_workspace_size(int batch, int heads_q, int seqlen_q, int d_v, int num_splits) {
+  if (batch < 0 || heads_q < 0 || seqlen_q < 0 || d_v < 0 || num_splits < 1) return 0;
+  if (num_splits == 1) return 0;
+  return static_cast<size_t>(num_splits) * batch * seqlen_q * heads_q * (d_v + 1) * sizeof(float);
+}
+
+int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v,
+                          int causal, int pack, int num_sms) {
+  if (batch < 1 || seqlen_q < 1 || seqlen_k < 1 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv ||
+      num_sms < 1)
+    return 1;
+  if (pack < 0 || (pack > 0 && (fa::kBM % pack != 0 || (heads_q / heads_kv) % pack != 0))) return 1;
+  fa::Problem p = fa::make_problem(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal ? 1 : 0,
+                                   int64_t(64) << 20, pack);
+  fa::set_splits(p, fa::choose_splits(p, num_sms));
+  return p.splits;
+}
+
+int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+                      int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+                      int num_splits, void* workspace, size_t workspace_bytes, const fa_options* opts,
+                      fa_stream_t stream) {
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  return fixed_fwd(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale,
+                   num_splits, workspace, workspace_bytes, opts, stream);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+                   int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+                   int num_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa_fwd_splitkv_ex(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale,
+                           num_splits, workspace, workspace_bytes, nullptr, stream);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q, int heads_kv,
@@ -728,6 +876,7 @@ static fa::Problem problem_of(const fa_plan* pl) {
   p.causal = pl->causal, p.pack = pl->pack, p.groups = pl->groups, p.pos_per_tile = pl->pos_per_tile;
   p.tiles = pl->tiles, p.mblocks = pl->mblocks, p.kv_blocks = pl->kv_blocks, p.ratio = pl->ratio;
   p.section_units = pl->section_units, p.heavy_levels = pl->heavy_levels, p.num_tasks = pl->num_tasks;
+  p.splits = 1, p.split_blocks = pl->kv_blocks;
   return p;
 }
 
@@ -746,7 +895,7 @@ int fa_plan_block_masked(const fa_plan* plan, int pos0, int j) {
 
 int fa_plan_first_masked_block(const fa_plan* plan, int pos0) {
   if (plan == nullptr) return 0;
-  return fa::first_masked_block(plan->seqlen_q, plan->seqlen_k, plan->causal, pos0);
+  return fa::first_masked_block(plan->seqlen_k, plan->seqlen_k - plan->seqlen_q, plan->causal, pos0);
 }
 
 }  // extern "C"

@@ -1,7 +1,7 @@
-// Kernel table: one entry per (d_qk, d_v, causal, variant) instantiation; the
-// variants are fixed-length, fixed-length with the FMA-pipe exp2, varlen (its
-// tasks always assigned dynamically), and fixed-length with dynamic task
-// assignment.  Each head
+// Kernel table: one entry per (d_qk, d_v, causal, mode) instantiation; the
+// modes are fixed-length, fixed-length with the FMA-pipe exp2, varlen (its
+// tasks always assigned dynamically), fixed-length with dynamic task
+// assignment, and split-KV.  Each head
 // dimension lives in its own translation unit so the build compiles them in
 // parallel.
 #pragma once
@@ -19,26 +19,28 @@ struct KernelEntry {
   LaunchFn launch;
 };
 
-template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
+template <int DQ, int DV, bool CAUSAL, int MODE>
 cudaError_t launch_kernel(const Params& p, int grid, cudaStream_t stream) {
-  fa_fwd_kernel<DQ, DV, CAUSAL, EMU, VARLEN, DYN><<<grid, kThreads, Layout<DQ, DV>::kDynSmem, stream>>>(p);
+  fa_fwd_kernel<DQ, DV, CAUSAL, MODE><<<grid, kThreads, Layout<DQ, DV>::kDynSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
+template <int DQ, int DV, bool CAUSAL, int MODE>
 KernelEntry make_entry() {
-  return KernelEntry{reinterpret_cast<const void*>(&fa_fwd_kernel<DQ, DV, CAUSAL, EMU, VARLEN, DYN>),
-                     Layout<DQ, DV>::kDynSmem, &launch_kernel<DQ, DV, CAUSAL, EMU, VARLEN, DYN>};
+  return KernelEntry{reinterpret_cast<const void*>(&fa_fwd_kernel<DQ, DV, CAUSAL, MODE>), Layout<DQ, DV>::kDynSmem,
+                     &launch_kernel<DQ, DV, CAUSAL, MODE>};
 }
 
-// variant: 0 fixed-length, 1 fixed-length with the FMA-pipe exp2, 2 varlen,
-// 3 fixed-length with dynamic task assignment
+// variant = kernel mode (kModeFixed .. kModeSplit)
 template <int DQ, int DV, bool CAUSAL>
 KernelEntry pick_variant(int variant) {
-  if (variant == 3) return make_entry<DQ, DV, CAUSAL, false, false, true>();
-  if (variant == 2) return make_entry<DQ, DV, CAUSAL, false, true, true>();
-  if (variant == 1) return make_entry<DQ, DV, CAUSAL, true, false, false>();
-  return make_entry<DQ, DV, CAUSAL, false, false, false>();
+  switch (variant) {
+    case kModeEmu: return make_entry<DQ, DV, CAUSAL, kModeEmu>();
+    case kModeVarlen: return make_entry<DQ, DV, CAUSAL, kModeVarlen>();
+    case kModeDyn: return make_entry<DQ, DV, CAUSAL, kModeDyn>();
+    case kModeSplit: return make_entry<DQ, DV, CAUSAL, kModeSplit>();
+    default: return make_entry<DQ, DV, CAUSAL, kModeFixed>();
+  }
 }
 
 template <int DQ, int DV>

@@ -18,6 +18,11 @@
 // come from a list written by the planning kernel; each task carries its
 // sequence's lengths and row offsets.
 //
+// Modes (one instantiation each): fixed-length; fixed-length with the FMA-pipe
+// exp2; varlen (tasks from the planned list, always dynamic); fixed-length
+// with dynamic task assignment; split-KV (each task one key range, partial
+// O / LSE in fp32 to a workspace, combined afterwards by the merge kernel).
+//
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DV),
 // O1 [384,384+DV).  P_s overwrites the first 64 columns of S_s as packed bf16
 // pairs.  SMEM: two Q stages, a ring of K/V tiles, a 16 KB O staging tile,
@@ -61,6 +66,9 @@ constexpr int kChunkBytes = 128 * 64 * 2;  // 128 rows x 64 bf16: one 128B-swizz
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.693147180559945309417f;
 constexpr int kTaskRing = 4;     // task indices the TMA thread may post ahead (DYN)
+
+// kernel modes
+enum : int { kModeFixed = 0, kModeEmu = 1, kModeVarlen = 2, kModeDyn = 3, kModeSplit = 4, kNumModes = 5 };
 constexpr int kTaskReaders = 13; // arrivals that free a ring slot: MMA warp + 12 softmax/correction warps
 
 // debug_flags bits
@@ -78,6 +86,8 @@ struct Params {
   const VarlenTask* vtasks;          // varlen: the planned task list
   const int* vtask_count;            // varlen: its length
   unsigned int* sched_next;          // DYN: next task index (cleared before the launch)
+  float* opart;                      // split-KV: O / row_sum per range, [splits, B, Sq, Hq, dv]
+  float* lpart;                      // split-KV: LSE per range, [splits, B, Hq, Sq]
   unsigned int* status;
   Problem prob;  // varlen: the shared fields (heads, pack, causal); lengths come per task
   float scale_log2;  // scale * log2(e)
@@ -166,9 +176,11 @@ __device__ __forceinline__ int task_count(const Params& p) {
   else return static_cast<int>(p.prob.num_tasks);
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool SPLIT = false>
 __device__ __forceinline__ Task get_task(const Params& p, int t) {
-  if constexpr (VARLEN) {
+  if constexpr (SPLIT) {
+    return decode_split_task(p.prob, t);
+  } else if constexpr (VARLEN) {
     const int4* r = reinterpret_cast<const int4*>(p.vtasks + t);
     const int4 a = r[0], b = r[1];
     VarlenTask rec;
@@ -277,7 +289,7 @@ __device__ __forceinline__ void ex2_fma_x2(uint64_t x2, float& y0, float& y1) {
 // ---------------------------------------------------------------------------
 // EMU: one in four exponentials of unmasked blocks on the FMA pipe (an option;
 // its own instantiation, so the default kernel carries no extra code)
-template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
+template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN, bool SPLIT>
 __device__ __forceinline__ void softmax_role(const Params& p, const int stage, const uint32_t tmem,
                                              const uint32_t sbase, float* mbox, const volatile int* ring,
                                              const WaitCtx& wc) {
@@ -301,19 +313,21 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, sbase + L::oBar, ring, wc, kSiteSoftmaxTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT>(p, task);
     const int n = stage ? tk.n[1] : tk.n[0];
     if (n == 0) continue;
     const int pos0 = stage ? tk.pos0[1] : tk.pos0[0];
-    // last key visible to this row (inclusive; keys >= sk are never visible;
-    // (pos - sq) + sk stays inside 32 bits for the sizes the host accepts),
-    // and the first block that needs the element mask
-    int last_key = tk.sk - 1;
+    // last key visible to this row (inclusive, counted from the task's first
+    // key; keys >= kend are never visible; pos + kshift stays inside 32 bits
+    // for the sizes the host accepts; below -1 it means the same as -1), and
+    // the first block that needs the element mask
+    int last_key = tk.kend - 1;
     if (CAUSAL) {
-      const int c = (pos0 + t / pr.pack - tk.sq) + tk.sk;
+      const int c = pos0 + t / pr.pack + tk.kshift;
       if (c < last_key) last_key = c;
     }
-    const int j_mask = first_masked_block(tk.sq, tk.sk, CAUSAL, pos0);
+    if (last_key < -1) last_key = -1;
+    const int j_mask = first_masked_block(tk.kend, tk.kshift, CAUSAL, pos0);
     float row_max = -INFINITY;  // kept reference, raw score units
     float row_sum = 0.f;
     float ref = 0.f;            // row_max * scale_log2 (0 while the row is empty)
@@ -429,7 +443,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 // ---------------------------------------------------------------------------
 // correction + epilogue (WG2)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT>
 __device__ __forceinline__ void correction_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                                 uint8_t* smem, float* mbox, const volatile int* ring,
                                                 const WaitCtx& wc) {
@@ -449,7 +463,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteCorrTask);
     if (task < 0) break;  // no task left, or an abort
-    Task tk = get_task<VARLEN>(p, task);
+    Task tk = get_task<VARLEN, SPLIT>(p, task);
     float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
 
     for (int j = 0; j < tk.nmax; ++j) {
@@ -516,6 +530,33 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         lse = (fin_ref[s] + __log2f(fin_sum[s])) * kLn2;
       }
       const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(s * 128);
+      if constexpr (SPLIT) {
+        // partial result of this key range: O / row_sum in fp32 and its LSE
+        // (-inf, O = 0 when no key of the range is visible to the row).  The
+        // TMEM loads are warp-collective: every lane runs them (has is
+        // uniform); only the stores depend on the row.
+        const bool store = pos < tk.sq;
+        const int64_t row = ((static_cast<int64_t>(tk.split) * pr.B + tk.b) * pr.Sq + pos) * pr.Hq + head;
+        float4* dst = reinterpret_cast<float4*>(p.opart + row * DV);
+#pragma unroll 1
+        for (int c = 0; c < DV; c += 32) {
+          uint32_t r[32];
+          if (has) {
+            tmem_ld32_wait(tO + static_cast<uint32_t>(c), r);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (store) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[c / 4 + q] = make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
+                                           __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+          }
+        }
+        if (store) p.lpart[((static_cast<int64_t>(tk.split) * pr.B + tk.b) * pr.Hq + head) * pr.Sq + pos] = lse;
+        continue;
+      }
       uint4* out_row = nullptr;
       if (direct && pos < tk.sq)
         out_row = reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(tk.q_row0) + pos) * p.o_row_stride +
@@ -613,11 +654,10 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // o_done[s] is committed once per task, after the stage's last P V: inside a
 // task, "S_j ready" already implies that P V_{j-1} has completed (a commit
 // tracks every earlier MMA of the issuing thread).
-template <int DQ, int DV, bool VARLEN, bool DYN>
+template <int DQ, int DV, bool VARLEN, bool DYN, bool SPLIT>
 __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                          const volatile int* ring, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
-  const Problem& pr = p.prob;
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   auto slot_addr = [&](uint32_t it) { return sbase + L::oRing + (it % L::NS) * L::kSlotBytes; };
@@ -639,7 +679,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteMmaTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT>(p, task);
     const uint32_t base = kv_it;
     kv_it += 2u * static_cast<uint32_t>(tk.nmax);
     if (tk.nmax == 0) continue;
@@ -698,11 +738,10 @@ out:
 // ---------------------------------------------------------------------------
 // TMA loads (warp 13, one thread)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool VARLEN, bool DYN>
+template <int DQ, int DV, bool VARLEN, bool DYN, bool SPLIT>
 __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase, volatile int* ring,
                                           const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
-  const Problem& pr = p.prob;
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t q_uses[2] = {0u, 0u};
@@ -716,7 +755,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
   for (int kt = 0;; ++kt) {
     const int task = post_task<DQ, DV, DYN>(p, kt, num_tasks, bar0, ring, wc);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT>(p, task);
     if (tk.nmax == 0) continue;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -761,9 +800,13 @@ out:
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN>
+template <int DQ, int DV, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = Layout<DQ, DV>;
+  constexpr bool EMU = MODE == kModeEmu;
+  constexpr bool VARLEN = MODE == kModeVarlen;
+  constexpr bool DYN = MODE == kModeVarlen || MODE == kModeDyn;
+  constexpr bool SPLIT = MODE == kModeSplit;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -814,17 +857,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   // register budget: 128 x (176 + 176 + 104 + 56) = 65536
   if (warp < 8) {
     setmaxnreg_inc<176>();
-    softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
+    softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN, SPLIT>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
-    correction_role<DQ, DV, CAUSAL, VARLEN, DYN>(p, tmem, sbase, smem, mbox, ring, wc);
+    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT>(p, tmem, sbase, smem, mbox, ring, wc);
   } else {
     setmaxnreg_dec<56>();
     if (warp == 12) {
-      mma_role<DQ, DV, VARLEN, DYN>(p, tmem, sbase, ring, wc);
+      mma_role<DQ, DV, VARLEN, DYN, SPLIT>(p, tmem, sbase, ring, wc);
       __syncwarp();
     } else if (warp == 13) {
-      if (lane == 0) load_role<DQ, DV, VARLEN, DYN>(p, sbase, ring, wc);
+      if (lane == 0) load_role<DQ, DV, VARLEN, DYN, SPLIT>(p, sbase, ring, wc);
       __syncwarp();
     }
   }

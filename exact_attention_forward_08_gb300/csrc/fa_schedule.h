@@ -27,6 +27,12 @@
 //    round-robin over "heaviest first per section" alone left the busiest CTA
 //    with 11-29 % more work than the average; this order halves that, and a
 //    dynamic assignment over it comes within about 1 %).
+//  * Split-KV (decode and other short-Q problems, where (b, g, m_block) tasks
+//    are too few to fill the GPU): each task also takes one of `splits`
+//    consecutive key ranges of split_blocks blocks ("Infra: Flash Attention",
+//    "Prefill and decode": the state merge does not fix the scan order, so
+//    the keys can be cut into segments computed apart and merged after); the
+//    partial results are combined by a separate merge kernel.
 //  * Variable-length batches (sequences packed back to back, offsets in
 //    cu_seqlens): a planning kernel sorts the sequences by the cost of their
 //    heaviest tile, longest first ("FlashAttention-4 wiki", "Core methods",
@@ -59,7 +65,9 @@ struct Problem {
   int ratio;          // Hq / Hkv
   int section_units;  // causal task order: (b, g) units per L2 section
   int heavy_levels;   // causal task order: m_blocks M-1 .. M-heavy_levels go by sections
-  int64_t num_tasks;  // B * groups * mblocks
+  int splits;         // split-KV: key ranges per (b, g, m_block) (1 = no split)
+  int split_blocks;   // split-KV: K/V blocks per range
+  int64_t num_tasks;  // B * groups * mblocks * splits
 };
 
 struct Task {
@@ -68,10 +76,16 @@ struct Task {
   int pos0[2];   // first sequence position of each stage's tile
   int n[2];      // K/V blocks each stage visits (0: nothing to do)
   int nmax;      // max(n[0], n[1])
-  int sq, sk;    // query and key count of this task's sequence
+  int sq;        // query count of this task's sequence
+  // keys of the task, counted from its first key: those >= kend are never
+  // visible; under the causal mask position pos sees key r iff r <= pos + kshift
+  // (a whole sequence: kend = sk, kshift = sk - sq; split-KV range starting at
+  // key k0: kend = its length, kshift = sk - sq - k0)
+  int kend, kshift;
   int q_row0;    // row of position 0 in the Q/O view (varlen: cu_seqlens_q[b]; else 0)
-  int k_row0;    // row of key 0 in the K/V view (varlen: cu_seqlens_k[b]; else 0)
+  int k_row0;    // row of the task's first key in the K/V view
   int bc;        // batch coordinate in the TMA views (varlen: 0; else b)
+  int split;     // split-KV range index (0 otherwise)
 };
 
 // One task of a variable-length batch as the planning kernel writes it
@@ -111,24 +125,37 @@ FA_HD Problem make_problem(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int
   if (su > units) su = units > 0 ? units : 1;
   p.section_units = static_cast<int>(su);
   p.heavy_levels = (p.mblocks + 1) / 2;
+  p.splits = 1;
+  p.split_blocks = p.kv_blocks;
   return p;
 }
 
-// K/V blocks a Q tile starting at pos0 visits, in a sequence of sq queries
-// and sk keys (kvb = ceil(sk / kBN) blocks), ppt positions per tile.
-FA_HD int tile_blocks_len(int sq, int sk, int kvb, int causal, int ppt, int pos0) {
-  if (pos0 >= sq || kvb == 0) return 0;
+// Split the keys of every (b, g, m_block) into about `splits` ranges of whole
+// blocks (no empty range: the count is recomputed from the range length).
+FA_HD void set_splits(Problem& p, int splits) {
+  if (splits < 1 || p.kv_blocks == 0) splits = 1;
+  if (splits > p.kv_blocks && p.kv_blocks > 0) splits = p.kv_blocks;
+  p.split_blocks = p.kv_blocks > 0 ? ceil_div(p.kv_blocks, splits) : 0;
+  p.splits = p.split_blocks > 0 ? ceil_div(p.kv_blocks, p.split_blocks) : 1;
+  p.num_tasks = static_cast<int64_t>(p.B) * p.groups * p.mblocks * p.splits;
+}
+
+// K/V blocks a Q tile starting at pos0 visits (sq queries, ppt positions per
+// tile; kend / kshift as in Task).
+FA_HD int tile_blocks_len(int sq, int kend, int kshift, int causal, int ppt, int pos0) {
+  if (pos0 >= sq || kend <= 0) return 0;
+  const int kvb = ceil_div(kend, kBN);
   if (!causal) return kvb;
   int last = pos0 + ppt;
   if (last > sq) last = sq;
-  const int64_t max_key = static_cast<int64_t>(last - 1) + sk - sq;
+  const int64_t max_key = static_cast<int64_t>(last - 1) + kshift;
   if (max_key < 0) return 0;
   const int64_t n = max_key / kBN + 1;
   return n < kvb ? static_cast<int>(n) : kvb;
 }
 
 FA_HD int tile_blocks(const Problem& p, int pos0) {
-  return tile_blocks_len(p.Sq, p.Sk, p.kv_blocks, p.causal, p.pos_per_tile, pos0);
+  return tile_blocks_len(p.Sq, p.Sk, p.Sk - p.Sq, p.causal, p.pos_per_tile, pos0);
 }
 
 // Task t (0 <= t < num_tasks < 2^31; the host refuses larger problems).
@@ -163,7 +190,7 @@ FA_HD Task decode_task(const Problem& p, int t) {
   k.g = unit - k.b * p.groups;
   k.mb = mb;
   k.kvh = (k.g * p.pack) / p.ratio;
-  k.sq = p.Sq, k.sk = p.Sk, k.q_row0 = 0, k.k_row0 = 0, k.bc = k.b;
+  k.sq = p.Sq, k.kend = p.Sk, k.kshift = p.Sk - p.Sq, k.q_row0 = 0, k.k_row0 = 0, k.bc = k.b, k.split = 0;
   k.nmax = 0;
   for (int s = 0; s < 2; ++s) {
     k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
@@ -175,27 +202,75 @@ FA_HD Task decode_task(const Problem& p, int t) {
 
 // Does K/V block j need the element mask for a tile starting at pos0?  (the
 // sequence tail, or the causal diagonal)
-FA_HD bool block_needs_mask_len(int sq, int sk, int causal, int pos0, int j) {
+FA_HD bool block_needs_mask_len(int kend, int kshift, int causal, int pos0, int j) {
   const int64_t key_hi = static_cast<int64_t>(j) * kBN + kBN - 1;
-  if (key_hi >= sk) return true;
-  return causal && key_hi > static_cast<int64_t>(pos0) + sk - sq;
+  if (key_hi >= kend) return true;
+  return causal && key_hi > static_cast<int64_t>(pos0) + kshift;
 }
 
 FA_HD bool block_needs_mask(const Problem& p, int pos0, int j) {
-  return block_needs_mask_len(p.Sq, p.Sk, p.causal, pos0, j);
+  return block_needs_mask_len(p.Sk, p.Sk - p.Sq, p.causal, pos0, j);
 }
 
 // The first K/V block that needs the mask (every later one needs it too):
-// the tail starts at block sk / kBN; under the causal mask block j hides a
-// key of the tile once j * kBN + kBN - 1 > pos0 + sk - sq.
-FA_HD int first_masked_block(int sq, int sk, int causal, int pos0) {
-  int j = sk / kBN;
+// the tail starts at block kend / kBN; under the causal mask block j hides a
+// key of the tile once j * kBN + kBN - 1 > pos0 + kshift.
+FA_HD int first_masked_block(int kend, int kshift, int causal, int pos0) {
+  int j = kend / kBN;
   if (causal) {
-    const int64_t c1 = static_cast<int64_t>(pos0) + sk - sq + 1;
+    const int64_t c1 = static_cast<int64_t>(pos0) + kshift + 1;
     const int jc = c1 > 0 ? static_cast<int>(c1 / kBN) : 0;
     if (jc < j) j = jc;
   }
   return j;
+}
+
+// Task t of a split-KV problem: t = ((b * groups + g) * splits + split) * M + m.
+FA_HD Task decode_split_task(const Problem& p, int t) {
+  Task k;
+  const int M = p.mblocks;
+  const int unit_split = t / M;
+  k.mb = t - unit_split * M;
+  const int unit = unit_split / p.splits;
+  k.split = unit_split - unit * p.splits;
+  k.b = unit / p.groups;
+  k.g = unit - k.b * p.groups;
+  k.kvh = (k.g * p.pack) / p.ratio;
+  const int k0 = k.split * p.split_blocks * kBN;
+  int k1 = k0 + p.split_blocks * kBN;
+  if (k1 > p.Sk) k1 = p.Sk;
+  k.sq = p.Sq, k.kend = k1 - k0, k.kshift = p.Sk - p.Sq - k0;
+  k.q_row0 = 0, k.k_row0 = k0, k.bc = k.b;
+  k.nmax = 0;
+  for (int s = 0; s < 2; ++s) {
+    k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
+    k.n[s] = tile_blocks_len(k.sq, k.kend, k.kshift, p.causal, p.pos_per_tile, k.pos0[s]);
+    if (k.n[s] > k.nmax) k.nmax = k.n[s];
+  }
+  return k;
+}
+
+// Split count for a problem whose (b, g, m_block) tasks may not fill `sms`
+// persistent CTAs: 1 when they do (or the keys are few); otherwise the
+// smallest count whose tasks fill the CTAs' last wave to at least 85 % of the
+// best count's fill, with at least 4 blocks (512 keys) per range.
+FA_HD int choose_splits(const Problem& p, int sms) {
+  const int64_t units = static_cast<int64_t>(p.B) * p.groups * p.mblocks;
+  if (sms < 1 || units >= sms || p.kv_blocks < 8) return 1;
+  int max_splits = p.kv_blocks / 4;
+  if (max_splits > 128) max_splits = 128;
+  double best = 0.0;
+  double eff[129];
+  for (int s = 1; s <= max_splits; ++s) {
+    const int bps = ceil_div(p.kv_blocks, s);
+    const int64_t tasks = units * ceil_div(p.kv_blocks, bps);
+    const int64_t waves = (tasks + sms - 1) / sms;
+    eff[s] = static_cast<double>(tasks) / static_cast<double>(waves * sms);
+    if (eff[s] > best) best = eff[s];
+  }
+  for (int s = 1; s <= max_splits; ++s)
+    if (eff[s] >= 0.85 * best) return s;
+  return 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -242,12 +317,12 @@ FA_HD Task task_from_record(const Problem& p, const VarlenTask& r) {
   Task k;
   k.b = r.b, k.g = r.g, k.mb = r.mb;
   k.kvh = (k.g * p.pack) / p.ratio;
-  k.sq = r.sq, k.sk = r.sk, k.q_row0 = r.q_row0, k.k_row0 = r.k_row0, k.bc = 0;
-  const int kvb = ceil_div(r.sk, kBN);
+  k.sq = r.sq, k.kend = r.sk, k.kshift = r.sk - r.sq, k.q_row0 = r.q_row0, k.k_row0 = r.k_row0, k.bc = 0;
+  k.split = 0;
   k.nmax = 0;
   for (int s = 0; s < 2; ++s) {
     k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
-    k.n[s] = tile_blocks_len(r.sq, r.sk, kvb, p.causal, p.pos_per_tile, k.pos0[s]);
+    k.n[s] = tile_blocks_len(r.sq, r.sk, r.sk - r.sq, p.causal, p.pos_per_tile, k.pos0[s]);
     if (k.n[s] > k.nmax) k.nmax = k.n[s];
   }
   return k;

@@ -120,6 +120,54 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
               const fa_options* opts, fa_stream_t stream);
 
 /*
+ * Split-KV forward for decode and other short-query problems.  When the
+ * (batch, head group, 256-query block) tasks are too few to fill the GPU, the
+ * kernel is starved of parallel work and bound by latency ("FlashAttention-4
+ * wiki", "Stress-testing assumptions": the decode failure mode).  Here the
+ * keys of every task are cut into `splits` ranges computed by separate CTAs;
+ * each writes O / row_sum and its LSE in fp32 to the workspace, and a merge
+ * kernel combines them exactly ("Infra: Flash Attention", "Prefill and
+ * decode": the merge of softmax states does not fix the scan order, so the
+ * keys can be split and merged afterwards; floating-point results differ from
+ * fa_fwd only by rounding).
+ *
+ * Arguments, layouts, masks and results as for fa_fwd_ex, plus:
+ *   num_splits  >= 1: key ranges per task (reduced so that none is empty; 1
+ *               runs fa_fwd's kernel and ignores the workspace); 0: the
+ *               library's choice, fa_splitkv_num_splits() with this device's
+ *               SM count.  At most 1024.
+ *   workspace   device memory, 16-byte aligned, at least
+ *               fa_splitkv_workspace_size(batch, heads_q, seqlen_q, d_v, splits)
+ *               bytes for the split count used (partial O [splits, B, Sq, Hq, d_v]
+ *               then partial LSE [splits, B, Hq, Sq], fp32); may be NULL when
+ *               that count is 1.  Calls that may overlap need different
+ *               workspaces.
+ * fa_options.workspace and exp_emu must be unset (FA_ERR_UNSUPPORTED).
+ * Two launches per call when splitting: the attention kernel and the merge.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+                   int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+                   int num_splits, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+int fa_fwd_splitkv_ex(const void* q, const void* k, const void* v, void* o, float* lse, int batch, int heads_q,
+                      int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v, int causal, float scale,
+                      int num_splits, void* workspace, size_t workspace_bytes, const fa_options* opts,
+                      fa_stream_t stream);
+
+/* Bytes of the split-KV workspace for `num_splits` ranges (0 when num_splits is 1). */
+size_t fa_splitkv_workspace_size(int batch, int heads_q, int seqlen_q, int d_v, int num_splits);
+
+/*
+ * The split count fa_fwd_splitkv uses for num_splits = 0 on a GPU with
+ * num_sms SMs (host only): 1 when the unsplit tasks fill the SMs or the keys
+ * are fewer than 8 blocks; otherwise the smallest count (at most 128, at least
+ * 4 blocks per range) whose tasks fill the last wave of persistent CTAs to at
+ * least 85 % of the best count's fill.  pack as in fa_options.
+ */
+int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v,
+                          int causal, int pack, int num_sms);
+
+/*
  * Test hook for the emulated exponential: for i < n, y_fma[i] = 2^x[i] by the
  * FMA-pipe polynomial used with exp_emu = 1, y_mufu[i] = the hardware ex2
  * (ex2.approx.ftz).  Device pointers, fp32; stream-ordered.

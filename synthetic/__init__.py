@@ -279,3 +279,16 @@ def varlen_workloads() -> dict:
                                        notes=f"{len(lens)} sequences, 32768 tokens, lengths 128..8192 "
                                              "log-uniform, H16 d128 non-causal")
     return w
+
+
+def decode_workloads() -> dict:
+    """Decode-shaped problems (few queries against a long K/V cache), the
+    split-KV path's workloads.  K/V is read once, so they are HBM-bound."""
+    w = {}
+    w["decode32k"] = Workload("decode32k", 8, 32, 8, 1, 32768, 128, 128, False, seed=51,
+                              notes="B8 Hq32 Hkv8 Sq1 Sk32768 d128 (one query per sequence, 32k-key cache)")
+    w["decode_mqa"] = Workload("decode_mqa", 32, 32, 1, 1, 16384, 128, 128, False, seed=52,
+                               notes="B32 Hq32 Hkv1 Sq1 Sk16384 d128 (MQA decode)")
+    w["specdec"] = Workload("specdec", 8, 32, 8, 4, 16384, 128, 128, True, seed=53,
+                            notes="B8 Hq32 Hkv8 Sq4 Sk16384 d128 causal (4 draft tokens)")
+    return w
