@@ -291,4 +291,7 @@ def decode_workloads() -> dict:
                                notes="B32 Hq32 Hkv1 Sq1 Sk16384 d128 (MQA decode)")
     w["specdec"] = Workload("specdec", 8, 32, 8, 4, 16384, 128, 128, True, seed=53,
                             notes="B8 Hq32 Hkv8 Sq4 Sk16384 d128 causal (4 draft tokens)")
+    # smaller case of the split-KV kernel for detailed profiling (K/V still > L2)
+    w["prof_decode"] = Workload("prof_decode", 4, 32, 8, 1, 16384, 128, 128, False, seed=54,
+                                notes="B4 Hq32 Hkv8 Sq1 Sk16384 d128 (decode profiling case)")
     return w
