@@ -8,7 +8,8 @@ which draws seeded inputs and holds none of the method's arithmetic.
 
 ``attn_fwd`` is the plain definition O = softmax(scale * Q K^T) V with the
 per-row log-sum-exp, written out row by row in double precision in
-``attn_oracle.c`` (see that file for the citations).  ``online`` restates the
+``attn_oracle.c`` (see that file for the citations); ``attn_bwd`` is the
+chain rule through it (dQ, dK, dV for a given dO), in the same file.  ``online`` restates the
 pages' online-softmax algebra (block state, two-block merge, conditional
 rescaling) in fp64 for the pins in ``tests/``.
 
@@ -50,6 +51,10 @@ def load_library(path: str):
                                     i64, i64, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_double,
                                     ctypes.c_void_p, i64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     lib.oracle_attn_fwd.restype = ctypes.c_int
+    lib.oracle_attn_bwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [i64] * 7 + [ctypes.c_int, ctypes.c_double,
+                                                                                   ctypes.c_void_p, ctypes.c_void_p,
+                                                                                   ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_attn_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -113,6 +118,37 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, rows=Non
     if full:
         return o.reshape(B, Sq, Hq, dv), lse.reshape(B, Sq, Hq).transpose(0, 2, 1).copy()
     return o, lse
+
+
+def attn_bwd(q, k, v, dout, causal: bool = False, scale: float | None = None, threads: int | None = None, lib=None):
+    """Reference attention backward: (dQ, dK, dV) as float64 for a loss with
+    dLoss/dO = dout.  q [B,Sq,Hq,dqk], k [B,Sk,Hkv,dqk], v [B,Sk,Hkv,dv],
+    dout [B,Sq,Hq,dv]; all float64, or all uint16 bf16 bit patterns."""
+    arrs = [np.ascontiguousarray(x) for x in (q, k, v, dout)]
+    kinds = {a.dtype for a in arrs}
+    if kinds == {np.dtype(np.uint16)}:
+        elem = 1
+    elif kinds == {np.dtype(np.float64)}:
+        elem = 0
+    else:
+        raise TypeError(f"q, k, v, dout must all be uint16 (bf16 bits) or all float64, got {kinds}")
+    q, k, v, dout = arrs
+    B, Sq, Hq, dqk = q.shape
+    _, Sk, Hkv, _ = k.shape
+    dv = v.shape[3]
+    if dout.shape != (B, Sq, Hq, dv) or k.shape != (B, Sk, Hkv, dqk) or v.shape[:3] != (B, Sk, Hkv):
+        raise ValueError("inconsistent shapes")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dqk)
+    dq = np.empty((B, Sq, Hq, dqk))
+    dk = np.empty((B, Sk, Hkv, dqk))
+    dvv = np.empty((B, Sk, Hkv, dv))
+    rc = (lib or _load()).oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, elem, B, Hq,
+                                          Hkv, Sq, Sk, dqk, dv, int(bool(causal)), float(scale), dq.ctypes.data,
+                                          dk.ctypes.data, dvv.ctypes.data, threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd failed with status {rc}")
+    return dq, dk, dvv
 
 
 def row_ids(b, i, h, Sq: int, Hq: int) -> np.ndarray:

@@ -368,8 +368,8 @@ def test_matches_torch_sdpa_float64():
 
 MUTANTS = {
     "scale dropped": ("s[j] = J->scale * acc;", "s[j] = acc;"),
-    "causal off by one": ("nvis = last + 1 < J->Sk ? last + 1 : J->Sk;", "nvis = last < J->Sk ? last : J->Sk;"),
-    "top-left causal": ("int64_t last = i + J->Sk - J->Sq;", "int64_t last = i;"),
+    "causal off by one": ("nvis = last + 1 < Sk ? last + 1 : Sk;", "nvis = last < Sk ? last : Sk;"),
+    "top-left causal": ("int64_t last = i + Sk - Sq;", "int64_t last = i;"),
     "kv head modulo": ("const int64_t kvh = h / (J->Hq / J->Hkv);", "const int64_t kvh = h % J->Hkv;"),
     "lse without max": ("*lse_out = m + log(l);", "*lse_out = log(l);"),
     "no normalisation": ("o_row[c] /= l;", "o_row[c] /= 1.0;"),
