@@ -24,7 +24,8 @@ from . import _build
 
 __all__ = ["fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_varlen_ex", "fa_varlen_workspace_size",
            "fa_varlen_plan_host", "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_num_splits",
-           "attention_forward_splitkv", "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
+           "attention_forward_splitkv", "fa_bwd", "fa_bwd_workspace_size", "attention_backward",
+           "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
            "fa_plan_task", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
            "FaTask", "FaVarlenTask", "attention_forward", "attention_forward_varlen", "FaError", "load_library",
            "LIB_PATH", "STATUS", "VARLEN_HEADER_BYTES"]
@@ -124,6 +125,13 @@ def load_library(path: str | None = None):
     lib.fa_splitkv_workspace_size.restype = ctypes.c_size_t
     lib.fa_splitkv_num_splits.argtypes = [_I] * 10
     lib.fa_splitkv_num_splits.restype = _I
+    bw = [_P] * 9 + [_I] * 8 + [ctypes.c_float, _P, ctypes.c_size_t]
+    lib.fa_bwd.argtypes = bw + [_P]
+    lib.fa_bwd.restype = _I
+    lib.fa_bwd_ex.argtypes = bw + [ctypes.POINTER(FaOptions), _P]
+    lib.fa_bwd_ex.restype = _I
+    lib.fa_bwd_workspace_size.argtypes = [_I, _I, _I]
+    lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
     lib.fa_fwd_varlen_noalloc.argtypes = vl[:16] + [_P]
     lib.fa_fwd_varlen_noalloc.restype = _I
     lib.fa_noalloc_scratch_bytes.argtypes = []
@@ -280,6 +288,51 @@ def attention_forward_splitkv(q, k, v, causal: bool = False, scale: float | None
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_splitkv")
     return out, lse
+
+
+def fa_bwd_workspace_size(batch: int, heads_q: int, seqlen_q: int) -> int:
+    return load_library().fa_bwd_workspace_size(batch, heads_q, seqlen_q)
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal, scale,
+           workspace, workspace_bytes, stream, opts=None) -> int:
+    """``fa_bwd_ex`` of include/fa.h (``opts`` None: defaults); pointers as integers."""
+    return load_library().fa_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, batch, heads_q, heads_kv, seqlen_q, seqlen_k,
+                                    d_qk, d_v, int(causal), float(scale), workspace, workspace_bytes,
+                                    ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None,
+                       dv=None, workspace=None, stream=None, options: FaOptions | None = None):
+    """(dQ, dK, dV) for bf16 CUDA tensors laid out as ``attention_forward``'s
+    (q, k, v, its outputs o and lse, and dout = dLoss/dO).  Allocates the
+    gradients and the workspace when not given."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise FaError(FA_ERR_INVALID_ARG, "lse must be a contiguous fp32 CUDA tensor")
+    B, Sq, Hq, dqk = q.shape
+    _, Sk, Hkv, _ = k.shape
+    dvh = v.shape[3]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, Hq, Sq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    s = 0.0 if scale is None else float(scale)
+    rc = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Sq, Sk, dqk, dvh, causal, s,
+                workspace.data_ptr(), workspace.numel() * workspace.element_size(), sptr, options)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_fwd_varlen_noalloc(q, k, v, o, lse, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv, d_qk, d_v,

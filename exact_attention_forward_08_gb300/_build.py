@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libfa_gb300.so")
 
-SOURCES = ["fa_api.cu", "fa_inst_d64.cu", "fa_inst_d128.cu", "fa_inst_d192.cu"]
+SOURCES = ["fa_api.cu", "fa_inst_d64.cu", "fa_inst_d128.cu", "fa_inst_d192.cu", "fa_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

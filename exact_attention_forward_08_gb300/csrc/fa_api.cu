@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "fa.h"
+#include "fa_bwd_dispatch.h"
 #include "fa_dispatch.h"
 #include "fa_schedule.h"
 
@@ -53,6 +54,7 @@ struct DeviceState {
   unsigned int* status = nullptr;
   void* noalloc_scratch = nullptr;  // g_fa_noalloc_scratch on this device
   bool kernel_ready[kNumKernels] = {};
+  bool bwd_ready[2 * 2 * 2] = {};   // (d 64 / 128) x (dK/dV, dQ) x (non-causal, causal)
   bool plan_ready = false;
 };
 
@@ -816,6 +818,139 @@ int fa_varlen_plan_host(const int* cu_seqlens_q, const int* cu_seqlens_k, int ba
   }
   *count = n;
   return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int batch, int heads_q, int seqlen_q) {
+  if (batch < 0 || heads_q < 1 || seqlen_q < 0) return 0;
+  const int64_t sq_pad = (static_cast<int64_t>(seqlen_q) + fa::kBM - 1) / fa::kBM * fa::kBM;
+  return static_cast<size_t>(2) * batch * heads_q * sq_pad * sizeof(float);
+}
+
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+              void* dq, void* dk, void* dv, int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k,
+              int d_qk, int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
+              const fa_options* opts, fa_stream_t stream_) {
+  fa_options opt;
+  fa_options_default(&opt);
+  if (opts) opt = *opts;
+  if (opt.timeout_s <= 0.0) opt.timeout_s = 1.0;
+  causal = causal ? 1 : 0;
+  if (batch < 0 || seqlen_q < 0 || seqlen_k < 0 || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv)
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (opt.grid < 0 || !std::isfinite(opt.timeout_s) || opt.timeout_s > 3600.0) return FA_ERR_INVALID_ARG;
+  if (opt.debug_flags != 0 || opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1) return FA_ERR_UNSUPPORTED;
+  if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return FA_ERR_UNSUPPORTED;
+  if (batch == 0) return FA_OK;
+  const int64_t big = int64_t(1) << 31;
+  if (static_cast<int64_t>(seqlen_q) + seqlen_k + 4 * fa::kBM >= big) return FA_ERR_INVALID_ARG;
+  const bool any_q = seqlen_q > 0, any_k = seqlen_k > 0;
+  if ((any_q && (q == nullptr || o == nullptr || lse == nullptr || dout == nullptr || dq == nullptr)) ||
+      (any_k && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return FA_ERR_INVALID_ARG;
+  if (any_q && any_k && (workspace == nullptr || workspace_bytes < fa_bwd_workspace_size(batch, heads_q, seqlen_q)))
+    return FA_ERR_INVALID_ARG;
+  if (scale == 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d_qk));
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* st = nullptr;
+  int rc = init_device(dev, &st);
+  if (rc != FA_OK) return rc;
+  auto dev_ok = [&](const void* ptr) { return ptr == nullptr || is_device_ptr(ptr, dev); };
+  if (!dev_ok(q) || !dev_ok(k) || !dev_ok(v) || !dev_ok(o) || !dev_ok(lse) || !dev_ok(dout) || !dev_ok(dq) ||
+      !dev_ok(dk) || !dev_ok(dv) || !dev_ok(workspace))
+    return FA_ERR_INVALID_ARG;
+
+  // degenerate shapes: no query (dK = dV = 0) or no key (dQ = 0)
+  if (!any_q || !any_k) {
+    if (any_k) {
+      const size_t bytes = static_cast<size_t>(batch) * seqlen_k * heads_kv * d_qk * 2;
+      if (cudaMemsetAsync(dk, 0, bytes, stream) != cudaSuccess || cudaMemsetAsync(dv, 0, bytes, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    }
+    if (any_q) {
+      const size_t bytes = static_cast<size_t>(batch) * seqlen_q * heads_q * d_qk * 2;
+      if (cudaMemsetAsync(dq, 0, bytes, stream) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return FA_OK;
+  }
+
+  fa::BwdEntry ent[2];
+  for (int kind = 0; kind < 2; ++kind) {
+    if (!fa::bwd_entry(d_qk, kind, causal, &ent[kind])) return FA_ERR_UNSUPPORTED;
+    const int idx = ((d_qk == 128 ? 1 : 0) * 2 + kind) * 2 + causal;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!st->bwd_ready[idx]) {
+      if (ent[kind].smem > st->smem_optin) return FA_ERR_UNSUPPORTED;
+      if (cudaFuncSetAttribute(ent[kind].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ent[kind].smem) !=
+          cudaSuccess)
+        return FA_ERR_CUDA;
+      st->bwd_ready[idx] = true;
+    }
+  }
+
+  const int sq_pad = (seqlen_q + fa::kBM - 1) / fa::kBM * fa::kBM;
+  float* l2 = static_cast<float*>(workspace);
+  float* dvec = l2 + static_cast<int64_t>(batch) * heads_q * sq_pad;
+  if (fa::launch_bwd_prep(d_qk, o, dout, lse, l2, dvec, batch, heads_q, seqlen_q, sq_pad, st->sms * 16, stream) !=
+      cudaSuccess)
+    return FA_ERR_CUDA;
+
+  const int ratio = heads_q / heads_kv;
+  const int64_t l2_budget = st->l2_bytes / 2;
+  for (int kind = 0; kind < 2; ++kind) {
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const bool kv = kind == fa::kBwdDkDv;
+    // resident / streamed tiles: K, V with Q, dO streamed (dK/dV); Q, dO with K, V streamed (dQ)
+    const void* r0 = kv ? k : q;
+    const void* r1 = kv ? v : dout;
+    const void* t0 = kv ? q : k;
+    const void* t1 = kv ? dout : v;
+    const int hr = kv ? heads_kv : heads_q, sr = kv ? seqlen_k : seqlen_q;
+    const int ht = kv ? heads_q : heads_kv, stt = kv ? seqlen_q : seqlen_k;
+    if (encode_kv(&p.tm_r0, r0, batch, sr, hr, d_qk) != FA_OK || encode_kv(&p.tm_r1, r1, batch, sr, hr, d_qk) != FA_OK ||
+        encode_kv(&p.tm_t0, t0, batch, stt, ht, d_qk) != FA_OK || encode_kv(&p.tm_t1, t1, batch, stt, ht, d_qk) != FA_OK)
+      return FA_ERR_CUDA;
+    p.l2 = l2;
+    p.dvec = dvec;
+    p.out0 = static_cast<uint16_t*>(kv ? dv : dq);
+    p.out1 = static_cast<uint16_t*>(kv ? dk : nullptr);
+    p.status = st->status;
+    p.B = batch, p.Hq = heads_q, p.Hkv = heads_kv, p.Sq = seqlen_q, p.Sk = seqlen_k, p.sq_pad = sq_pad;
+    p.ratio = ratio, p.causal = causal;
+    p.mq = (seqlen_q + fa::kBM - 1) / fa::kBM;
+    p.nk = (seqlen_k + fa::kBN - 1) / fa::kBN;
+    p.units = batch * hr;
+    p.blocks = kv ? p.nk : p.mq;
+    // causal sections: units whose streamed tiles fit in half the L2 together
+    const int64_t streamed = static_cast<int64_t>(stt) * d_qk * 2 * 2 * (kv ? ratio : 1);
+    int64_t su = streamed > 0 ? l2_budget / streamed : 1;
+    if (su < 1) su = 1;
+    if (su > p.units) su = p.units;
+    p.section_units = static_cast<int>(su);
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.timeout_ns = static_cast<unsigned long long>(opt.timeout_s * 1e9);
+    const int64_t tasks = static_cast<int64_t>(p.units) * p.blocks;
+    if (tasks >= big) return FA_ERR_INVALID_ARG;
+    int64_t grid = opt.grid > 0 ? opt.grid : st->sms;
+    if (grid > tasks) grid = tasks;
+    if (ent[kind].launch(p, static_cast<int>(grid), stream) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+           void* dk, void* dv, int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v,
+           int causal, float scale, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal,
+                   scale, workspace, workspace_bytes, nullptr, stream);
 }
 
 int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]) {

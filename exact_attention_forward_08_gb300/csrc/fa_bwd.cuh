@@ -1,0 +1,562 @@
+// Exact attention backward for sm_103a: dQ, dK, dV for a given dO, from the
+// forward's O and LSE ("Infra: Flash Attention", section "Why backward
+// recomputes" and its detail on the block-wise gradients):
+//
+//   P = exp(scale * Q K^T - LSE)        (recomputed, never stored)
+//   dV = P^T dO          dP = dO V^T
+//   dS = P (dP - D),     D_i = dO_i . O_i
+//   dQ = scale dS K      dK = scale dS^T Q
+//
+// Three launches, no atomics, deterministic:
+//   bwd_prep   D = rowsum(dO * O) and LSE * log2(e) per query row, padded to
+//              whole 128-row blocks (+inf LSE on padded or empty rows, so
+//              their P is 0 without a mask).
+//   bwd kernel KIND = kBwdDkDv: one task per (b, K/V head, 128-key block):
+//              K and V resident, the Q / dO blocks of every query head that
+//              reads this K/V head streamed through a ring; S^T = K Q^T and
+//              dP^T = V dO^T on tcgen05, P^T and dS^T on the CUDA cores back
+//              into TMEM, dV += P^T dO and dK += dS^T Q accumulated in TMEM.
+//   bwd kernel KIND = kBwdDq: one task per (b, query head, 128-query block):
+//              Q and dO resident, K / V blocks streamed; S = Q K^T,
+//              dP = dO V^T, dS, dQ += dS K.
+// Both directions are the same loop with the roles of the tiles swapped, so
+// they share this code.  Computing dQ in its own pass costs two more GEMMs
+// per tile pair (S and dP recomputed) but needs neither the fp32 dQ
+// reductions across key blocks nor TMEM beyond 512 columns (S, dP, dK, dV).
+//
+// CTA: 192 threads, persistent (grid = SM count):
+//   warps 0-3  row role: thread = row = TMEM lane (a key for dK/dV, a query
+//              for dQ); P and dS, then the epilogue (accumulators -> bf16).
+//   warp 4     tcgen05.mma issue (one lane) and TMEM alloc / free.
+//   warp 5     TMA loads (one lane).
+// TMEM: S [0,128), dP [128,256), accumulator 0 [256, 256+D) (dV or dQ),
+// accumulator 1 [384, 384+D) (dK).  P (or dS for dQ) is written as packed
+// bf16 pairs over the first 64 columns of S, dS^T over the first 64 of dP.
+//
+// Hand-offs (all mbarriers, all waits bounded):
+//   res_full / res_empty     resident tiles of a task loaded / no longer read
+//   t_full[r] / t_empty[r]   ring slot r of streamed tiles (+ the LSE and D
+//                            vectors of the block for dK/dV)
+//   s_full                   S and dP of the current block in TMEM
+//   p_ready  (count 128)     P / dS written to TMEM by the row role
+//   acc_done                 the task's accumulators are final
+//   acc_free (count 128)     the epilogue has read them
+#pragma once
+#include "fa_kernel.cuh"
+
+namespace fa {
+
+enum : int { kBwdDkDv = 0, kBwdDq = 1 };
+constexpr int kBwdThreads = 192;
+
+struct BwdParams {
+  CUtensorMap tm_r0, tm_r1;  // resident tiles: (K, V) for dK/dV, (Q, dO) for dQ; 4-D (d, H, S, B)
+  CUtensorMap tm_t0, tm_t1;  // streamed tiles: (Q, dO) for dK/dV, (K, V) for dQ
+  const float* l2;           // [B, Hq, sq_pad]: LSE * log2(e), +inf on padded / empty rows
+  const float* dvec;         // [B, Hq, sq_pad]: D = rowsum(dO * O), 0 on padded rows
+  uint16_t* out0;            // dV (dK/dV) or dQ, bf16 bits
+  uint16_t* out1;            // dK (dK/dV)
+  unsigned int* status;
+  int B, Hq, Hkv, Sq, Sk, sq_pad, ratio;
+  int causal;
+  int mq, nk;                // ceil(Sq / 128), ceil(Sk / 128)
+  int units, blocks;         // tasks = units * blocks: (b, head) units x 128-row blocks
+  int section_units;         // causal order: units per L2 section
+  float scale, scale_log2;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct BwdLayout {
+  static_assert(D == 64 || D == 128, "backward head dims");
+  static constexpr int NC = D / 64;
+  static constexpr int kTile = NC * kChunkBytes;  // one 128-row tile
+  static constexpr int kVec = 128 * 4;            // 128 fp32
+  static constexpr int kSlot = 2 * kTile + 2 * kVec;
+  static constexpr int kMaxSmem = 232448;
+  static constexpr int NSLOT_fit = (kMaxSmem - 2 * kTile - 2048 - 1024) / kSlot;
+  static constexpr int NSLOT = NSLOT_fit > 4 ? 4 : NSLOT_fit;
+  static_assert(NSLOT >= 2, "ring needs two slots");
+  static constexpr int oR0 = 0;
+  static constexpr int oR1 = kTile;
+  static constexpr int oRing = 2 * kTile;  // slot r: T0, T1, L2 vector, D vector
+  static constexpr int oBar = oRing + NSLOT * kSlot;
+  static constexpr int bResFull = 0;
+  static constexpr int bResEmpty = 1;
+  static constexpr int bTFull = 2;               // [NSLOT]
+  static constexpr int bTEmpty = 2 + NSLOT;      // [NSLOT]
+  static constexpr int bSFull = 2 + 2 * NSLOT;
+  static constexpr int bPReady = bSFull + 1;
+  static constexpr int bAccDone = bSFull + 2;
+  static constexpr int bAccFree = bSFull + 3;
+  static constexpr int bDrain = bSFull + 4;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int oMisc = oBar + kNumBars * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int kBytes = oMisc + 16;
+  static constexpr int kDynSmem = kBytes + 1024;
+  static_assert(kDynSmem <= kMaxSmem, "shared memory budget");
+  static __device__ __forceinline__ uint32_t slot_off(int r) { return oRing + r * kSlot; }
+};
+
+enum : unsigned int {
+  kSiteBwdRowS = 601,
+  kSiteBwdRowAcc = 602,
+  kSiteBwdMmaRes = 611,
+  kSiteBwdMmaT = 612,
+  kSiteBwdMmaP = 613,
+  kSiteBwdMmaAcc = 614,
+  kSiteBwdMmaDrain = 615,
+  kSiteBwdLoadRes = 621,
+  kSiteBwdLoadT = 622,
+  kSiteBwdLoadDrain = 623,
+};
+
+// One task of either direction.
+struct BwdTask {
+  int b, h;      // batch; K/V head (dK/dV) or query head (dQ)
+  int blk;       // 128-row block of the resident tiles
+  int it0;       // dK/dV: first query block; dQ: 0
+  int nit;       // streamed blocks (dK/dV: ratio query heads x (mq - it0) blocks)
+};
+
+// Task t.  Units are (b, head) pairs; tasks of a unit cover its 128-row
+// blocks.  Non-causal: unit by unit.  Causal: sections of `section_units`
+// units whose streamed tiles fit in L2 together, heaviest block first inside
+// a section (for dK/dV the first key blocks, which every later query sees;
+// for dQ the last query blocks, which see every earlier key).
+template <int KIND>
+__device__ __forceinline__ BwdTask bwd_task(const BwdParams& p, int t) {
+  BwdTask k;
+  const int M = p.blocks;
+  int unit, q;
+  if (!p.causal) {
+    unit = t / M;
+    q = t - unit * M;
+  } else {
+    const int su = p.section_units;
+    const int section = t / (su * M);
+    const int first = section * su;
+    int in_section = p.units - first;
+    if (in_section > su) in_section = su;
+    const int idx = t - section * su * M;
+    q = idx / in_section;  // heaviness rank inside the section
+    unit = first + (idx - q * in_section);
+  }
+  const int H = KIND == kBwdDkDv ? p.Hkv : p.Hq;
+  k.b = unit / H;
+  k.h = unit - k.b * H;
+  if (KIND == kBwdDkDv) {
+    k.blk = q;  // key block, heaviest (lowest) first
+    int first_q = 0;
+    if (p.causal) {  // the first query that sees key blk * 128: q >= k - (Sk - Sq)
+      const int qmin = k.blk * kBN - (p.Sk - p.Sq);
+      first_q = qmin > 0 ? qmin / kBM : 0;
+    }
+    k.it0 = first_q;
+    k.nit = first_q < p.mq ? p.ratio * (p.mq - first_q) : 0;
+  } else {
+    k.blk = p.causal ? M - 1 - q : q;  // query block, heaviest (highest) first under the mask
+    k.it0 = 0;
+    int n = p.nk;
+    if (p.causal) {
+      int last = (k.blk + 1) * kBM;
+      if (last > p.Sq) last = p.Sq;
+      const int64_t max_key = static_cast<int64_t>(last - 1) + p.Sk - p.Sq;
+      n = max_key < 0 ? 0 : static_cast<int>(max_key / kBN + 1);
+      if (n > p.nk) n = p.nk;
+    }
+    k.nit = k.blk * kBM < p.Sq ? n : 0;
+  }
+  return k;
+}
+
+// Streamed block `it` of a task: for dK/dV the query head and query block,
+// for dQ the key block.
+struct BwdIter {
+  int head;  // head of the streamed tiles' view
+  int blk;   // their 128-row block
+};
+
+template <int KIND>
+__device__ __forceinline__ BwdIter bwd_iter(const BwdParams& p, const BwdTask& k, int it) {
+  BwdIter r;
+  if (KIND == kBwdDkDv) {
+    const int nq = p.mq - k.it0;
+    const int hh = it / nq;
+    r.head = k.h * p.ratio + hh;
+    r.blk = k.it0 + (it - hh * nq);
+  } else {
+    r.head = k.h / p.ratio;  // the K/V head the query head reads
+    r.blk = it;
+  }
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// row role (warps 0-3): thread = row = TMEM lane
+// ---------------------------------------------------------------------------
+// Per streamed block: P = 2^(S * scale * log2(e) - LSE * log2(e)) on the
+// visible entries (0 elsewhere), dS = P (dP - D).  dK/dV: rows are keys and
+// columns queries (LSE and D per column, from the block's vectors in the ring
+// slot); dQ: rows are queries (LSE and D per row) and columns keys.
+template <int D, int KIND, bool CAUSAL>
+__device__ __forceinline__ void bwd_row_role(const BwdParams& p, const uint32_t tmem, const uint32_t sbase,
+                                             const uint8_t* smem, const WaitCtx& wc) {
+  using L = BwdLayout<D>;
+  const int t = threadIdx.x;
+  const uint32_t lane_off = static_cast<uint32_t>(t & ~31) << 16;
+  const uint32_t tS = tmem + lane_off;          // S (dK/dV: S^T), then P^T (dK/dV) or dS (dQ) over its first 64 columns
+  const uint32_t tP = tmem + lane_off + 128u;   // dP (dK/dV: dP^T), then dS^T (dK/dV) over its first 64 columns
+  const uint32_t bar0 = sbase + L::oBar;
+  const float sl2 = p.scale_log2;
+  uint32_t s_phase = 0, acc_phase = 0;
+  int slot_it = 0;
+  const int num_tasks = p.units * p.blocks;
+
+  for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
+    const BwdTask tk = bwd_task<KIND>(p, task);
+    const int row = tk.blk * kBM + t;  // key (dK/dV) or query (dQ)
+    float l2_row = 0.f, d_row = 0.f;
+    if (KIND == kBwdDq) {  // row < sq_pad: the block lies inside the padded rows
+      const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + tk.h) * p.sq_pad + row;
+      l2_row = p.l2[vi];
+      d_row = p.dvec[vi];
+    }
+    for (int it = 0; it < tk.nit; ++it, ++slot_it) {
+      const BwdIter bi = bwd_iter<KIND>(p, tk, it);
+      const int slot = slot_it % L::NSLOT;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bSFull, s_phase, wc, kSiteBwdRowS))) return;
+      s_phase ^= 1u;
+      tc_fence_after();
+
+      // visible columns c in [cmin, cmax]
+      int cmin = 0, cmax = kBN - 1;
+      bool row_ok = true;
+      if (KIND == kBwdDkDv) {
+        row_ok = row < p.Sk;
+        if (CAUSAL) cmin = row - (p.Sk - p.Sq) - bi.blk * kBM;  // query q sees key k iff q >= k - (Sk - Sq)
+      } else {
+        cmax = min(kBN - 1, p.Sk - 1 - bi.blk * kBN);  // keys < Sk
+        if (CAUSAL) cmax = min(cmax, row + (p.Sk - p.Sq) - bi.blk * kBN);
+      }
+      const float* l2v = reinterpret_cast<const float*>(smem + L::slot_off(slot) + 2 * L::kTile);
+      const float* dvv = l2v + 128;
+
+      // two halves of 64 columns: P of the half from S, P^T (dK/dV) back over
+      // S columns 32h .. 32h+31, then dS from dP 32 columns at a time, back
+      // over dP (dK/dV) or S (dQ) columns 32h + 16c ..; every TMEM column is
+      // read before anything is stored over it
+      const uint32_t tDst = KIND == kBwdDkDv ? tP : tS;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[64];
+        tmem_ld64_wait(tS + static_cast<uint32_t>(64 * h), r);
+        float pr[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const int c = 64 * h + i;
+          const float lse2 = KIND == kBwdDkDv ? l2v[c] : l2_row;
+          const bool vis = row_ok && c >= cmin && c <= cmax;
+          pr[i] = vis ? ex2_approx(__uint_as_float(r[i]) * sl2 - lse2) : 0.f;
+        }
+        if (KIND == kBwdDkDv) {  // P^T for dV += P^T dO
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+          tmem_st32(tS + static_cast<uint32_t>(32 * h), pk);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t dp[32];
+          tmem_ld32_wait(tP + static_cast<uint32_t>(64 * h + 32 * q), dp);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c0 = 64 * h + 32 * q + 2 * i;
+            const float d0 = KIND == kBwdDkDv ? dvv[c0] : d_row;
+            const float d1 = KIND == kBwdDkDv ? dvv[c0 + 1] : d_row;
+            pk[i] = pack_bf16x2(pr[32 * q + 2 * i] * (__uint_as_float(dp[2 * i]) - d0),
+                                pr[32 * q + 2 * i + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
+          }
+          tmem_st16(tDst + static_cast<uint32_t>(32 * h + 16 * q), pk);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar0 + 8u * L::bPReady);
+    }
+
+    // epilogue: accumulators -> bf16 rows (dK scaled by `scale`, dQ too)
+    if (tk.nit > 0) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bAccDone, acc_phase, wc, kSiteBwdRowAcc))) return;
+      acc_phase ^= 1u;
+      tc_fence_after();
+    }
+    const bool store = KIND == kBwdDkDv ? row < p.Sk : row < p.Sq;
+    constexpr int kAccs = KIND == kBwdDkDv ? 2 : 1;
+#pragma unroll 1
+    for (int a = 0; a < kAccs; ++a) {
+      uint16_t* dst;
+      float mult;
+      if (KIND == kBwdDkDv) {
+        const int64_t off = ((static_cast<int64_t>(tk.b) * p.Sk + row) * p.Hkv + tk.h) * D;
+        dst = (a == 0 ? p.out0 : p.out1) + off;  // dV, dK
+        mult = a == 0 ? 1.f : p.scale;
+      } else {
+        dst = p.out0 + ((static_cast<int64_t>(tk.b) * p.Sq + row) * p.Hq + tk.h) * D;
+        mult = p.scale;
+      }
+      const uint32_t tA = tmem + lane_off + 256u + static_cast<uint32_t>(128 * a);
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t v[32];
+        if (tk.nit > 0) {  // uniform across the CTA: the loads stay warp-collective
+          tmem_ld32_wait(tA + static_cast<uint32_t>(c), v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (store) {
+          uint4* o4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * mult, __uint_as_float(v[8 * q + 1]) * mult);
+            w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mult, __uint_as_float(v[8 * q + 3]) * mult);
+            w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mult, __uint_as_float(v[8 * q + 5]) * mult);
+            w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mult, __uint_as_float(v[8 * q + 7]) * mult);
+            o4[q] = w;
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar0 + 8u * L::bAccFree);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issue (warp 4; lane 0 issues)
+// ---------------------------------------------------------------------------
+template <int D, int KIND>
+__device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t tmem, const uint32_t sbase,
+                                             const WaitCtx& wc) {
+  using L = BwdLayout<D>;
+  const uint32_t bar0 = sbase + L::oBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const uint32_t leader = (threadIdx.x & 31) == 0 ? 1u : 0u;
+  auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
+    return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
+  };
+  uint32_t res_phase = 0, p_phase = 0, free_phase = 0;
+  int slot_it = 0;
+  const int num_tasks = p.units * p.blocks;
+  const uint32_t r0 = sbase + L::oR0, r1 = sbase + L::oR1;
+
+  for (int task = blockIdx.x, n = 0; task < num_tasks; task += gridDim.x, ++n) {
+    const BwdTask tk = bwd_task<KIND>(p, task);
+    if (!wait(bar(L::bResFull), res_phase, kSiteBwdMmaRes)) goto out;
+    res_phase ^= 1u;
+    // the previous task's epilogue has read the accumulators
+    if (n > 0) {
+      if (!wait(bar(L::bAccFree), free_phase, kSiteBwdMmaAcc)) goto out;
+      free_phase ^= 1u;
+    }
+    tc_fence_after();
+    for (int it = 0; it < tk.nit; ++it, ++slot_it) {
+      const int slot = slot_it % L::NSLOT;
+      const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kTile;
+      if (!wait(bar(L::bTFull + slot), static_cast<uint32_t>(slot_it / L::NSLOT) & 1u, kSiteBwdMmaT)) goto out;
+      tc_fence_after();
+      issue_qk<D, D>(tmem, r0, t0, leader);         // S  = R0 T0^T  (dK/dV: K Q^T;  dQ: Q K^T)
+      issue_qk<D, D>(tmem + 128u, r1, t1, leader);  // dP = R1 T1^T  (dK/dV: V dO^T; dQ: dO V^T)
+      mma_commit(bar(L::bSFull), leader);
+      if (!wait(bar(L::bPReady), p_phase, kSiteBwdMmaP)) goto out;
+      p_phase ^= 1u;
+      tc_fence_after();
+      if (KIND == kBwdDkDv) {
+        issue_pv_half<D>(tmem + 256u, tmem, t1, 0, it > 0, leader);  // dV += P^T dO
+        issue_pv_half<D>(tmem + 256u, tmem, t1, 1, true, leader);
+        issue_pv_half<D>(tmem + 384u, tmem + 128u, t0, 0, it > 0, leader);  // dK += dS^T Q
+        issue_pv_half<D>(tmem + 384u, tmem + 128u, t0, 1, true, leader);
+      } else {
+        issue_pv_half<D>(tmem + 256u, tmem, t0, 0, it > 0, leader);  // dQ += dS K
+        issue_pv_half<D>(tmem + 256u, tmem, t0, 1, true, leader);
+      }
+      mma_commit(bar(L::bTEmpty + slot), leader);
+    }
+    if (tk.nit > 0) mma_commit(bar(L::bAccDone), leader);
+    mma_commit(bar(L::bResEmpty), leader);
+  }
+out:
+  mma_commit(bar(L::bDrain), leader);
+  mbar_drain_wait(bar(L::bDrain), 0u, wc, kSiteBwdMmaDrain);
+}
+
+// ---------------------------------------------------------------------------
+// TMA loads (warp 5, one lane)
+// ---------------------------------------------------------------------------
+template <int D, int KIND>
+__device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t sbase, const WaitCtx& wc) {
+  using L = BwdLayout<D>;
+  const uint32_t bar0 = sbase + L::oBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t res_uses = 0;
+  int slot_it = 0;
+  const int num_tasks = p.units * p.blocks;
+  tma_prefetch_desc(&p.tm_r0);
+  tma_prefetch_desc(&p.tm_r1);
+  tma_prefetch_desc(&p.tm_t0);
+  tma_prefetch_desc(&p.tm_t1);
+
+  for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
+    const BwdTask tk = bwd_task<KIND>(p, task);
+    if (res_uses > 0 && !mbar_wait(bar(L::bResEmpty), (res_uses - 1u) & 1u, wc, kSiteBwdLoadRes)) goto out;
+    mbar_arrive_expect_tx(bar(L::bResFull), 2u * L::kTile);
+    for (int c = 0; c < L::NC; ++c) {
+      tma_load_4d(sbase + L::oR0 + c * kChunkBytes, &p.tm_r0, bar(L::bResFull), c * 64, tk.h, tk.blk * kBM, tk.b);
+      tma_load_4d(sbase + L::oR1 + c * kChunkBytes, &p.tm_r1, bar(L::bResFull), c * 64, tk.h, tk.blk * kBM, tk.b);
+    }
+    ++res_uses;
+    for (int it = 0; it < tk.nit; ++it, ++slot_it) {
+      const int slot = slot_it % L::NSLOT;
+      if (slot_it >= L::NSLOT &&
+          !mbar_wait(bar(L::bTEmpty + slot), static_cast<uint32_t>(slot_it / L::NSLOT - 1) & 1u, wc,
+                     kSiteBwdLoadT))
+        goto out;
+      const BwdIter bi = bwd_iter<KIND>(p, tk, it);
+      const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kTile;
+      const uint32_t fb = bar(L::bTFull + slot);
+      mbar_arrive_expect_tx(fb, 2u * L::kTile + (KIND == kBwdDkDv ? 2u * L::kVec : 0u));
+      for (int c = 0; c < L::NC; ++c) {
+        tma_load_4d(t0 + c * kChunkBytes, &p.tm_t0, fb, c * 64, bi.head, bi.blk * kBM, tk.b);
+        tma_load_4d(t1 + c * kChunkBytes, &p.tm_t1, fb, c * 64, bi.head, bi.blk * kBM, tk.b);
+      }
+      if (KIND == kBwdDkDv) {  // the block's LSE and D vectors (whole padded blocks: always in range)
+        const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + bi.head) * p.sq_pad + bi.blk * kBM;
+        bulk_load(t1 + L::kTile, p.l2 + vi, L::kVec, fb);
+        bulk_load(t1 + L::kTile + L::kVec, p.dvec + vi, L::kVec, fb);
+      }
+    }
+  }
+out:
+  if (res_uses > 0) mbar_drain_wait(bar(L::bResFull), (res_uses - 1u) & 1u, wc, kSiteBwdLoadDrain);
+  for (int i = 0; i < L::NSLOT && i < slot_it; ++i) {
+    const uint32_t uses = static_cast<uint32_t>((slot_it - i + L::NSLOT - 1) / L::NSLOT);
+    mbar_drain_wait(bar(L::bTFull + i), (uses - 1u) & 1u, wc, kSiteBwdLoadDrain);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int D, int KIND, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::oMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    const uint32_t b = sbase + L::oBar;
+    mbar_init(b + 8 * L::bResFull, 1);
+    mbar_init(b + 8 * L::bResEmpty, 1);
+    for (int i = 0; i < L::NSLOT; ++i) {
+      mbar_init(b + 8 * (L::bTFull + i), 1);
+      mbar_init(b + 8 * (L::bTEmpty + i), 1);
+    }
+    mbar_init(b + 8 * L::bSFull, 1);
+    mbar_init(b + 8 * L::bPReady, 128);
+    mbar_init(b + 8 * L::bAccDone, 1);
+    mbar_init(b + 8 * L::bAccFree, 128);
+    mbar_init(b + 8 * L::bDrain, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+
+  if (warp < 4) {
+    bwd_row_role<D, KIND, CAUSAL>(p, tmem, sbase, smem, wc);
+  } else if (warp == 4) {
+    bwd_mma_role<D, KIND>(p, tmem, sbase, wc);
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) bwd_load_role<D, KIND>(p, sbase, wc);
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// prep: D = rowsum(dO * O) and LSE * log2(e) per (b, query head, row), rows
+// padded to whole 128-row blocks; one warp per row
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __restrict__ o,
+                                                          const uint16_t* __restrict__ dout,
+                                                          const float* __restrict__ lse, float* __restrict__ l2,
+                                                          float* __restrict__ dvec, int B, int Hq, int Sq,
+                                                          int sq_pad) {
+  constexpr int kPer = D / 32;  // 2 or 4 bf16 per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = static_cast<int64_t>(B) * Hq * sq_pad;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += step) {
+    const int64_t bh = r / sq_pad;
+    const int i = static_cast<int>(r - bh * sq_pad);
+    const int64_t b = bh / Hq;
+    const int h = static_cast<int>(bh - b * Hq);
+    float acc = 0.f;
+    if (i < Sq) {
+      const int64_t off = ((b * Sq + i) * Hq + h) * D + lane * kPer;
+      uint32_t ow[kPer / 2], gw[kPer / 2];
+      if constexpr (kPer == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+        const uint2 g = *reinterpret_cast<const uint2*>(dout + off);
+        ow[0] = a.x, ow[1] = a.y, gw[0] = g.x, gw[1] = g.y;
+      } else {
+        ow[0] = *reinterpret_cast<const uint32_t*>(o + off);
+        gw[0] = *reinterpret_cast<const uint32_t*>(dout + off);
+      }
+#pragma unroll
+      for (int w = 0; w < kPer / 2; ++w) {
+        acc += __uint_as_float(ow[w] << 16) * __uint_as_float(gw[w] << 16);
+        acc += __uint_as_float(ow[w] & 0xffff0000u) * __uint_as_float(gw[w] & 0xffff0000u);
+      }
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) {
+      float v = INFINITY;  // padded rows, and rows with no visible key, get P = 0
+      if (i < Sq) {
+        const float l = lse[bh * Sq + i];
+        if (l != -INFINITY) v = l * 1.4426950408889634f;
+      }
+      l2[r] = v;
+      dvec[r] = i < Sq ? acc : 0.f;
+    }
+  }
+}
+
+
+}  // namespace fa

@@ -1,0 +1,22 @@
+// Backward launch table (instantiated in fa_bwd.cu, its own translation unit).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "fa_bwd.cuh"
+
+namespace fa {
+
+struct BwdEntry {
+  const void* fn;  // the __global__ function (for attributes)
+  int smem;        // dynamic shared memory bytes
+  cudaError_t (*launch)(const BwdParams& p, int grid, cudaStream_t stream);
+};
+
+// false when (d, kind, causal) is not built
+bool bwd_entry(int d, int kind, int causal, BwdEntry* out);
+
+// D = rowsum(dO * O) and LSE * log2(e) per row, padded to whole 128-row blocks
+cudaError_t launch_bwd_prep(int d, const void* o, const void* dout, const float* lse, float* l2, float* dvec, int B,
+                            int Hq, int Sq, int sq_pad, int max_blocks, cudaStream_t stream);
+
+}  // namespace fa

@@ -168,6 +168,41 @@ int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, in
                           int causal, int pack, int num_sms);
 
 /*
+ * Exact attention backward: dQ, dK, dV for a given dO = dLoss/dO, from the
+ * forward's inputs, output O and lse ("Infra: Flash Attention", section "Why
+ * backward recomputes": P is recomputed from lse, never stored;
+ * dV = P^T dO, dP = dO V^T, dS = P (dP - D) with D_i = dO_i . O_i,
+ * dQ = scale dS K, dK = scale dS^T Q).  A shared key/value head (GQA/MQA)
+ * receives the sum over its query heads.
+ *
+ * Layouts as fa_fwd: q, o, dout, dq [batch, seqlen_q, heads_q, d];
+ * k, v, dk, dv [batch, seqlen_k, heads_kv, d]; lse [batch, heads_q, seqlen_q]
+ * fp32 as fa_fwd writes it.  d_qk == d_v in {64, 128} (FA_ERR_UNSUPPORTED
+ * otherwise).  dq, dk, dv are written whole (bf16).
+ *
+ * workspace: device memory, 16-byte aligned, at least
+ * fa_bwd_workspace_size(batch, heads_q, seqlen_q) bytes: D and lse * log2(e) per query row, padded to
+ * whole 128-row blocks.  Calls that may overlap need different workspaces.
+ *
+ * Three launches on `stream`: the row preparation, the dK/dV kernel and the
+ * dQ kernel; no atomics, so the result is deterministic.  seqlen_q == 0
+ * writes dK = dV = 0; seqlen_k == 0 writes dQ = 0.  fa_options: grid and
+ * timeout_s apply; tau, pack > 1, exp_emu, debug_flags and workspace do not
+ * (FA_ERR_UNSUPPORTED when set).
+ */
+size_t fa_bwd_workspace_size(int batch, int heads_q, int seqlen_q);
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k,
+           int d_qk, int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
+           fa_stream_t stream);
+
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+              void* dq, void* dk, void* dv, int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k,
+              int d_qk, int d_v, int causal, float scale, void* workspace, size_t workspace_bytes,
+              const fa_options* opts, fa_stream_t stream);
+
+/*
  * Test hook for the emulated exponential: for i < n, y_fma[i] = 2^x[i] by the
  * FMA-pipe polynomial used with exp_emu = 1, y_mufu[i] = the hardware ex2
  * (ex2.approx.ftz).  Device pointers, fp32; stream-ordered.

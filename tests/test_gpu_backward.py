@@ -1,0 +1,105 @@
+"""Backward pass on the GPU (through the C ABI) against the fp64 oracle.
+
+The forward's O and LSE come from the CUDA forward; dO is seeded N(0,1) bf16.
+The oracle differentiates the exact definition from the same bf16 inputs.
+Tolerance, relative to the size of each reference gradient: the bf16 P, dS
+and outputs carry 2^-9 (2e-3) relative rounding, and the measured errors on
+these cases are 2-5e-3 of max|ref| at the worst element and 2.3e-3 of
+mean|ref| on average.  Bounds: max|d - ref| <= 2e-2 * max(max|ref|, 1e-3)
+and mean|d - ref| <= 1e-2 * max(mean|ref|, 1e-3) per gradient; the 1e-3
+floor covers gradients that vanish exactly (one key: P = 1, so dS = 0 and
+dQ = dK = 0, where the GPU leaves rounding of order 1e-7).
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MAX_REL, MEAN_REL = 2e-2, 1e-2
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_forward_08_gb300 as m
+    from exact_attention_forward_08_gb300 import _build
+    _build.build()
+    m.load_library()
+    return m
+
+
+def to_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def run(fa, w, seed):
+    q, k, v = w.generate()
+    g = synthetic.normal_bf16(w.shapes["o"], seed, 7)
+    qd, kd, vd, gd = (to_dev(a) for a in (q, k, v, g))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=w.causal, scale=w.softmax_scale)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, gd, causal=w.causal, scale=w.softmax_scale)
+    torch.cuda.synchronize()
+    code, detail = fa.fa_device_status()
+    assert code == 0, f"device status {code} {detail}"
+    return (q, k, v, g), (dq, dk, dv)
+
+
+def check(w, inputs, grads, what):
+    q, k, v, g = inputs
+    ref = oracle.attn_bwd(q, k, v, g, causal=w.causal, scale=w.softmax_scale)
+    out = {}
+    for name, got, want in zip(("dq", "dk", "dv"), grads, ref):
+        got = got.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), f"{what} {name}: non-finite"
+        err = np.abs(got - want)
+        scale_max = max(float(np.abs(want).max()), 1e-3)
+        scale_mean = max(float(np.abs(want).mean()), 1e-3)
+        out[name] = (float(err.max()) / scale_max, float(err.mean()) / scale_mean)
+        print(f"{what} {name}: max {out[name][0]:.2e} mean {out[name][1]:.2e} (|ref| max {scale_max:.3g})")
+        assert err.max() <= MAX_REL * scale_max, f"{what} {name}: max rel {out[name][0]:.3e}"
+        assert err.mean() <= MEAN_REL * scale_mean, f"{what} {name}: mean rel {out[name][1]:.3e}"
+    return out
+
+
+CASES = [
+    # name, B, Hq, Hkv, Sq, Sk, d, causal
+    ("b_tiny", 1, 2, 2, 128, 128, 64, False),
+    ("b_causal", 2, 4, 2, 300, 300, 128, True),
+    ("b_sq_lt_sk", 1, 8, 2, 200, 456, 128, True),
+    ("b_empty_rows", 1, 4, 2, 456, 200, 128, True),
+    ("b_mqa", 1, 8, 1, 257, 257, 64, True),
+    ("b_ragged", 2, 2, 2, 700, 530, 128, False),
+    ("b_many", 2, 8, 8, 1300, 1300, 64, True),
+    ("b_one_key", 1, 2, 1, 5, 1, 64, False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_backward_small(fa, case):
+    name, B, Hq, Hkv, Sq, Sk, d, causal = case
+    w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, d, d, causal, seed=zlib.crc32(name.encode()) % 1000)
+    inputs, grads = run(fa, w, 11)
+    check(w, inputs, grads, name)
+
+
+def test_backward_deterministic(fa):
+    w = synthetic.Workload("det", 2, 4, 2, 600, 600, 128, 128, True, seed=5)
+    _, g1 = run(fa, w, 3)
+    _, g2 = run(fa, w, 3)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_backward_degenerate(fa):
+    q = torch.randn(1, 0, 2, 64, device="cuda").to(torch.bfloat16)
+    k = torch.randn(1, 10, 2, 64, device="cuda").to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 0, device="cuda")
+    dq, dk, dv = fa.attention_backward(q, k, k, o, lse, o)
+    torch.cuda.synchronize()
+    assert torch.all(dk == 0) and torch.all(dv == 0)
