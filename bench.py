@@ -36,6 +36,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s on 1 GB300 (BF16) and % of dense BF16 tensor peak"
+METRIC_BWD = "attention bwd TFLOP/s on 1 GB300 (BF16, 2.5x forward flops) and % of dense BF16 tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0  # burst bf16 of one earlier GB300 measurement
 FALLBACK_HBM_GBS = 6800.0      # copy bandwidth of one earlier GB300 measurement
 KERNEL_NAME = "fa_fwd_kernel"
@@ -54,6 +55,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--dynamic", action="store_true",
                     help="fixed-length workloads: assign tasks dynamically (scheduling workspace)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="fwd: the forward (default); bwd: the backward (dQ, dK, dV), flops counted as 2.5x the "
+                         "forward's")
     ap.add_argument("--splitkv", type=int, default=0,
                     help="split-KV ranges for fixed-length workloads (decode workloads always split; 0 = auto there)")
     a = ap.parse_args(argv)
@@ -467,6 +471,151 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------------------
+# our arm, backward
+# ---------------------------------------------------------------------------
+
+def bwd_cpu_sample(w, q, k, v, g, seconds: float):
+    """Time the backward oracle on the first rows of every (batch, head): the
+    same key count and heads, fewer query rows (the oracle's cost per query
+    row is that of the full problem's).  Returns (TFLOP/s, sample text, s)."""
+    import oracle
+    threads = oracle.default_threads()
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.attn_bwd(q[:, :rows], k, v, g[:, :rows], causal=w.causal, scale=w.softmax_scale, threads=threads)
+        return time.perf_counter() - t0
+
+    rows = max(1, min(w.seqlen_q, 8))
+    dt = run(rows)
+    rows = int(max(1, min(w.seqlen_q, rows * seconds / max(dt, 1e-3))))
+    dt = run(rows)
+    flops = 2.5 * 2.0 * w.batch * w.heads_q * rows * w.seqlen_k * (w.d_qk + w.d_v)
+    if w.causal:
+        flops /= 2
+    text = (f"first {rows} of {w.seqlen_q} query rows of every (batch, head) of {w.name} (fp64 C oracle backward, "
+            f"{min(threads, w.batch * w.heads_kv)} threads over batch x key/value heads, {dt:.1f} s)")
+    return flops / dt / 1e12, text, dt, min(threads, w.batch * w.heads_kv)
+
+
+def run_ours_bwd(args):
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    import exact_attention_forward_08_gb300 as fa
+    import synthetic
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl" if world > 1 else "gloo")
+    fa.load_library()
+    w0 = get_workload(args.config)
+    if is_varlen(w0):
+        raise SystemExit("--pass bwd takes fixed-length workloads")
+    w = dataclasses.replace(w0, seed=rank_batch_seed(w0.seed, rank))
+    qb, kb, vb = w.generate()
+    gb = synthetic.normal_bf16(w.shapes["o"], w.seed, 7)
+    to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    qh, kh, vh, gh = (to_t(a).pin_memory() for a in (qb, kb, vb, gb))
+    qd, kd, vd, gd = (t.to(dev) for t in (qh, kh, vh, gh))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=w.causal, scale=w.softmax_scale)
+    oh, lh = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_bytes = fa.fa_bwd_workspace_size(w.batch, w.heads_q, w.seqlen_q)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+    scale = w.softmax_scale
+
+    def step():
+        rc = fa.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), gd.data_ptr(),
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.batch, w.heads_q, w.heads_kv, w.seqlen_q,
+                       w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, sp)
+        if rc != 0:
+            raise fa.FaError(rc, "fa_bwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    code, detail = fa.fa_device_status()
+    if code != 0:
+        raise fa.FaError(code, f"device status after warm-up {detail}")
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    clocks.start()
+    time.sleep(0.3 if clocks.enabled else 0)
+    for _ in range(args.warmup):
+        step()
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark("start")
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark("stop")
+    barrier()
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    clk = clocks.stop()
+    code, detail = fa.fa_device_status()
+    if code != 0:
+        raise fa.FaError(code, f"device status after timed region {detail}")
+    ms_step = ms_total / args.steps
+    flops = 2.5 * w.flops()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # end to end: the backward's inputs in, the three gradients out
+    dqh, dkh, dvh = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv))
+    host_in, dev_in = [qh, kh, vh, oh, lh, gh], [qd, kd, vd, o, lse, gd]
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip((dqh, dkh, dvh), (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev) / args.e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in (dqh, dkh, dvh))
+    peak, peak_src = load_peak()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    cfg = config_of(w, world, flops, False)
+    cfg["pass"] = "backward (dQ, dK, dV; flops = 2.5x forward, 5 GEMMs; the kernels run 7)"
+    result = {
+        "metric": METRIC_BWD, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
+        "gpu_launches": args.steps * 3,  # row preparation, dK/dV kernel, dQ kernel
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} (bf16 dense, burst)", "algorithmic_flops": flops},
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_, text, dt, cores = bwd_cpu_sample(w, qb, kb, vb, gb, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": v_, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": text,
+                                  "seconds": round(dt, 2)}
+    elif rank == 0:
+        result["cpu_baseline"] = None
+    return rank, result
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the fp64 oracle on the host cores
 # ---------------------------------------------------------------------------
 
@@ -483,6 +632,8 @@ def run_reference(args):
     w = get_workload(args.config)
     q, k, v = w.generate()
     threads = oracle.default_threads()
+    if args.pass_ == "bwd":
+        return rank, run_reference_bwd(args, w, q, k, v)
     rows_all = total_rows(w)
     per_row = w.flops() / rows_all
     rng = np.random.default_rng(777)
@@ -512,9 +663,39 @@ def run_reference(args):
     return rank, result
 
 
+def run_reference_bwd(args, w, q, k, v):
+    """The backward oracle, each step on the first rows of every (batch, head)
+    (bwd_cpu_sample), sized so the whole run stays near two minutes."""
+    import synthetic
+    if is_varlen(w):
+        raise SystemExit("--pass bwd takes fixed-length workloads")
+    g = synthetic.normal_bf16(w.shapes["o"], w.seed, 7)
+    per_step = min(10.0, 120.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        bwd_cpu_sample(w, q, k, v, g, per_step)
+    runs = [bwd_cpu_sample(w, q, k, v, g, per_step) for _ in range(args.steps)]
+    value = sum(r[0] for r in runs) / len(runs)
+    cfg = config_of(w, 1, 2.5 * w.flops(), False)
+    cfg["pass"] = "backward (flops = 2.5x forward)"
+    return {
+        "metric": METRIC_BWD, "impl": "reference", "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(r[2] for r in runs) / len(runs) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": runs[0][3], "kind": "oracle",
+                         "sample": runs[0][1]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
-    rank, result = (run_reference if args.impl == "reference" else run_ours)(args)
+    if args.impl == "reference":
+        runner = run_reference
+    else:
+        runner = run_ours_bwd if args.pass_ == "bwd" else run_ours
+    rank, result = runner(args)
     if rank == 0 and result is not None:
         print(json.dumps(result), flush=True)
     try:
