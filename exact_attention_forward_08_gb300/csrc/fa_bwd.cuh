@@ -24,30 +24,34 @@
 // per tile pair (S and dP recomputed) but needs neither the fp32 dQ
 // reductions across key blocks nor TMEM beyond 512 columns (S, dP, dK, dV).
 //
-// CTA: 192 threads, persistent (grid = SM count):
-//   warps 0-3  row role: thread = row = TMEM lane (a key for dK/dV, a query
-//              for dQ); P and dS, then the epilogue (accumulators -> bf16).
-//   warp 4     tcgen05.mma issue (one lane) and TMEM alloc / free.
-//   warp 5     TMA loads (one lane).
-// TMEM: S [0,128), dP [128,256), accumulator 0 [256, 256+D) (dV or dQ),
-// accumulator 1 [384, 384+D) (dK).  P (or dS for dQ) is written as packed
-// bf16 pairs over the first 64 columns of S, dS^T over the first 64 of dP.
+// CTA: 320 threads, persistent (grid = SM count).  Each 128-row streamed
+// block is taken as two 64-row stages (the forward's two-stage overlap: one
+// stage's row warps work while the other stage's GEMMs run):
+//   warps 0-3, 4-7  row role of stage 0 / 1: thread = row = TMEM lane (a key
+//              for dK/dV, a query for dQ); P and dS for the stage's 64
+//              columns, then the epilogue (accumulators -> bf16).
+//   warp 8     tcgen05.mma issue (one lane) and TMEM alloc / free.
+//   warp 9     TMA loads (one lane).
+// TMEM: S_0 [0,64), dP_0 [64,128), S_1 [128,192), dP_1 [192,256),
+// accumulator 0 [256, 256+D) (dV or dQ), accumulator 1 [384, 384+D) (dK).
+// P^T (dK/dV) or dS (dQ) is written as packed bf16 pairs over the first 32
+// columns of S_s, dS^T over the first 32 of dP_s.
 //
 // Hand-offs (all mbarriers, all waits bounded):
 //   res_full / res_empty     resident tiles of a task loaded / no longer read
 //   t_full[r] / t_empty[r]   ring slot r of streamed tiles (+ the LSE and D
 //                            vectors of the block for dK/dV)
-//   s_full                   S and dP of the current block in TMEM
-//   p_ready  (count 128)     P / dS written to TMEM by the row role
+//   s_full[s]                S_s and dP_s of the current block in TMEM
+//   p_ready[s] (count 128)   P / dS of stage s written to TMEM
 //   acc_done                 the task's accumulators are final
-//   acc_free (count 128)     the epilogue has read them
+//   acc_free (count 256)     the epilogue of both stages has read them
 #pragma once
 #include "fa_kernel.cuh"
 
 namespace fa {
 
 enum : int { kBwdDkDv = 0, kBwdDq = 1 };
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;
 
 struct BwdParams {
   CUtensorMap tm_r0, tm_r1;  // resident tiles: (K, V) for dK/dV, (Q, dO) for dQ; 4-D (d, H, S, B)
@@ -85,11 +89,11 @@ struct BwdLayout {
   static constexpr int bResEmpty = 1;
   static constexpr int bTFull = 2;               // [NSLOT]
   static constexpr int bTEmpty = 2 + NSLOT;      // [NSLOT]
-  static constexpr int bSFull = 2 + 2 * NSLOT;
-  static constexpr int bPReady = bSFull + 1;
-  static constexpr int bAccDone = bSFull + 2;
-  static constexpr int bAccFree = bSFull + 3;
-  static constexpr int bDrain = bSFull + 4;
+  static constexpr int bSFull = 2 + 2 * NSLOT;   // [2] per stage
+  static constexpr int bPReady = bSFull + 2;      // [2] per stage, count 128
+  static constexpr int bAccDone = bSFull + 4;
+  static constexpr int bAccFree = bSFull + 5;     // count 256
+  static constexpr int bDrain = bSFull + 6;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int oMisc = oBar + kNumBars * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int kBytes = oMisc + 16;
@@ -193,22 +197,45 @@ __device__ __forceinline__ BwdIter bwd_iter(const BwdParams& p, const BwdTask& k
 }
 
 // ---------------------------------------------------------------------------
-// row role (warps 0-3): thread = row = TMEM lane
+// S-like GEMM over half a streamed tile: D[128 x 64] = A[128 x D] B[64 x D]^T,
+// A and B K-major in SMEM (B = rows 64s .. 64s+63 of the streamed tile: the
+// 128-byte swizzle repeats every 8 rows, so the offset keeps its phase).
 // ---------------------------------------------------------------------------
-// Per streamed block: P = 2^(S * scale * log2(e) - LSE * log2(e)) on the
-// visible entries (0 elsewhere), dS = P (dP - D).  dK/dV: rows are keys and
-// columns queries (LSE and D per column, from the block's vectors in the ring
-// slot); dQ: rows are queries (LSE and D per row) and columns keys.
+template <int D>
+__device__ __forceinline__ void issue_qk64(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t leader) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint32_t co = opaque_u32(static_cast<uint32_t>(c * kChunkBytes));
+    mma_ss_x4<2, 2>(d_tmem, smem_desc_sw128(a_addr + co, 16, 1024), smem_desc_sw128(b_addr + co, 16, 1024), kIdesc,
+                    c != 0 ? 1u : 0u, leader);
+  }
+}
+
+// TMEM columns of stage s: S_s at 128 s, dP_s at 128 s + 64 (64 each);
+// accumulators at 256 (dV or dQ) and 384 (dK).
+__device__ __forceinline__ uint32_t bwd_s_col(int s) { return static_cast<uint32_t>(128 * s); }
+__device__ __forceinline__ uint32_t bwd_p_col(int s) { return static_cast<uint32_t>(128 * s + 64); }
+
+// ---------------------------------------------------------------------------
+// row role (warpgroup s = stage s): thread = row = TMEM lane
+// ---------------------------------------------------------------------------
+// Per streamed block, stage s takes its 64 columns (rows 64s .. 64s+63 of the
+// streamed tile): P = 2^(S * scale * log2(e) - LSE * log2(e)) on the visible
+// entries (0 elsewhere), dS = P (dP - D).  dK/dV: rows are keys, columns
+// queries (LSE and D per column, from the block's vectors in the ring slot);
+// dQ: rows are queries (LSE and D per row), columns keys.
 template <int D, int KIND, bool CAUSAL>
-__device__ __forceinline__ void bwd_row_role(const BwdParams& p, const uint32_t tmem, const uint32_t sbase,
-                                             const uint8_t* smem, const WaitCtx& wc) {
+__device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage, const uint32_t tmem,
+                                             const uint32_t sbase, const uint8_t* smem, const WaitCtx& wc) {
   using L = BwdLayout<D>;
-  const int t = threadIdx.x;
+  const int t = threadIdx.x - 128 * stage;
   const uint32_t lane_off = static_cast<uint32_t>(t & ~31) << 16;
-  const uint32_t tS = tmem + lane_off;          // S (dK/dV: S^T), then P^T (dK/dV) or dS (dQ) over its first 64 columns
-  const uint32_t tP = tmem + lane_off + 128u;   // dP (dK/dV: dP^T), then dS^T (dK/dV) over its first 64 columns
+  const uint32_t tS = tmem + lane_off + bwd_s_col(stage);  // S_s, then P^T (dK/dV) or dS (dQ) over its first 32 columns
+  const uint32_t tP = tmem + lane_off + bwd_p_col(stage);  // dP_s, then dS^T (dK/dV) over its first 32 columns
   const uint32_t bar0 = sbase + L::oBar;
   const float sl2 = p.scale_log2;
+  const int cb = 64 * stage;  // first column of this stage inside the streamed block
   uint32_t s_phase = 0, acc_phase = 0;
   int slot_it = 0;
   const int num_tasks = p.units * p.blocks;
@@ -225,108 +252,104 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const uint32_t 
     for (int it = 0; it < tk.nit; ++it, ++slot_it) {
       const BwdIter bi = bwd_iter<KIND>(p, tk, it);
       const int slot = slot_it % L::NSLOT;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bSFull, s_phase, wc, kSiteBwdRowS))) return;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (L::bSFull + stage), s_phase, wc, kSiteBwdRowS))) return;
       s_phase ^= 1u;
       tc_fence_after();
 
-      // visible columns c in [cmin, cmax]
-      int cmin = 0, cmax = kBN - 1;
+      // visible columns c (0 .. 63 of this stage) in [cmin, cmax]
+      int cmin = 0, cmax = 63;
       bool row_ok = true;
       if (KIND == kBwdDkDv) {
         row_ok = row < p.Sk;
-        if (CAUSAL) cmin = row - (p.Sk - p.Sq) - bi.blk * kBM;  // query q sees key k iff q >= k - (Sk - Sq)
+        if (CAUSAL) cmin = row - (p.Sk - p.Sq) - bi.blk * kBM - cb;  // query q sees key k iff q >= k - (Sk - Sq)
       } else {
-        cmax = min(kBN - 1, p.Sk - 1 - bi.blk * kBN);  // keys < Sk
-        if (CAUSAL) cmax = min(cmax, row + (p.Sk - p.Sq) - bi.blk * kBN);
+        cmax = min(63, p.Sk - 1 - bi.blk * kBN - cb);  // keys < Sk
+        if (CAUSAL) cmax = min(cmax, row + (p.Sk - p.Sq) - bi.blk * kBN - cb);
       }
-      const float* l2v = reinterpret_cast<const float*>(smem + L::slot_off(slot) + 2 * L::kTile);
+      const float* l2v = reinterpret_cast<const float*>(smem + L::slot_off(slot) + 2 * L::kTile) + cb;
       const float* dvv = l2v + 128;
 
-      // two halves of 64 columns: P of the half from S, P^T (dK/dV) back over
-      // S columns 32h .. 32h+31, then dS from dP 32 columns at a time, back
-      // over dP (dK/dV) or S (dQ) columns 32h + 16c ..; every TMEM column is
-      // read before anything is stored over it
+      uint32_t r[64];
+      tmem_ld64_wait(tS, r);
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float lse2 = KIND == kBwdDkDv ? l2v[c] : l2_row;
+        const bool vis = row_ok && c >= cmin && c <= cmax;
+        pr[c] = vis ? ex2_approx(__uint_as_float(r[c]) * sl2 - lse2) : 0.f;
+      }
+      if (KIND == kBwdDkDv) {  // P^T for dV += P^T dO
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+        tmem_st32(tS, pk);
+      }
+      // dS = P (dP - D), 32 columns at a time, onto columns 16q .. 16q+15 of
+      // dP (dK/dV) or S (dQ), all of them read already
       const uint32_t tDst = KIND == kBwdDkDv ? tP : tS;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t r[64];
-        tmem_ld64_wait(tS + static_cast<uint32_t>(64 * h), r);
-        float pr[64];
+      for (int q = 0; q < 2; ++q) {
+        uint32_t dp[32];
+        tmem_ld32_wait(tP + static_cast<uint32_t>(32 * q), dp);
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int c = 64 * h + i;
-          const float lse2 = KIND == kBwdDkDv ? l2v[c] : l2_row;
-          const bool vis = row_ok && c >= cmin && c <= cmax;
-          pr[i] = vis ? ex2_approx(__uint_as_float(r[i]) * sl2 - lse2) : 0.f;
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = 32 * q + 2 * i;
+          const float d0 = KIND == kBwdDkDv ? dvv[c0] : d_row;
+          const float d1 = KIND == kBwdDkDv ? dvv[c0 + 1] : d_row;
+          pk[i] = pack_bf16x2(pr[c0] * (__uint_as_float(dp[2 * i]) - d0),
+                              pr[c0 + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
         }
-        if (KIND == kBwdDkDv) {  // P^T for dV += P^T dO
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
-          tmem_st32(tS + static_cast<uint32_t>(32 * h), pk);
-        }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t dp[32];
-          tmem_ld32_wait(tP + static_cast<uint32_t>(64 * h + 32 * q), dp);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c0 = 64 * h + 32 * q + 2 * i;
-            const float d0 = KIND == kBwdDkDv ? dvv[c0] : d_row;
-            const float d1 = KIND == kBwdDkDv ? dvv[c0 + 1] : d_row;
-            pk[i] = pack_bf16x2(pr[32 * q + 2 * i] * (__uint_as_float(dp[2 * i]) - d0),
-                                pr[32 * q + 2 * i + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
-          }
-          tmem_st16(tDst + static_cast<uint32_t>(32 * h + 16 * q), pk);
-        }
+        tmem_st16(tDst + static_cast<uint32_t>(16 * q), pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar0 + 8u * L::bPReady);
+      mbar_arrive(bar0 + 8u * (L::bPReady + stage));
     }
 
-    // epilogue: accumulators -> bf16 rows (dK scaled by `scale`, dQ too)
+    // epilogue: dK/dV: stage 0 writes dV, stage 1 dK (scaled); dQ: stage s
+    // writes columns [s D/2, (s+1) D/2) (scaled)
     if (tk.nit > 0) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bAccDone, acc_phase, wc, kSiteBwdRowAcc))) return;
       acc_phase ^= 1u;
       tc_fence_after();
     }
     const bool store = KIND == kBwdDkDv ? row < p.Sk : row < p.Sq;
-    constexpr int kAccs = KIND == kBwdDkDv ? 2 : 1;
+    uint16_t* dst;
+    float mult;
+    uint32_t tA;
+    int c_lo, c_hi;
+    if (KIND == kBwdDkDv) {
+      const int64_t off = ((static_cast<int64_t>(tk.b) * p.Sk + row) * p.Hkv + tk.h) * D;
+      dst = (stage == 0 ? p.out0 : p.out1) + off;  // dV, dK
+      mult = stage == 0 ? 1.f : p.scale;
+      tA = tmem + lane_off + (stage == 0 ? 256u : 384u);
+      c_lo = 0, c_hi = D;
+    } else {
+      dst = p.out0 + ((static_cast<int64_t>(tk.b) * p.Sq + row) * p.Hq + tk.h) * D;
+      mult = p.scale;
+      tA = tmem + lane_off + 256u;
+      c_lo = stage * (D / 2), c_hi = c_lo + D / 2;
+    }
 #pragma unroll 1
-    for (int a = 0; a < kAccs; ++a) {
-      uint16_t* dst;
-      float mult;
-      if (KIND == kBwdDkDv) {
-        const int64_t off = ((static_cast<int64_t>(tk.b) * p.Sk + row) * p.Hkv + tk.h) * D;
-        dst = (a == 0 ? p.out0 : p.out1) + off;  // dV, dK
-        mult = a == 0 ? 1.f : p.scale;
+    for (int c = c_lo; c < c_hi; c += 32) {
+      uint32_t v[32];
+      if (tk.nit > 0) {  // uniform across the CTA: the loads stay warp-collective
+        tmem_ld32_wait(tA + static_cast<uint32_t>(c), v);
       } else {
-        dst = p.out0 + ((static_cast<int64_t>(tk.b) * p.Sq + row) * p.Hq + tk.h) * D;
-        mult = p.scale;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
       }
-      const uint32_t tA = tmem + lane_off + 256u + static_cast<uint32_t>(128 * a);
-#pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        if (tk.nit > 0) {  // uniform across the CTA: the loads stay warp-collective
-          tmem_ld32_wait(tA + static_cast<uint32_t>(c), v);
-        } else {
+      if (store) {
+        uint4* o4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0u;
-        }
-        if (store) {
-          uint4* o4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * mult, __uint_as_float(v[8 * q + 1]) * mult);
-            w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mult, __uint_as_float(v[8 * q + 3]) * mult);
-            w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mult, __uint_as_float(v[8 * q + 5]) * mult);
-            w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mult, __uint_as_float(v[8 * q + 7]) * mult);
-            o4[q] = w;
-          }
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * mult, __uint_as_float(v[8 * q + 1]) * mult);
+          w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mult, __uint_as_float(v[8 * q + 3]) * mult);
+          w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mult, __uint_as_float(v[8 * q + 5]) * mult);
+          w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mult, __uint_as_float(v[8 * q + 7]) * mult);
+          o4[q] = w;
         }
       }
     }
@@ -336,8 +359,11 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const uint32_t 
 }
 
 // ---------------------------------------------------------------------------
-// MMA issue (warp 4; lane 0 issues)
+// MMA issue (warp 8; lane 0 issues)
 // ---------------------------------------------------------------------------
+// Per streamed block j and stage s: the accumulating GEMMs of (j, s) as soon
+// as stage s has written P / dS, then S and dP of (j+1, s), so one stage's
+// row warps work while the other stage's GEMMs run.
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t tmem, const uint32_t sbase,
                                              const WaitCtx& wc) {
@@ -348,40 +374,63 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
   auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
   };
-  uint32_t res_phase = 0, p_phase = 0, free_phase = 0;
+  uint32_t res_phase = 0, free_phase = 0, p_phase[2] = {0u, 0u};
   int slot_it = 0;
   const int num_tasks = p.units * p.blocks;
   const uint32_t r0 = sbase + L::oR0, r1 = sbase + L::oR1;
+  constexpr uint32_t kHalfRows = 64 * 128;  // bytes of 64 tile rows inside a 64-column chunk
+  auto issue_sdp = [&](int s, uint32_t t0, uint32_t t1) {
+    issue_qk64<D>(tmem + bwd_s_col(s), r0, t0 + s * kHalfRows, leader);  // S_s  = R0 T0_s^T
+    issue_qk64<D>(tmem + bwd_p_col(s), r1, t1 + s * kHalfRows, leader);  // dP_s = R1 T1_s^T
+    mma_commit(bar(L::bSFull + s), leader);
+  };
 
   for (int task = blockIdx.x, n = 0; task < num_tasks; task += gridDim.x, ++n) {
     const BwdTask tk = bwd_task<KIND>(p, task);
     if (!wait(bar(L::bResFull), res_phase, kSiteBwdMmaRes)) goto out;
     res_phase ^= 1u;
-    // the previous task's epilogue has read the accumulators
-    if (n > 0) {
+    if (n > 0) {  // the previous task's epilogue has read the accumulators
       if (!wait(bar(L::bAccFree), free_phase, kSiteBwdMmaAcc)) goto out;
       free_phase ^= 1u;
     }
     tc_fence_after();
+    if (tk.nit > 0) {
+      const int slot = slot_it % L::NSLOT;
+      if (!wait(bar(L::bTFull + slot), static_cast<uint32_t>(slot_it / L::NSLOT) & 1u, kSiteBwdMmaT)) goto out;
+      tc_fence_after();
+      const uint32_t t0 = sbase + L::slot_off(slot);
+      issue_sdp(0, t0, t0 + L::kTile);
+      issue_sdp(1, t0, t0 + L::kTile);
+    }
     for (int it = 0; it < tk.nit; ++it, ++slot_it) {
       const int slot = slot_it % L::NSLOT;
       const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kTile;
-      if (!wait(bar(L::bTFull + slot), static_cast<uint32_t>(slot_it / L::NSLOT) & 1u, kSiteBwdMmaT)) goto out;
-      tc_fence_after();
-      issue_qk<D, D>(tmem, r0, t0, leader);         // S  = R0 T0^T  (dK/dV: K Q^T;  dQ: Q K^T)
-      issue_qk<D, D>(tmem + 128u, r1, t1, leader);  // dP = R1 T1^T  (dK/dV: V dO^T; dQ: dO V^T)
-      mma_commit(bar(L::bSFull), leader);
-      if (!wait(bar(L::bPReady), p_phase, kSiteBwdMmaP)) goto out;
-      p_phase ^= 1u;
-      tc_fence_after();
-      if (KIND == kBwdDkDv) {
-        issue_pv_half<D>(tmem + 256u, tmem, t1, 0, it > 0, leader);  // dV += P^T dO
-        issue_pv_half<D>(tmem + 256u, tmem, t1, 1, true, leader);
-        issue_pv_half<D>(tmem + 384u, tmem + 128u, t0, 0, it > 0, leader);  // dK += dS^T Q
-        issue_pv_half<D>(tmem + 384u, tmem + 128u, t0, 1, true, leader);
-      } else {
-        issue_pv_half<D>(tmem + 256u, tmem, t0, 0, it > 0, leader);  // dQ += dS K
-        issue_pv_half<D>(tmem + 256u, tmem, t0, 1, true, leader);
+      const int nslot = (slot_it + 1) % L::NSLOT;
+      const uint32_t n0 = sbase + L::slot_off(nslot), n1 = n0 + L::kTile;
+      bool next_ready = false;
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!wait(bar(L::bPReady + s), p_phase[s], kSiteBwdMmaP)) goto out;
+        p_phase[s] ^= 1u;
+        tc_fence_after();
+        const bool acc = it > 0 || s > 0;
+        // A of stage s starts at its own S / dP columns (issue_pv_half adds 32 per half)
+        const uint32_t a_p = tmem + bwd_s_col(s) - 32u * s, a_ds = tmem + bwd_p_col(s) - 32u * s;
+        if (KIND == kBwdDkDv) {
+          issue_pv_half<D>(tmem + 256u, a_p, t1, s, acc, leader);   // dV += P^T_s dO_s
+          issue_pv_half<D>(tmem + 384u, a_ds, t0, s, acc, leader);  // dK += dS^T_s Q_s
+        } else {
+          issue_pv_half<D>(tmem + 256u, a_p, t0, s, acc, leader);   // dQ += dS_s K_s
+        }
+        if (it + 1 < tk.nit) {
+          if (!next_ready) {
+            if (!wait(bar(L::bTFull + nslot), static_cast<uint32_t>((slot_it + 1) / L::NSLOT) & 1u, kSiteBwdMmaT))
+              goto out;
+            tc_fence_after();
+            next_ready = true;
+          }
+          issue_sdp(s, n0, n1);
+        }
       }
       mma_commit(bar(L::bTEmpty + slot), leader);
     }
@@ -394,7 +443,7 @@ out:
 }
 
 // ---------------------------------------------------------------------------
-// TMA loads (warp 5, one lane)
+// TMA loads (warp 9, one lane)
 // ---------------------------------------------------------------------------
 template <int D, int KIND>
 __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t sbase, const WaitCtx& wc) {
@@ -471,15 +520,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
       mbar_init(b + 8 * (L::bTFull + i), 1);
       mbar_init(b + 8 * (L::bTEmpty + i), 1);
     }
-    mbar_init(b + 8 * L::bSFull, 1);
-    mbar_init(b + 8 * L::bPReady, 128);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(b + 8 * (L::bSFull + st), 1);
+      mbar_init(b + 8 * (L::bPReady + st), 128);
+    }
     mbar_init(b + 8 * L::bAccDone, 1);
-    mbar_init(b + 8 * L::bAccFree, 128);
+    mbar_init(b + 8 * L::bAccFree, 256);
     mbar_init(b + 8 * L::bDrain, 1);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
   }
@@ -489,19 +540,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   const uint32_t tmem = *tmem_holder;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
-  if (warp < 4) {
-    bwd_row_role<D, KIND, CAUSAL>(p, tmem, sbase, smem, wc);
-  } else if (warp == 4) {
+  if (warp < 8) {
+    bwd_row_role<D, KIND, CAUSAL>(p, warp >> 2, tmem, sbase, smem, wc);
+  } else if (warp == 8) {
     bwd_mma_role<D, KIND>(p, tmem, sbase, wc);
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) bwd_load_role<D, KIND>(p, sbase, wc);
     __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
