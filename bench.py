@@ -308,6 +308,54 @@ def cpu_baseline(w, q, k, v, seconds: float):
 
 
 # ---------------------------------------------------------------------------
+# end to end: host inputs in, call, results out, pipelined over two slots
+# ---------------------------------------------------------------------------
+
+def e2e_pipelined(torch, dev, launch, host_in, dev_in, dev_out, steps: int, warm: int = 3) -> float:
+    """Seconds per step of: copy this step's inputs from pinned host memory,
+    run `launch(inputs, outputs, stream)`, copy its outputs back to pinned host
+    memory.  Two slots of device buffers: the copies of step i+1 (H2D and D2H
+    on their own streams) overlap the call of step i, as a pipelined caller
+    would run them; every step still moves all of its own bytes.  Slot 0 is
+    (dev_in, dev_out); slot 1 is allocated here."""
+    ins = [dev_in, [torch.empty_like(t) for t in dev_in]]
+    outs = [dev_out, [torch.empty_like(t) for t in dev_out]]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out] for _ in range(2)]
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        for i in range(n):
+            k = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_done[k])  # the call of step i-2 has read these inputs
+                for d_, h_ in zip(ins[k], host_in):
+                    d_.copy_(h_, non_blocking=True)
+                ev_in[k].record(s_in)
+            comp.wait_event(ev_in[k])
+            if i >= 2:
+                comp.wait_event(ev_out[k])  # step i-2's results have been read back
+            launch(ins[k], outs[k], comp.cuda_stream)
+            ev_done[k].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[k])
+                for h_, d_ in zip(host_out[k], outs[k]):
+                    h_.copy_(d_, non_blocking=True)
+                ev_out[k].record(s_out)
+        torch.cuda.synchronize(dev)
+
+    run(warm)
+    barrier()
+    t0 = time.perf_counter()
+    run(steps)
+    return max_over_ranks(time.perf_counter() - t0, dev) / steps
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -350,10 +398,12 @@ def run_ours(args):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         launches_per_step = 2  # planning kernel + attention kernel
 
-        def step():
-            rc = fa.fa_fwd_varlen(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                  cqd.data_ptr(), ckd.data_ptr(), w.batch, w.total_q, w.total_k, w.heads_q,
-                                  w.heads_kv, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, sp)
+        def launch(ins, outs, stream):
+            q_, k_, v_, cq_, ck_ = ins
+            rc = fa.fa_fwd_varlen(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), outs[0].data_ptr(),
+                                  outs[1].data_ptr(), cq_.data_ptr(), ck_.data_ptr(), w.batch, w.total_q, w.total_k,
+                                  w.heads_q, w.heads_kv, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(),
+                                  ws_bytes, stream)
             if rc != 0:
                 raise fa.FaError(rc, "fa_fwd_varlen")
     elif is_decode(args.config) or args.splitkv > 0:
@@ -364,10 +414,10 @@ def run_ours(args):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         launches_per_step = 2 if splits > 1 else 1  # attention kernel + merge kernel
 
-        def step():
-            rc = fa.fa_fwd_splitkv(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                   w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v,
-                                   int(w.causal), scale, splits, ws.data_ptr(), ws_bytes, sp)
+        def launch(ins, outs, stream):
+            rc = fa.fa_fwd_splitkv(ins[0].data_ptr(), ins[1].data_ptr(), ins[2].data_ptr(), outs[0].data_ptr(),
+                                   outs[1].data_ptr(), w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k,
+                                   w.d_qk, w.d_v, int(w.causal), scale, splits, ws.data_ptr(), ws_bytes, stream)
             if rc != 0:
                 raise fa.FaError(rc, "fa_fwd_splitkv")
     else:
@@ -378,12 +428,15 @@ def run_ours(args):
             opts.workspace = ws.data_ptr()
         launches_per_step = 1
 
-        def step():
-            rc = fa.fa_fwd_ex(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), w.batch,
-                              w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale,
-                              opts, sp)
+        def launch(ins, outs, stream):
+            rc = fa.fa_fwd_ex(ins[0].data_ptr(), ins[1].data_ptr(), ins[2].data_ptr(), outs[0].data_ptr(),
+                              outs[1].data_ptr(), w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk,
+                              w.d_v, int(w.causal), scale, opts, stream)
             if rc != 0:
                 raise fa.FaError(rc, "fa_fwd")
+
+    def step():
+        launch(dev_inputs, [o, lse], sp)
 
     for _ in range(args.warmup):
         step()
@@ -418,27 +471,9 @@ def run_ours(args):
     value = world * flops / (ms_step * 1e-3) / 1e12
 
     # end to end: pinned host inputs -> device, forward, O and LSE back to host
-    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-
-    def e2e_step():
-        for d_, h_ in zip(dev_inputs, host_inputs):
-            d_.copy_(h_, non_blocking=True)
-        step()
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e2e_s = max_over_ranks(time.perf_counter() - t0, dev) / args.e2e_steps
+    e2e_s = e2e_pipelined(torch, dev, launch, host_inputs, dev_inputs, [o, lse], args.e2e_steps)
     h2d = sum(t.numel() * t.element_size() for t in host_inputs)
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
     hbm_bound = is_decode(args.config)  # K/V read once: bytes, not flops, bound it
     if hbm_bound:
@@ -529,12 +564,16 @@ def run_ours_bwd(args):
     sp = torch.cuda.current_stream(dev).cuda_stream
     scale = w.softmax_scale
 
-    def step():
-        rc = fa.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(), gd.data_ptr(),
-                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.batch, w.heads_q, w.heads_kv, w.seqlen_q,
-                       w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, sp)
+    def launch(ins, outs, stream):
+        q_, k_, v_, o_, l_, g_ = ins
+        rc = fa.fa_bwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), l_.data_ptr(), g_.data_ptr(),
+                       outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), w.batch, w.heads_q, w.heads_kv,
+                       w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, stream)
         if rc != 0:
             raise fa.FaError(rc, "fa_bwd")
+
+    def step():
+        launch([qd, kd, vd, o, lse, gd], [dq, dk, dv], sp)
 
     for _ in range(args.warmup):
         step()
@@ -569,27 +608,10 @@ def run_ours_bwd(args):
     value = world * flops / (ms_step * 1e-3) / 1e12
 
     # end to end: the backward's inputs in, the three gradients out
-    dqh, dkh, dvh = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv))
     host_in, dev_in = [qh, kh, vh, oh, lh, gh], [qd, kd, vd, o, lse, gd]
-
-    def e2e_step():
-        for d_, h_ in zip(dev_in, host_in):
-            d_.copy_(h_, non_blocking=True)
-        step()
-        for h_, d_ in zip((dqh, dkh, dvh), (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e2e_s = max_over_ranks(time.perf_counter() - t0, dev) / args.e2e_steps
+    e2e_s = e2e_pipelined(torch, dev, launch, host_in, dev_in, [dq, dk, dv], args.e2e_steps)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in (dqh, dkh, dvh))
+    d2h = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
     peak, peak_src = load_peak()
     achieved = flops / (ms_step * 1e-3) / 1e12
     cfg = config_of(w, world, flops, False)
