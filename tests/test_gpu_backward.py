@@ -103,3 +103,13 @@ def test_backward_degenerate(fa):
     dq, dk, dv = fa.attention_backward(q, k, k, o, lse, o)
     torch.cuda.synchronize()
     assert torch.all(dk == 0) and torch.all(dv == 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_mid_size_full(fa, causal):
+    """Every element of dQ, dK, dV at a size spanning many tiles and both
+    kernels' task orders (32 x 32 key x query blocks per head)."""
+    w = synthetic.Workload("bmid", 1, 4, 2, 4096, 4096, 128, 128, causal, seed=21 + int(causal))
+    inputs, grads = run(fa, w, 17)
+    check(w, inputs, grads, f"mid causal={causal}")
