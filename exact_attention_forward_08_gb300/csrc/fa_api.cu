@@ -169,14 +169,14 @@ int encode_q_like(CUtensorMap* m, const void* base, int B, int S, int H, int d, 
   return encode(m, base, 5, dims, strides, box);
 }
 
-// K or V viewed as (d, Hkv, S, B): one box is 128 keys x 64 columns of a head.
-int encode_kv(CUtensorMap* m, const void* base, int B, int S, int H, int d) {
+// K or V viewed as (d, Hkv, S, B): one box is box_rows keys x 64 columns of a head.
+int encode_kv(CUtensorMap* m, const void* base, int B, int S, int H, int d, int box_rows = fa::kBN) {
   const cuuint64_t e = 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {d * e, static_cast<cuuint64_t>(H) * d * e,
                            static_cast<cuuint64_t>(B > 1 ? S : 1) * H * d * e};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(fa::kBN), 1};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   return encode(m, base, 4, dims, strides, box);
 }
 
@@ -914,8 +914,10 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     const void* t1 = kv ? dout : v;
     const int hr = kv ? heads_kv : heads_q, sr = kv ? seqlen_k : seqlen_q;
     const int ht = kv ? heads_q : heads_kv, stt = kv ? seqlen_q : seqlen_k;
+    // streamed tiles travel as 64-row halves (one per stage)
     if (encode_kv(&p.tm_r0, r0, batch, sr, hr, d_qk) != FA_OK || encode_kv(&p.tm_r1, r1, batch, sr, hr, d_qk) != FA_OK ||
-        encode_kv(&p.tm_t0, t0, batch, stt, ht, d_qk) != FA_OK || encode_kv(&p.tm_t1, t1, batch, stt, ht, d_qk) != FA_OK)
+        encode_kv(&p.tm_t0, t0, batch, stt, ht, d_qk, 64) != FA_OK ||
+        encode_kv(&p.tm_t1, t1, batch, stt, ht, d_qk, 64) != FA_OK)
       return FA_ERR_CUDA;
     p.l2 = l2;
     p.dvec = dvec;

@@ -70,21 +70,29 @@ struct BwdParams {
   unsigned long long timeout_ns;
 };
 
+// Streamed tiles travel as half-tiles: rows 64s .. 64s+63 of a 128-row block
+// are what stage s reads, so each ring slot holds one stage's half of both
+// streamed tensors and is released as soon as that stage's GEMMs are done.
+// (With whole-block slots the ring only held two blocks at d = 128 and the
+// loader could not fetch far enough ahead to hide the L2 latency.)
 template <int D>
 struct BwdLayout {
   static_assert(D == 64 || D == 128, "backward head dims");
   static constexpr int NC = D / 64;
-  static constexpr int kTile = NC * kChunkBytes;  // one 128-row tile
-  static constexpr int kVec = 128 * 4;            // 128 fp32
-  static constexpr int kSlot = 2 * kTile + 2 * kVec;
+  static constexpr int kTile = NC * kChunkBytes;    // one resident 128-row tile
+  static constexpr int kHalfChunk = 64 * 128;       // 64 rows x 128 B
+  static constexpr int kHalf = NC * kHalfChunk;     // one streamed 64-row half-tile
+  static constexpr int kVecH = 64 * 4;              // 64 fp32
+  static constexpr int kSlot = 2 * kHalf;           // T0 half, T1 half (1024-aligned)
   static constexpr int kMaxSmem = 232448;
-  static constexpr int NSLOT_fit = (kMaxSmem - 2 * kTile - 2048 - 1024) / kSlot;
-  static constexpr int NSLOT = NSLOT_fit > 4 ? 4 : NSLOT_fit;
-  static_assert(NSLOT >= 2, "ring needs two slots");
+  static constexpr int NSLOT_fit = (kMaxSmem - 2 * kTile - 2048 - 1024) / (kSlot + 2 * kVecH);
+  static constexpr int NSLOT = NSLOT_fit > 8 ? 8 : NSLOT_fit;
+  static_assert(NSLOT >= 4, "ring needs two blocks");
   static constexpr int oR0 = 0;
   static constexpr int oR1 = kTile;
-  static constexpr int oRing = 2 * kTile;  // slot r: T0, T1, L2 vector, D vector
-  static constexpr int oBar = oRing + NSLOT * kSlot;
+  static constexpr int oRing = 2 * kTile;                   // slot r: T0 half, T1 half
+  static constexpr int oVec = oRing + NSLOT * kSlot;        // slot r: L2 vector (64), D vector (64)
+  static constexpr int oBar = oVec + NSLOT * 2 * kVecH;
   static constexpr int bResFull = 0;
   static constexpr int bResEmpty = 1;
   static constexpr int bTFull = 2;               // [NSLOT]
@@ -100,6 +108,7 @@ struct BwdLayout {
   static constexpr int kDynSmem = kBytes + 1024;
   static_assert(kDynSmem <= kMaxSmem, "shared memory budget");
   static __device__ __forceinline__ uint32_t slot_off(int r) { return oRing + r * kSlot; }
+  static __device__ __forceinline__ uint32_t vec_off(int r) { return oVec + r * 2 * kVecH; }
 };
 
 enum : unsigned int {
@@ -205,11 +214,24 @@ template <int D>
 __device__ __forceinline__ void issue_qk64(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t leader) {
   constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
-  for (int c = 0; c < D / 64; ++c) {
-    const uint32_t co = opaque_u32(static_cast<uint32_t>(c * kChunkBytes));
-    mma_ss_x4<2, 2>(d_tmem, smem_desc_sw128(a_addr + co, 16, 1024), smem_desc_sw128(b_addr + co, 16, 1024), kIdesc,
+  for (int c = 0; c < D / 64; ++c) {  // A: whole tile, 64-column chunks 16 KB apart; B: half-tile, 8 KB apart
+    const uint32_t ao = opaque_u32(static_cast<uint32_t>(c * kChunkBytes));
+    const uint32_t bo = opaque_u32(static_cast<uint32_t>(c * 64 * 128));
+    mma_ss_x4<2, 2>(d_tmem, smem_desc_sw128(a_addr + ao, 16, 1024), smem_desc_sw128(b_addr + bo, 16, 1024), kIdesc,
                     c != 0 ? 1u : 0u, leader);
   }
+}
+
+// Accumulating GEMM over one stage: D[128 x D] (+)= A[128 x 64] B[64 x D],
+// A in TMEM (32 columns of packed bf16 pairs), B a streamed half-tile read
+// MN-major (16 rows per step; its 64-column chunks 8 KB apart).
+template <int D>
+__device__ __forceinline__ void issue_pv64(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr, bool accumulate,
+                                           uint32_t leader) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, D, false, true);
+  constexpr uint32_t kStep = 16 * 128 >> 4;  // 16 rows, in 16-byte units
+  mma_ts_x4<kStep>(d_tmem, a_tmem, smem_desc_sw128(opaque_u32(b_addr), 64 * 128, 1024), kIdesc,
+                   accumulate ? 1u : 0u, leader);
 }
 
 // TMEM columns of stage s: S_s at 128 s, dP_s at 128 s + 64 (64 each);
@@ -251,7 +273,7 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
     }
     for (int it = 0; it < tk.nit; ++it, ++slot_it) {
       const BwdIter bi = bwd_iter<KIND>(p, tk, it);
-      const int slot = slot_it % L::NSLOT;
+      const int slot = (2 * slot_it + stage) % L::NSLOT;  // this stage's half of block it
       if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (L::bSFull + stage), s_phase, wc, kSiteBwdRowS))) return;
       s_phase ^= 1u;
       tc_fence_after();
@@ -266,8 +288,8 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
         cmax = min(63, p.Sk - 1 - bi.blk * kBN - cb);  // keys < Sk
         if (CAUSAL) cmax = min(cmax, row + (p.Sk - p.Sq) - bi.blk * kBN - cb);
       }
-      const float* l2v = reinterpret_cast<const float*>(smem + L::slot_off(slot) + 2 * L::kTile) + cb;
-      const float* dvv = l2v + 128;
+      const float* l2v = reinterpret_cast<const float*>(smem + L::vec_off(slot));
+      const float* dvv = l2v + 64;
 
       uint32_t r[64];
       tmem_ld64_wait(tS, r);
@@ -375,13 +397,15 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
   };
   uint32_t res_phase = 0, free_phase = 0, p_phase[2] = {0u, 0u};
-  int slot_it = 0;
+  int slot_it = 0;  // streamed blocks consumed; block i's stage-s half sits in slot (2 i + s) % NSLOT
   const int num_tasks = p.units * p.blocks;
   const uint32_t r0 = sbase + L::oR0, r1 = sbase + L::oR1;
-  constexpr uint32_t kHalfRows = 64 * 128;  // bytes of 64 tile rows inside a 64-column chunk
-  auto issue_sdp = [&](int s, uint32_t t0, uint32_t t1) {
-    issue_qk64<D>(tmem + bwd_s_col(s), r0, t0 + s * kHalfRows, leader);  // S_s  = R0 T0_s^T
-    issue_qk64<D>(tmem + bwd_p_col(s), r1, t1 + s * kHalfRows, leader);  // dP_s = R1 T1_s^T
+  auto half_slot = [&](int blk_it, int s) { return (2 * blk_it + s) % L::NSLOT; };
+  auto half_parity = [&](int blk_it, int s) { return static_cast<uint32_t>((2 * blk_it + s) / L::NSLOT) & 1u; };
+  auto issue_sdp = [&](int s, int slot) {
+    const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf;
+    issue_qk64<D>(tmem + bwd_s_col(s), r0, t0, leader);  // S_s  = R0 T0_s^T
+    issue_qk64<D>(tmem + bwd_p_col(s), r1, t1, leader);  // dP_s = R1 T1_s^T
     mma_commit(bar(L::bSFull + s), leader);
   };
 
@@ -395,44 +419,36 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
     }
     tc_fence_after();
     if (tk.nit > 0) {
-      const int slot = slot_it % L::NSLOT;
-      if (!wait(bar(L::bTFull + slot), static_cast<uint32_t>(slot_it / L::NSLOT) & 1u, kSiteBwdMmaT)) goto out;
-      tc_fence_after();
-      const uint32_t t0 = sbase + L::slot_off(slot);
-      issue_sdp(0, t0, t0 + L::kTile);
-      issue_sdp(1, t0, t0 + L::kTile);
-    }
-    for (int it = 0; it < tk.nit; ++it, ++slot_it) {
-      const int slot = slot_it % L::NSLOT;
-      const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kTile;
-      const int nslot = (slot_it + 1) % L::NSLOT;
-      const uint32_t n0 = sbase + L::slot_off(nslot), n1 = n0 + L::kTile;
-      bool next_ready = false;
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
+        if (!wait(bar(L::bTFull + half_slot(slot_it, s)), half_parity(slot_it, s), kSiteBwdMmaT)) goto out;
+        tc_fence_after();
+        issue_sdp(s, half_slot(slot_it, s));
+      }
+    }
+    for (int it = 0; it < tk.nit; ++it, ++slot_it) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int slot = half_slot(slot_it, s);
+        const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf;
         if (!wait(bar(L::bPReady + s), p_phase[s], kSiteBwdMmaP)) goto out;
         p_phase[s] ^= 1u;
         tc_fence_after();
         const bool acc = it > 0 || s > 0;
-        // A of stage s starts at its own S / dP columns (issue_pv_half adds 32 per half)
-        const uint32_t a_p = tmem + bwd_s_col(s) - 32u * s, a_ds = tmem + bwd_p_col(s) - 32u * s;
         if (KIND == kBwdDkDv) {
-          issue_pv_half<D>(tmem + 256u, a_p, t1, s, acc, leader);   // dV += P^T_s dO_s
-          issue_pv_half<D>(tmem + 384u, a_ds, t0, s, acc, leader);  // dK += dS^T_s Q_s
+          issue_pv64<D>(tmem + 256u, tmem + bwd_s_col(s), t1, acc, leader);  // dV += P^T_s dO_s
+          issue_pv64<D>(tmem + 384u, tmem + bwd_p_col(s), t0, acc, leader);  // dK += dS^T_s Q_s
         } else {
-          issue_pv_half<D>(tmem + 256u, a_p, t0, s, acc, leader);   // dQ += dS_s K_s
+          issue_pv64<D>(tmem + 256u, tmem + bwd_s_col(s), t0, acc, leader);  // dQ += dS_s K_s
         }
+        mma_commit(bar(L::bTEmpty + slot), leader);  // this half is no longer read
         if (it + 1 < tk.nit) {
-          if (!next_ready) {
-            if (!wait(bar(L::bTFull + nslot), static_cast<uint32_t>((slot_it + 1) / L::NSLOT) & 1u, kSiteBwdMmaT))
-              goto out;
-            tc_fence_after();
-            next_ready = true;
-          }
-          issue_sdp(s, n0, n1);
+          const int nslot = half_slot(slot_it + 1, s);
+          if (!wait(bar(L::bTFull + nslot), half_parity(slot_it + 1, s), kSiteBwdMmaT)) goto out;
+          tc_fence_after();
+          issue_sdp(s, nslot);
         }
       }
-      mma_commit(bar(L::bTEmpty + slot), leader);
     }
     if (tk.nit > 0) mma_commit(bar(L::bAccDone), leader);
     mma_commit(bar(L::bResEmpty), leader);
@@ -451,7 +467,7 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t res_uses = 0;
-  int slot_it = 0;
+  int half_it = 0;  // streamed half-tiles issued
   const int num_tasks = p.units * p.blocks;
   tma_prefetch_desc(&p.tm_r0);
   tma_prefetch_desc(&p.tm_r1);
@@ -467,31 +483,35 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
       tma_load_4d(sbase + L::oR1 + c * kChunkBytes, &p.tm_r1, bar(L::bResFull), c * 64, tk.h, tk.blk * kBM, tk.b);
     }
     ++res_uses;
-    for (int it = 0; it < tk.nit; ++it, ++slot_it) {
-      const int slot = slot_it % L::NSLOT;
-      if (slot_it >= L::NSLOT &&
-          !mbar_wait(bar(L::bTEmpty + slot), static_cast<uint32_t>(slot_it / L::NSLOT - 1) & 1u, wc,
-                     kSiteBwdLoadT))
-        goto out;
+    for (int it = 0; it < tk.nit; ++it) {
       const BwdIter bi = bwd_iter<KIND>(p, tk, it);
-      const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kTile;
-      const uint32_t fb = bar(L::bTFull + slot);
-      mbar_arrive_expect_tx(fb, 2u * L::kTile + (KIND == kBwdDkDv ? 2u * L::kVec : 0u));
-      for (int c = 0; c < L::NC; ++c) {
-        tma_load_4d(t0 + c * kChunkBytes, &p.tm_t0, fb, c * 64, bi.head, bi.blk * kBM, tk.b);
-        tma_load_4d(t1 + c * kChunkBytes, &p.tm_t1, fb, c * 64, bi.head, bi.blk * kBM, tk.b);
-      }
-      if (KIND == kBwdDkDv) {  // the block's LSE and D vectors (whole padded blocks: always in range)
-        const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + bi.head) * p.sq_pad + bi.blk * kBM;
-        bulk_load(t1 + L::kTile, p.l2 + vi, L::kVec, fb);
-        bulk_load(t1 + L::kTile + L::kVec, p.dvec + vi, L::kVec, fb);
+      for (int s = 0; s < 2; ++s, ++half_it) {  // stage s's half: rows 64s .. 64s+63 of the block
+        const int slot = half_it % L::NSLOT;
+        if (half_it >= L::NSLOT &&
+            !mbar_wait(bar(L::bTEmpty + slot), static_cast<uint32_t>(half_it / L::NSLOT - 1) & 1u, wc,
+                       kSiteBwdLoadT))
+          goto out;
+        const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf;
+        const uint32_t fb = bar(L::bTFull + slot);
+        const int row = bi.blk * kBM + 64 * s;
+        mbar_arrive_expect_tx(fb, 2u * L::kHalf + (KIND == kBwdDkDv ? 2u * L::kVecH : 0u));
+        for (int c = 0; c < L::NC; ++c) {
+          tma_load_4d(t0 + c * L::kHalfChunk, &p.tm_t0, fb, c * 64, bi.head, row, tk.b);
+          tma_load_4d(t1 + c * L::kHalfChunk, &p.tm_t1, fb, c * 64, bi.head, row, tk.b);
+        }
+        if (KIND == kBwdDkDv) {  // LSE and D of these 64 queries (whole padded blocks: always in range)
+          const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + bi.head) * p.sq_pad + row;
+          const uint32_t vdst = sbase + L::vec_off(slot);
+          bulk_load(vdst, p.l2 + vi, L::kVecH, fb);
+          bulk_load(vdst + L::kVecH, p.dvec + vi, L::kVecH, fb);
+        }
       }
     }
   }
 out:
   if (res_uses > 0) mbar_drain_wait(bar(L::bResFull), (res_uses - 1u) & 1u, wc, kSiteBwdLoadDrain);
-  for (int i = 0; i < L::NSLOT && i < slot_it; ++i) {
-    const uint32_t uses = static_cast<uint32_t>((slot_it - i + L::NSLOT - 1) / L::NSLOT);
+  for (int i = 0; i < L::NSLOT && i < half_it; ++i) {
+    const uint32_t uses = static_cast<uint32_t>((half_it - i + L::NSLOT - 1) / L::NSLOT);
     mbar_drain_wait(bar(L::bTFull + i), (uses - 1u) & 1u, wc, kSiteBwdLoadDrain);
   }
 }
