@@ -102,7 +102,8 @@ struct BwdLayout {
   static constexpr int bAccDone = bSFull + 4;
   static constexpr int bAccFree = bSFull + 5;     // count 256
   static constexpr int bDrain = bSFull + 6;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bAReady = bSFull + 7;     // dQ: Q and dO copied into TMEM (count 256)
+  static constexpr int kNumBars = bAReady + 1;
   static constexpr int oMisc = oBar + kNumBars * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int kBytes = oMisc + 16;
   static constexpr int kDynSmem = kBytes + 1024;
@@ -222,6 +223,19 @@ __device__ __forceinline__ void issue_qk64(uint32_t d_tmem, uint32_t a_addr, uin
   }
 }
 
+// The same with A in TMEM (the dQ kernel's Q or dO, D / 2 columns of packed
+// bf16 pairs): only B is read from SMEM.
+template <int D>
+__device__ __forceinline__ void issue_ts_qk64(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr, uint32_t leader) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint32_t bo = opaque_u32(static_cast<uint32_t>(c * 64 * 128));
+    mma_ts_x4<2>(d_tmem, a_tmem + static_cast<uint32_t>(32 * c), smem_desc_sw128(b_addr + bo, 16, 1024), kIdesc,
+                 c != 0 ? 1u : 0u, leader);
+  }
+}
+
 // Accumulating GEMM over one stage: D[128 x D] (+)= A[128 x 64] B[64 x D],
 // A in TMEM (32 columns of packed bf16 pairs), B a streamed half-tile read
 // MN-major (16 rows per step; its 64-column chunks 8 KB apart).
@@ -235,7 +249,10 @@ __device__ __forceinline__ void issue_pv64(uint32_t d_tmem, uint32_t a_tmem, uin
 }
 
 // TMEM columns of stage s: S_s at 128 s, dP_s at 128 s + 64 (64 each);
-// accumulators at 256 (dV or dQ) and 384 (dK).
+// accumulators at 256 (dV or dQ) and 384 (dK).  The dQ kernel keeps its
+// resident Q at 384 and dO at 448 (packed bf16 pairs) as the A operands of S
+// and dP, so those GEMMs read only the streamed half-tile from SMEM.
+constexpr uint32_t kBwdQCol = 384, kBwdOCol = 448;
 __device__ __forceinline__ uint32_t bwd_s_col(int s) { return static_cast<uint32_t>(128 * s); }
 __device__ __forceinline__ uint32_t bwd_p_col(int s) { return static_cast<uint32_t>(128 * s + 64); }
 
@@ -262,9 +279,33 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
   int slot_it = 0;
   const int num_tasks = p.units * p.blocks;
 
+  uint32_t res_phase = 0;
   for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
     const BwdTask tk = bwd_task<KIND>(p, task);
     const int row = tk.blk * kBM + t;  // key (dK/dV) or query (dQ)
+    if (KIND == kBwdDq) {
+      // stage s copies its resident tile (Q or dO, row t, 128-byte swizzled
+      // in SMEM) into TMEM as packed bf16 pairs.  The previous task's
+      // epilogue waited for all its MMAs, so these columns are free.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bResFull, res_phase, wc, kSiteBwdRowS))) return;
+      res_phase ^= 1u;
+      const uint8_t* tile = smem + (stage == 0 ? L::oR0 : L::oR1);
+      const uint32_t tA = tmem + lane_off + (stage == 0 ? kBwdQCol : kBwdOCol);
+#pragma unroll
+      for (int c = 0; c < L::NC; ++c) {
+        const uint4* src = reinterpret_cast<const uint4*>(tile + c * kChunkBytes + t * 128);
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = src[q ^ (t & 7)];
+          w[4 * q] = v.x, w[4 * q + 1] = v.y, w[4 * q + 2] = v.z, w[4 * q + 3] = v.w;
+        }
+        tmem_st32(tA + static_cast<uint32_t>(32 * c), w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar0 + 8u * L::bAReady);
+    }
     float l2_row = 0.f, d_row = 0.f;
     if (KIND == kBwdDq) {  // row < sq_pad: the block lies inside the padded rows
       const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + tk.h) * p.sq_pad + row;
@@ -396,7 +437,7 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
   auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
   };
-  uint32_t res_phase = 0, free_phase = 0, p_phase[2] = {0u, 0u};
+  uint32_t res_phase = 0, free_phase = 0, a_phase = 0, p_phase[2] = {0u, 0u};
   int slot_it = 0;  // streamed blocks consumed; block i's stage-s half sits in slot (2 i + s) % NSLOT
   const int num_tasks = p.units * p.blocks;
   const uint32_t r0 = sbase + L::oR0, r1 = sbase + L::oR1;
@@ -404,8 +445,13 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
   auto half_parity = [&](int blk_it, int s) { return static_cast<uint32_t>((2 * blk_it + s) / L::NSLOT) & 1u; };
   auto issue_sdp = [&](int s, int slot) {
     const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf;
-    issue_qk64<D>(tmem + bwd_s_col(s), r0, t0, leader);  // S_s  = R0 T0_s^T
-    issue_qk64<D>(tmem + bwd_p_col(s), r1, t1, leader);  // dP_s = R1 T1_s^T
+    if (KIND == kBwdDkDv) {
+      issue_qk64<D>(tmem + bwd_s_col(s), r0, t0, leader);  // S_s  = R0 T0_s^T  (K Q_s^T)
+      issue_qk64<D>(tmem + bwd_p_col(s), r1, t1, leader);  // dP_s = R1 T1_s^T  (V dO_s^T)
+    } else {
+      issue_ts_qk64<D>(tmem + bwd_s_col(s), tmem + kBwdQCol, t0, leader);  // S_s  = Q K_s^T
+      issue_ts_qk64<D>(tmem + bwd_p_col(s), tmem + kBwdOCol, t1, leader);  // dP_s = dO V_s^T
+    }
     mma_commit(bar(L::bSFull + s), leader);
   };
 
@@ -416,6 +462,10 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
     if (n > 0) {  // the previous task's epilogue has read the accumulators
       if (!wait(bar(L::bAccFree), free_phase, kSiteBwdMmaAcc)) goto out;
       free_phase ^= 1u;
+    }
+    if (KIND == kBwdDq) {  // Q and dO of this task are in TMEM
+      if (!wait(bar(L::bAReady), a_phase, kSiteBwdMmaRes)) goto out;
+      a_phase ^= 1u;
     }
     tc_fence_after();
     if (tk.nit > 0) {
@@ -547,6 +597,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     mbar_init(b + 8 * L::bAccDone, 1);
     mbar_init(b + 8 * L::bAccFree, 256);
     mbar_init(b + 8 * L::bDrain, 1);
+    mbar_init(b + 8 * L::bAReady, 256);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
