@@ -839,7 +839,8 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (opt.grid < 0 || !std::isfinite(opt.timeout_s) || opt.timeout_s > 3600.0) return FA_ERR_INVALID_ARG;
-  if (opt.debug_flags != 0 || opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1) return FA_ERR_UNSUPPORTED;
+  if ((opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
+  if (opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1) return FA_ERR_UNSUPPORTED;
   if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return FA_ERR_UNSUPPORTED;
   if (batch == 0) return FA_OK;
   const int64_t big = int64_t(1) << 31;
@@ -939,6 +940,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.timeout_ns = static_cast<unsigned long long>(opt.timeout_s * 1e9);
+    p.debug_flags = opt.debug_flags;
     const int64_t tasks = static_cast<int64_t>(p.units) * p.blocks;
     if (tasks >= big) return FA_ERR_INVALID_ARG;
     int64_t grid = opt.grid > 0 ? opt.grid : st->sms;

@@ -68,6 +68,7 @@ struct BwdParams {
   int section_units;         // causal order: units per L2 section
   float scale, scale_log2;
   unsigned long long timeout_ns;
+  int debug_flags;           // kDebugSkipPArrive: the row warps never signal p_ready (failure-path test)
 };
 
 // Streamed tiles travel as half-tiles: rows 64s .. 64s+63 of a 128-row block
@@ -367,7 +368,7 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar0 + 8u * (L::bPReady + stage));
+      if (!(p.debug_flags & kDebugSkipPArrive)) mbar_arrive(bar0 + 8u * (L::bPReady + stage));
     }
 
     // epilogue: dK/dV: stage 0 writes dV, stage 1 dK (scaled); dQ: stage s

@@ -186,9 +186,10 @@ int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, in
  *
  * Three launches on `stream`: the row preparation, the dK/dV kernel and the
  * dQ kernel; no atomics, so the result is deterministic.  seqlen_q == 0
- * writes dK = dV = 0; seqlen_k == 0 writes dQ = 0.  fa_options: grid and
- * timeout_s apply; tau, pack > 1, exp_emu, debug_flags and workspace do not
- * (FA_ERR_UNSUPPORTED when set).
+ * writes dK = dV = 0; seqlen_k == 0 writes dQ = 0.  fa_options: grid,
+ * timeout_s and debug_flags (bit 0: the row warps never signal P ready, so a
+ * bounded wait expires and fa_device_status reports FA_ERR_DEVICE_TIMEOUT)
+ * apply; pack > 1, exp_emu and workspace do not (FA_ERR_UNSUPPORTED when set).
  */
 size_t fa_bwd_workspace_size(int batch, int heads_q, int seqlen_q);
 

@@ -60,3 +60,36 @@ def test_bounded_wait_reports_timeout_and_context_survives(fa, causal):
     err = np.abs(o.float().cpu().numpy() - o_ref)
     assert err.max() <= 2e-2 and err.mean() <= 2e-3
     assert np.abs(lse.cpu().numpy() - lse_ref).max() <= 1e-3
+
+
+# backward wait sites behind the missing "P ready": the MMA warp waiting for P
+# (613), the TMA warp waiting for a half-tile slot (622) or resident tiles
+# (621), the row warps waiting for S (601) or the accumulators (602)
+BWD_STALLED_SITES = {601, 602, 613, 621, 622}
+
+
+def test_backward_bounded_wait_reports_timeout_and_context_survives(fa):
+    w = synthetic.Workload("bfault", 1, 4, 2, 300, 300, 128, 128, True, seed=78)
+    q, k, v = w.generate()
+    g = synthetic.normal_bf16(w.shapes["o"], 5, 7)
+    qd, kd, vd, gd = _dev(q), _dev(k), _dev(v), _dev(g)
+    o, lse = fa.attention_forward(qd, kd, vd, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == fa.FA_OK
+
+    opts = fa.default_options()
+    opts.debug_flags = 1      # the row warps never arrive on p_ready
+    opts.timeout_s = 0.2
+    fa.attention_backward(qd, kd, vd, o, lse, gd, causal=True, options=opts)
+    code, detail = fa.fa_device_status()
+    assert code == fa.FA_ERR_DEVICE_TIMEOUT
+    assert detail[0] == 4 and detail[1] in BWD_STALLED_SITES, detail
+    assert fa.fa_device_status()[0] == fa.FA_OK
+
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, gd, causal=True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == fa.FA_OK
+    ref = oracle.attn_bwd(q, k, v, g, causal=True)
+    for got, want in zip((dq, dk, dv), ref):
+        err = np.abs(got.float().cpu().numpy() - want)
+        assert err.max() <= 2e-2 * max(np.abs(want).max(), 1e-3)
