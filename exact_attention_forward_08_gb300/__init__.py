@@ -45,7 +45,7 @@ class FaError(RuntimeError):
 class FaOptions(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("pack", ctypes.c_int), ("grid", ctypes.c_int),
                 ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int), ("exp_emu", ctypes.c_int),
-                ("workspace", ctypes.c_void_p)]
+                ("workspace", ctypes.c_void_p), ("store_mode", ctypes.c_int)]
 
 
 # bytes of the optional fixed-length scheduling workspace (fa_options.workspace)

@@ -1,7 +1,7 @@
 // Kernel table: one entry per (d_qk, d_v, causal, mode) instantiation; the
 // modes are fixed-length, fixed-length with the FMA-pipe exp2, varlen (its
 // tasks always assigned dynamically), fixed-length with dynamic task
-// assignment, and split-KV.  Each head
+// assignment, split-KV, and fixed-length with the direct epilogue.  Each head
 // dimension lives in its own translation unit so the build compiles them in
 // parallel.
 #pragma once
@@ -39,6 +39,7 @@ KernelEntry pick_variant(int variant) {
     case kModeVarlen: return make_entry<DQ, DV, CAUSAL, kModeVarlen>();
     case kModeDyn: return make_entry<DQ, DV, CAUSAL, kModeDyn>();
     case kModeSplit: return make_entry<DQ, DV, CAUSAL, kModeSplit>();
+    case kModeDirect: return make_entry<DQ, DV, CAUSAL, kModeDirect>();
     default: return make_entry<DQ, DV, CAUSAL, kModeFixed>();
   }
 }

@@ -21,7 +21,11 @@
 // Modes (one instantiation each): fixed-length; fixed-length with the FMA-pipe
 // exp2; varlen (tasks from the planned list, always dynamic); fixed-length
 // with dynamic task assignment; split-KV (each task one key range, partial
-// O / LSE in fp32 to a workspace, combined afterwards by the merge kernel).
+// O / LSE in fp32 to a workspace, combined afterwards by the merge kernel);
+// fixed-length with a direct epilogue (each O row written from registers
+// with 16-byte stores instead of SMEM staging and TMA stores: faster when
+// tasks are short, since the correction warps then return sooner to the next
+// task; slower on long ones).
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DV),
 // O1 [384,384+DV).  P_s overwrites the first 64 columns of S_s as packed bf16
@@ -68,7 +72,15 @@ constexpr float kLn2 = 0.693147180559945309417f;
 constexpr int kTaskRing = 4;     // task indices the TMA thread may post ahead (DYN)
 
 // kernel modes
-enum : int { kModeFixed = 0, kModeEmu = 1, kModeVarlen = 2, kModeDyn = 3, kModeSplit = 4, kNumModes = 5 };
+enum : int {
+  kModeFixed = 0,
+  kModeEmu = 1,
+  kModeVarlen = 2,
+  kModeDyn = 3,
+  kModeSplit = 4,
+  kModeDirect = 5,  // fixed-length, O rows stored straight from registers (short tasks)
+  kNumModes = 6
+};
 constexpr int kTaskReaders = 13; // arrivals that free a ring slot: MMA warp + 12 softmax/correction warps
 
 // debug_flags bits
@@ -443,7 +455,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 // ---------------------------------------------------------------------------
 // correction + epilogue (WG2)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool DIRECT>
 __device__ __forceinline__ void correction_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                                 uint8_t* smem, float* mbox, const volatile int* ring,
                                                 const WaitCtx& wc) {
@@ -512,9 +524,10 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
       const int pos0 = tk.pos0[s];
       if (pos0 >= tk.sq) continue;  // tile past the end of the sequence
       const bool has = tk.n[s] > 0;
-      // a varlen tile that runs past its sequence is stored row by row: a TMA
-      // store would write the next sequence's rows
-      const bool direct = VARLEN && pos0 + pr.pos_per_tile > tk.sq;
+      // a varlen tile that runs past its sequence is stored row by row (a TMA
+      // store would write the next sequence's rows); so is every tile in the
+      // direct-epilogue mode
+      const bool direct = DIRECT || (VARLEN && pos0 + pr.pos_per_tile > tk.sq);
       const int pos = pos0 + t / pr.pack;
       const int head = tk.g * pr.pack + t % pr.pack;
       if (has) {  // o_done completes once per task: after the stage's last P V
@@ -559,7 +572,8 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
       }
       uint4* out_row = nullptr;
       if (direct && pos < tk.sq)
-        out_row = reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(tk.q_row0) + pos) * p.o_row_stride +
+        out_row = reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(tk.bc) * tk.sq + tk.q_row0 + pos) *
+                                                     p.o_row_stride +
                                            static_cast<int64_t>(head) * DV);
 #pragma unroll 1
       for (int c = 0; c < L::NVC; ++c) {
@@ -807,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   constexpr bool VARLEN = MODE == kModeVarlen;
   constexpr bool DYN = MODE == kModeVarlen || MODE == kModeDyn;
   constexpr bool SPLIT = MODE == kModeSplit;
+  constexpr bool DIRECT = MODE == kModeDirect;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -860,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN, SPLIT>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
-    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT>(p, tmem, sbase, smem, mbox, ring, wc);
+    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT>(p, tmem, sbase, smem, mbox, ring, wc);
   } else {
     setmaxnreg_dec<56>();
     if (warp == 12) {

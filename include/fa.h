@@ -107,6 +107,12 @@ typedef struct fa_options {
                          4 on Blackwell", "Scheduling").  Calls that may overlap on different
                          streams need different buffers.  Not combinable with exp_emu; must
                          be NULL for the varlen calls (they take their own workspace). */
+  int store_mode;     /* fixed-length epilogue: 0 (default) chooses by problem (O rows written
+                         straight from registers when a task sees at most 32 K/V blocks, else
+                         staged in SMEM and written by TMA); 1 forces the TMA store; 2 forces
+                         the direct stores.  Results are identical; only the speed differs.
+                         Other values are rejected.  Ignored by the varlen, split-KV, dynamic
+                         and exp_emu paths. */
 } fa_options;
 
 #define FA_SCHED_WORKSPACE_BYTES 16

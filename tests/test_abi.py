@@ -84,7 +84,7 @@ def test_bad_options_rejected(fa):
     assert abs(opts.tau - 8.0) < 1e-7 and opts.pack == 0 and opts.grid == 0
     for field, value in (("pack", 3), ("pack", -1), ("grid", -2), ("debug_flags", 2), ("timeout_s", 1e9), ("tau", 65.0),
                          ("tau", float("inf")), ("tau", float("nan")), ("exp_emu", 2),
-                         ("exp_emu", -1)):
+                         ("exp_emu", -1), ("store_mode", 3), ("store_mode", -1)):
         o = fa.default_options()
         setattr(o, field, value)
         rc = fa.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 64, 128, 128, 0, 0.0, o, None)

@@ -306,3 +306,22 @@ def test_dynamic_assignment_full_size_sampled(fa):
     og = o.float().cpu().numpy().astype(np.float64)[b, i, h]
     lg = lse.cpu().numpy().astype(np.float64)[b, h, i]
     compare(og, lg, o_ref, l_ref, "causal8k dynamic")
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_store_modes_bitwise_equal(fa, case):
+    """The epilogue writes O either staged through SMEM by TMA (store_mode 1)
+    or row by row from registers (2); the default picks by problem size.  The
+    arithmetic is the same, so the outputs must be bit-identical."""
+    name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, extra = case
+    w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, seed=zlib.crc32(name.encode()) % 1000, **extra)
+    q, k, v = (to_dev(a) for a in w.generate())
+    outs = []
+    for mode in (1, 2, 0):
+        opts = fa.default_options()
+        opts.store_mode = mode
+        outs.append(fa.attention_forward(q, k, v, causal=causal, scale=w.softmax_scale, options=opts))
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
