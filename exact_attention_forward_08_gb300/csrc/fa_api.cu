@@ -1024,6 +1024,7 @@ static fa::Problem problem_of(const fa_plan* pl) {
   p.tiles = pl->tiles, p.mblocks = pl->mblocks, p.kv_blocks = pl->kv_blocks, p.ratio = pl->ratio;
   p.section_units = pl->section_units, p.heavy_levels = pl->heavy_levels, p.num_tasks = pl->num_tasks;
   p.splits = 1, p.split_blocks = pl->kv_blocks;
+  fa::set_divisors(p);
   return p;
 }
 

@@ -188,7 +188,9 @@ __device__ __forceinline__ int task_count(const Params& p) {
   else return static_cast<int>(p.prob.num_tasks);
 }
 
-template <bool VARLEN, bool SPLIT = false>
+// FD: decode with the FastDiv fields (short-task kernels, where the decoding
+// sits on the path between tasks); otherwise plain division.
+template <bool VARLEN, bool SPLIT, bool CAUSAL, bool FD>
 __device__ __forceinline__ Task get_task(const Params& p, int t) {
   if constexpr (SPLIT) {
     return decode_split_task(p.prob, t);
@@ -200,7 +202,8 @@ __device__ __forceinline__ Task get_task(const Params& p, int t) {
     rec.q_row0 = b.x, rec.sq = b.y, rec.k_row0 = b.z, rec.sk = b.w;
     return task_from_record(p.prob, rec);
   } else {
-    return decode_task(p.prob, t);
+    if constexpr (FD) return decode_task_k<CAUSAL ? 1 : 0, true>(p.prob, t);
+    else return decode_task_k<-1, false>(p.prob, t);
   }
 }
 
@@ -301,7 +304,7 @@ __device__ __forceinline__ void ex2_fma_x2(uint64_t x2, float& y0, float& y1) {
 // ---------------------------------------------------------------------------
 // EMU: one in four exponentials of unmasked blocks on the FMA pipe (an option;
 // its own instantiation, so the default kernel carries no extra code)
-template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN, bool SPLIT>
+template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN, bool SPLIT, bool FD>
 __device__ __forceinline__ void softmax_role(const Params& p, const int stage, const uint32_t tmem,
                                              const uint32_t sbase, float* mbox, const volatile int* ring,
                                              const WaitCtx& wc) {
@@ -325,7 +328,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, sbase + L::oBar, ring, wc, kSiteSoftmaxTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD>(p, task);
     const int n = stage ? tk.n[1] : tk.n[0];
     if (n == 0) continue;
     const int pos0 = stage ? tk.pos0[1] : tk.pos0[0];
@@ -335,7 +338,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
     // the first block that needs the element mask
     int last_key = tk.kend - 1;
     if (CAUSAL) {
-      const int c = pos0 + t / pr.pack + tk.kshift;
+      const int c = pos0 + (FD ? fdiv(t, pr.fd_pack) : t / pr.pack) + tk.kshift;
       if (c < last_key) last_key = c;
     }
     if (last_key < -1) last_key = -1;
@@ -475,7 +478,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteCorrTask);
     if (task < 0) break;  // no task left, or an abort
-    Task tk = get_task<VARLEN, SPLIT>(p, task);
+    Task tk = get_task<VARLEN, SPLIT, CAUSAL, DIRECT>(p, task);
     float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
 
     for (int j = 0; j < tk.nmax; ++j) {
@@ -518,7 +521,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
     // epilogue: O / row_sum -> bf16 -> staging -> TMA store; LSE.  A varlen
     // task record is read again here rather than kept in registers across
     // the K/V loop (this role runs at 104 registers).
-    if constexpr (VARLEN) tk = get_task<VARLEN>(p, opaque_i32(task));
+    if constexpr (VARLEN) tk = get_task<VARLEN, false, CAUSAL, false>(p, opaque_i32(task));
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int pos0 = tk.pos0[s];
@@ -528,8 +531,9 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
       // store would write the next sequence's rows); so is every tile in the
       // direct-epilogue mode
       const bool direct = DIRECT || (VARLEN && pos0 + pr.pos_per_tile > tk.sq);
-      const int pos = pos0 + t / pr.pack;
-      const int head = tk.g * pr.pack + t % pr.pack;
+      const int row_pos = DIRECT ? fdiv(t, pr.fd_pack) : t / pr.pack;
+      const int pos = pos0 + row_pos;
+      const int head = tk.g * pr.pack + (t - row_pos * pr.pack);
       if (has) {  // o_done completes once per task: after the stage's last P V
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), od_count[s] & 1u, wc, kSiteCorrODone));
@@ -668,7 +672,7 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // o_done[s] is committed once per task, after the stage's last P V: inside a
 // task, "S_j ready" already implies that P V_{j-1} has completed (a commit
 // tracks every earlier MMA of the issuing thread).
-template <int DQ, int DV, bool VARLEN, bool DYN, bool SPLIT>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool FD>
 __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                          const volatile int* ring, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
@@ -693,7 +697,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteMmaTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD>(p, task);
     const uint32_t base = kv_it;
     kv_it += 2u * static_cast<uint32_t>(tk.nmax);
     if (tk.nmax == 0) continue;
@@ -752,7 +756,7 @@ out:
 // ---------------------------------------------------------------------------
 // TMA loads (warp 13, one thread)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool VARLEN, bool DYN, bool SPLIT>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool FD>
 __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase, volatile int* ring,
                                           const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
@@ -769,7 +773,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
   for (int kt = 0;; ++kt) {
     const int task = post_task<DQ, DV, DYN>(p, kt, num_tasks, bar0, ring, wc);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD>(p, task);
     if (tk.nmax == 0) continue;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -872,17 +876,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   // register budget: 128 x (176 + 176 + 104 + 56) = 65536
   if (warp < 8) {
     setmaxnreg_inc<176>();
-    softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN, SPLIT>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
+    softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN, SPLIT, DIRECT>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
     correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT>(p, tmem, sbase, smem, mbox, ring, wc);
   } else {
     setmaxnreg_dec<56>();
     if (warp == 12) {
-      mma_role<DQ, DV, VARLEN, DYN, SPLIT>(p, tmem, sbase, ring, wc);
+      mma_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT>(p, tmem, sbase, ring, wc);
       __syncwarp();
     } else if (warp == 13) {
-      if (lane == 0) load_role<DQ, DV, VARLEN, DYN, SPLIT>(p, sbase, ring, wc);
+      if (lane == 0) load_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT>(p, sbase, ring, wc);
       __syncwarp();
     }
   }

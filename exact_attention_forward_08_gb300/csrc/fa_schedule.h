@@ -53,6 +53,35 @@ namespace fa {
 constexpr int kBM = 128;  // rows of a Q tile (TMEM lanes)
 constexpr int kBN = 128;  // keys of a K/V block
 
+// Division by a divisor fixed when the problem is planned, as a multiply and
+// a shift (the round-up method of Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994): for 0 <= n < 2^31 and
+// 1 <= d <= 2^31, with L = ceil(log2 d) and m = ceil(2^(31+L) / d) (which is
+// below 2^32), floor(n / d) = floor(n * m / 2^(31+L)), because the error
+// n * (m d - 2^(31+L)) / (d 2^(31+L)) stays below 1/d.  A run-time integer
+// division compiles to a reciprocal on the SFU, the pipe the softmax keeps
+// busy with exponentials, so the kernel's task decoding uses these instead.
+struct FastDiv {
+  uint32_t m;
+  uint32_t shift;
+};
+
+FA_HD FastDiv make_fastdiv(int d) {
+  if (d < 1) d = 1;
+  uint32_t L = 0;
+  while ((uint64_t(1) << L) < static_cast<uint64_t>(d)) ++L;
+  const uint64_t num = uint64_t(1) << (31 + L);
+  FastDiv f;
+  f.m = static_cast<uint32_t>((num + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d));
+  f.shift = 31 + L;
+  return f;
+}
+
+// floor(n / d) for 0 <= n < 2^31
+FA_HD int fdiv(int n, FastDiv f) {
+  return static_cast<int>((static_cast<uint64_t>(static_cast<uint32_t>(n)) * f.m) >> f.shift);
+}
+
 struct Problem {
   int B, Hq, Hkv, Sq, Sk;
   int causal;
@@ -68,7 +97,29 @@ struct Problem {
   int splits;         // split-KV: key ranges per (b, g, m_block) (1 = no split)
   int split_blocks;   // split-KV: K/V blocks per range
   int64_t num_tasks;  // B * groups * mblocks * splits
+  // the divisors of the task decoding (set_divisors)
+  FastDiv fd_mblocks, fd_splits, fd_groups, fd_ratio, fd_pack;
+  FastDiv fd_units;    // B * groups
+  FastDiv fd_section;  // section_units * heavy_levels
+  FastDiv fd_su;       // section_units
+  FastDiv fd_last;     // units of the last causal section
 };
+
+// Fill the FastDiv fields from the integer fields; call after any change.
+FA_HD void set_divisors(Problem& p) {
+  const int units = p.B * p.groups;
+  p.fd_mblocks = make_fastdiv(p.mblocks);
+  p.fd_splits = make_fastdiv(p.splits);
+  p.fd_groups = make_fastdiv(p.groups);
+  p.fd_ratio = make_fastdiv(p.ratio);
+  p.fd_pack = make_fastdiv(p.pack);
+  p.fd_units = make_fastdiv(units);
+  p.fd_section = make_fastdiv(p.section_units * p.heavy_levels);
+  p.fd_su = make_fastdiv(p.section_units);
+  const int su = p.section_units > 0 ? p.section_units : 1;
+  const int last_first = units > 0 ? ((units - 1) / su) * su : 0;
+  p.fd_last = make_fastdiv(units - last_first);
+}
 
 struct Task {
   int b, g, mb;
@@ -127,6 +178,7 @@ FA_HD Problem make_problem(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int
   p.heavy_levels = (p.mblocks + 1) / 2;
   p.splits = 1;
   p.split_blocks = p.kv_blocks;
+  set_divisors(p);
   return p;
 }
 
@@ -138,6 +190,7 @@ FA_HD void set_splits(Problem& p, int splits) {
   p.split_blocks = p.kv_blocks > 0 ? ceil_div(p.kv_blocks, splits) : 0;
   p.splits = p.split_blocks > 0 ? ceil_div(p.kv_blocks, p.split_blocks) : 1;
   p.num_tasks = static_cast<int64_t>(p.B) * p.groups * p.mblocks * p.splits;
+  set_divisors(p);
 }
 
 // K/V blocks a Q tile starting at pos0 visits (sq queries, ppt positions per
@@ -159,46 +212,53 @@ FA_HD int tile_blocks(const Problem& p, int pos0) {
 }
 
 // Task t (0 <= t < num_tasks < 2^31; the host refuses larger problems).
-FA_HD Task decode_task(const Problem& p, int t) {
+// CAUSAL is the mask kind when the caller knows it at compile time (0 or 1),
+// or -1 to read p.causal.  FAST divides with the FastDiv fields; the result is
+// the same either way (FastDiv is exact in this range).
+template <int CAUSAL, bool FAST>
+FA_HD Task decode_task_k(const Problem& p, int t) {
+  const bool causal = CAUSAL < 0 ? p.causal != 0 : CAUSAL != 0;
   Task k;
   const int M = p.mblocks;
   int unit, mb;
-  if (!p.causal) {
-    unit = t / M;
+  if (!causal) {
+    unit = FAST ? fdiv(t, p.fd_mblocks) : t / M;
     mb = t - unit * M;
   } else {
     const int units = p.B * p.groups;
     const int Mh = p.heavy_levels;
     if (t < units * Mh) {  // heavier half: L2 sections, m_block decreasing inside each
       const int su = p.section_units;
-      const int section = t / (su * Mh);
+      const int section = FAST ? fdiv(t, p.fd_section) : t / (su * Mh);
       const int first_unit = section * su;
       int in_section = units - first_unit;
-      if (in_section > su) in_section = su;
+      if (in_section > su) in_section = su;  // below su only in the last section
       const int idx = t - section * su * Mh;
-      const int q = idx / in_section;
+      const int q = FAST ? fdiv(idx, in_section == su ? p.fd_su : p.fd_last) : idx / in_section;
       mb = M - 1 - q;
       unit = first_unit + (idx - q * in_section);
     } else {  // lighter half: one level (m_block) at a time over all units
       const int idx = t - units * Mh;
-      const int q = idx / units;
+      const int q = FAST ? fdiv(idx, p.fd_units) : idx / units;
       mb = M - 1 - Mh - q;
       unit = idx - q * units;
     }
   }
-  k.b = unit / p.groups;
+  k.b = FAST ? fdiv(unit, p.fd_groups) : unit / p.groups;
   k.g = unit - k.b * p.groups;
   k.mb = mb;
-  k.kvh = (k.g * p.pack) / p.ratio;
+  k.kvh = FAST ? fdiv(k.g * p.pack, p.fd_ratio) : (k.g * p.pack) / p.ratio;
   k.sq = p.Sq, k.kend = p.Sk, k.kshift = p.Sk - p.Sq, k.q_row0 = 0, k.k_row0 = 0, k.bc = k.b, k.split = 0;
   k.nmax = 0;
   for (int s = 0; s < 2; ++s) {
     k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
-    k.n[s] = tile_blocks(p, k.pos0[s]);
+    k.n[s] = tile_blocks_len(p.Sq, p.Sk, p.Sk - p.Sq, causal ? 1 : 0, p.pos_per_tile, k.pos0[s]);
     if (k.n[s] > k.nmax) k.nmax = k.n[s];
   }
   return k;
 }
+
+FA_HD Task decode_task(const Problem& p, int t) { return decode_task_k<-1, true>(p, t); }
 
 // Does K/V block j need the element mask for a tile starting at pos0?  (the
 // sequence tail, or the causal diagonal)
@@ -229,13 +289,13 @@ FA_HD int first_masked_block(int kend, int kshift, int causal, int pos0) {
 FA_HD Task decode_split_task(const Problem& p, int t) {
   Task k;
   const int M = p.mblocks;
-  const int unit_split = t / M;
+  const int unit_split = fdiv(t, p.fd_mblocks);
   k.mb = t - unit_split * M;
-  const int unit = unit_split / p.splits;
+  const int unit = fdiv(unit_split, p.fd_splits);
   k.split = unit_split - unit * p.splits;
-  k.b = unit / p.groups;
+  k.b = fdiv(unit, p.fd_groups);
   k.g = unit - k.b * p.groups;
-  k.kvh = (k.g * p.pack) / p.ratio;
+  k.kvh = fdiv(k.g * p.pack, p.fd_ratio);
   const int k0 = k.split * p.split_blocks * kBN;
   int k1 = k0 + p.split_blocks * kBN;
   if (k1 > p.Sk) k1 = p.Sk;
@@ -316,7 +376,7 @@ FA_HD VarlenTask varlen_record(const Problem& seq, int b, int q_row0, int k_row0
 FA_HD Task task_from_record(const Problem& p, const VarlenTask& r) {
   Task k;
   k.b = r.b, k.g = r.g, k.mb = r.mb;
-  k.kvh = (k.g * p.pack) / p.ratio;
+  k.kvh = fdiv(k.g * p.pack, p.fd_ratio);
   k.sq = r.sq, k.kend = r.sk, k.kshift = r.sk - r.sq, k.q_row0 = r.q_row0, k.k_row0 = r.k_row0, k.bc = 0;
   k.split = 0;
   k.nmax = 0;
