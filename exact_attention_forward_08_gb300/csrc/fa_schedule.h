@@ -373,10 +373,11 @@ FA_HD VarlenTask varlen_record(const Problem& seq, int b, int q_row0, int k_row0
 }
 
 // The task the kernel runs for a record.
+template <bool FAST = false>
 FA_HD Task task_from_record(const Problem& p, const VarlenTask& r) {
   Task k;
   k.b = r.b, k.g = r.g, k.mb = r.mb;
-  k.kvh = fdiv(k.g * p.pack, p.fd_ratio);
+  k.kvh = FAST ? fdiv(k.g * p.pack, p.fd_ratio) : (k.g * p.pack) / p.ratio;
   k.sq = r.sq, k.kend = r.sk, k.kshift = r.sk - r.sq, k.q_row0 = r.q_row0, k.k_row0 = r.k_row0, k.bc = 0;
   k.split = 0;
   k.nmax = 0;
