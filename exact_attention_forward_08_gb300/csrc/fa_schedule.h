@@ -311,26 +311,31 @@ FA_HD Task decode_split_task(const Problem& p, int t) {
 }
 
 // Split count for a problem whose (b, g, m_block) tasks may not fill `sms`
-// persistent CTAs: 1 when they do (or the keys are few); otherwise the
-// smallest count whose tasks fill the CTAs' last wave to at least 85 % of the
-// best count's fill, with at least 4 blocks (512 keys) per range.
+// persistent CTAs: 1 when they do (or the keys are few); otherwise the count
+// that minimises the modelled time waves * (blocks per range + kSplitTaskCost):
+// a range costs its K/V blocks plus a fixed start-up worth about five block
+// times (the first tiles' HBM latency, the pipeline fill, the partial-result
+// epilogue; fitted to GB300 timings of the decode workloads), at least 4
+// blocks (512 keys) per range, at most 128 ranges.  Returns a count that
+// leaves no range empty.
+constexpr int kSplitTaskCost = 5;
+
 FA_HD int choose_splits(const Problem& p, int sms) {
   const int64_t units = static_cast<int64_t>(p.B) * p.groups * p.mblocks;
   if (sms < 1 || units >= sms || p.kv_blocks < 8) return 1;
   int max_splits = p.kv_blocks / 4;
   if (max_splits > 128) max_splits = 128;
-  double best = 0.0;
-  double eff[129];
+  int best = 1;
+  int64_t best_cost = -1;
   for (int s = 1; s <= max_splits; ++s) {
     const int bps = ceil_div(p.kv_blocks, s);
-    const int64_t tasks = units * ceil_div(p.kv_blocks, bps);
+    const int ranges = ceil_div(p.kv_blocks, bps);
+    const int64_t tasks = units * ranges;
     const int64_t waves = (tasks + sms - 1) / sms;
-    eff[s] = static_cast<double>(tasks) / static_cast<double>(waves * sms);
-    if (eff[s] > best) best = eff[s];
+    const int64_t cost = waves * (bps + kSplitTaskCost);
+    if (best_cost < 0 || cost < best_cost) best_cost = cost, best = ranges;
   }
-  for (int s = 1; s <= max_splits; ++s)
-    if (eff[s] >= 0.85 * best) return s;
-  return 1;
+  return best;
 }
 
 // ---------------------------------------------------------------------------

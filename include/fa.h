@@ -166,9 +166,11 @@ size_t fa_splitkv_workspace_size(int batch, int heads_q, int seqlen_q, int d_v, 
 /*
  * The split count fa_fwd_splitkv uses for num_splits = 0 on a GPU with
  * num_sms SMs (host only): 1 when the unsplit tasks fill the SMs or the keys
- * are fewer than 8 blocks; otherwise the smallest count (at most 128, at least
- * 4 blocks per range) whose tasks fill the last wave of persistent CTAs to at
- * least 85 % of the best count's fill.  pack as in fa_options.
+ * are fewer than 8 blocks; otherwise the count (at most 128, at least 4
+ * blocks per range, none empty) that minimises waves x (blocks per range + 5):
+ * each range pays a start-up of about five block times besides its blocks
+ * (fitted to GB300 timings of decode workloads; the smallest such count on a
+ * tie).  pack as in fa_options.
  */
 int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v,
                           int causal, int pack, int num_sms);

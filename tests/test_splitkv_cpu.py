@@ -14,16 +14,20 @@ def fa():
     return m
 
 
-def fill(units, kvb, s, sms):
+TASK_COST = 5  # fixed start-up of a key range, in K/V block times
+
+
+def cost(units, kvb, s, sms):
+    """Modelled time of s ranges: waves of tasks times (blocks per range + start-up)."""
     bps = math.ceil(kvb / s)
     tasks = units * math.ceil(kvb / bps)
-    return tasks / (math.ceil(tasks / sms) * sms)
+    return math.ceil(tasks / sms) * (bps + TASK_COST)
 
 
 @pytest.mark.parametrize("shape", [
     # B, Hq, Hkv, Sq, Sk, causal
     (8, 32, 8, 1, 32768, 0), (32, 32, 1, 1, 16384, 0), (8, 32, 8, 4, 16384, 1), (1, 8, 8, 1, 4096, 0),
-    (2, 16, 2, 1, 100000, 0), (1, 1, 1, 1, 1024, 0), (3, 8, 2, 1, 1000, 0),
+    (2, 16, 2, 1, 100000, 0), (1, 1, 1, 1, 1024, 0), (3, 8, 2, 1, 1000, 0), (4, 32, 8, 1, 16384, 0),
 ])
 def test_heuristic(fa, shape):
     B, Hq, Hkv, Sq, Sk, causal = shape
@@ -37,14 +41,17 @@ def test_heuristic(fa, shape):
         return
     assert 1 <= s <= min(128, kvb // 4)
     assert math.ceil(kvb / math.ceil(kvb / s)) == s  # no empty range
-    best = max(fill(units, kvb, t, sms) for t in range(1, min(128, kvb // 4) + 1))
-    assert fill(units, kvb, s, sms) >= 0.85 * best
-    assert all(fill(units, kvb, t, sms) < 0.85 * best for t in range(1, s))
+    counts = range(1, min(128, kvb // 4) + 1)
+    best = min(cost(units, kvb, t, sms) for t in counts)
+    assert cost(units, kvb, s, sms) == best
+    assert all(cost(units, kvb, t, sms) > best for t in counts if math.ceil(kvb / math.ceil(kvb / t)) < s)
 
 
-def test_decode32k_choice(fa):
-    # 8 x 8 head groups = 64 tasks on 152 SMs: 7 ranges make 448 tasks, 98 % of 3 waves
-    assert fa.fa_splitkv_num_splits(8, 32, 8, 1, 32768, 128, 128, 0, 152) == 7
+def test_decode_choices(fa):
+    # measured best counts on GB300 (TFLOP/s and GB/s sweeps over 1..32 ranges)
+    assert fa.fa_splitkv_num_splits(8, 32, 8, 1, 32768, 128, 128, 0, 152) == 7   # decode32k: 448 tasks, 3 waves
+    assert fa.fa_splitkv_num_splits(32, 32, 1, 1, 16384, 128, 128, 0, 152) == 4  # MQA decode: one wave of 128
+    assert fa.fa_splitkv_num_splits(8, 32, 8, 4, 16384, 128, 128, 1, 152) == 2   # 4 draft tokens: one wave
     assert fa.fa_splitkv_num_splits(64, 32, 8, 1, 32768, 128, 128, 0, 152) == 1  # 512 tasks already
 
 
