@@ -325,3 +325,31 @@ def test_store_modes_bitwise_equal(fa, case):
     assert fa.fa_device_status()[0] == 0
     for o, lse in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+
+
+# with half of GB300's L2 as the section budget: 48 units in sections of 32,
+# 40 units in sections of 32, and an MQA problem of 7 units in one section
+@pytest.mark.parametrize("shape", [(3, 16, 16, 4096), (5, 32, 8, 4096), (7, 4, 1, 2000)],
+                         ids=["mha_48_units", "gqa_40_units", "mqa_7_units"])
+def test_partial_l2_section_store_modes_bitwise_equal(fa, shape):
+    """Causal problems whose (b, head group) units do not fill a whole number
+    of L2 sections: the direct-epilogue kernel decodes its tasks with the
+    multiply-and-shift divisions, the staged kernel with plain division; both
+    must visit every tile exactly once, so their outputs (written over NaN)
+    are bit-identical."""
+    B, Hq, Hkv, S = shape
+    w = synthetic.Workload("sections", B, Hq, Hkv, S, S, 128, 128, True, seed=B * 31 + Hq)
+    q, k, v = (to_dev(a) for a in w.generate())
+    outs = []
+    for mode in (1, 2):
+        opts = fa.default_options()
+        opts.store_mode = mode
+        o = torch.full((B, S, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((B, Hq, S), float("nan"), dtype=torch.float32, device="cuda")
+        fa.attention_forward(q, k, v, causal=True, scale=w.softmax_scale, out=o, lse=lse, options=opts)
+        outs.append((o, lse))
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    assert not torch.isnan(outs[0][0].float()).any() and not torch.isnan(outs[0][1]).any()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
