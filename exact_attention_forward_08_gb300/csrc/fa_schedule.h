@@ -154,10 +154,12 @@ FA_HD int choose_pack(int Hq, int Hkv) {
 }
 
 // Fill the derived fields.  `pack_override` > 0 forces a pack (must divide
-// both 128 and the ratio); l2_budget_bytes sizes the causal sections.
-FA_HD Problem make_problem(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int d_v, int causal,
-                           int64_t l2_budget_bytes, int pack_override) {
-  Problem p;
+// both 128 and the ratio); l2_budget_bytes sizes the causal sections.  The
+// FastDiv fields are left for make_problem (the varlen planner builds a
+// problem per task record and decodes with plain division).
+FA_HD Problem make_problem_core(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int d_v, int causal,
+                                int64_t l2_budget_bytes, int pack_override) {
+  Problem p{};  // FastDiv fields zero until set_divisors
   p.B = B, p.Hq = Hq, p.Hkv = Hkv, p.Sq = Sq, p.Sk = Sk, p.causal = causal;
   p.ratio = Hq / Hkv;
   p.pack = pack_override > 0 ? pack_override : choose_pack(Hq, Hkv);
@@ -178,6 +180,12 @@ FA_HD Problem make_problem(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int
   p.heavy_levels = (p.mblocks + 1) / 2;
   p.splits = 1;
   p.split_blocks = p.kv_blocks;
+  return p;
+}
+
+FA_HD Problem make_problem(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int d_v, int causal,
+                           int64_t l2_budget_bytes, int pack_override) {
+  Problem p = make_problem_core(B, Hq, Hkv, Sq, Sk, d_qk, d_v, causal, l2_budget_bytes, pack_override);
   set_divisors(p);
   return p;
 }
@@ -365,12 +373,12 @@ FA_HD int varlen_sort_index(uint64_t value) { return static_cast<int>(~static_ca
 // Tasks of one sequence: the fixed-length decomposition of a batch of one.
 FA_HD Problem varlen_sequence_problem(const Problem& base, int sq, int sk, int d_qk, int d_v,
                                       int64_t l2_budget_bytes) {
-  return make_problem(1, base.Hq, base.Hkv, sq, sk, d_qk, d_v, base.causal, l2_budget_bytes, base.pack);
+  return make_problem_core(1, base.Hq, base.Hkv, sq, sk, d_qk, d_v, base.causal, l2_budget_bytes, base.pack);
 }
 
 // Record of the i-th task of sequence b (rows q_row0.., k_row0.. of the packed views).
 FA_HD VarlenTask varlen_record(const Problem& seq, int b, int q_row0, int k_row0, int i) {
-  const Task t = decode_task(seq, i);
+  const Task t = decode_task_k<-1, false>(seq, i);
   VarlenTask r;
   r.b = b, r.g = t.g, r.mb = t.mb, r.reserved = 0;
   r.q_row0 = q_row0, r.sq = seq.Sq, r.k_row0 = k_row0, r.sk = seq.Sk;
