@@ -60,6 +60,10 @@ def parse_args(argv=None):
                          "forward's")
     ap.add_argument("--splitkv", type=int, default=0,
                     help="split-KV ranges for fixed-length workloads (decode workloads always split; 0 = auto there)")
+    ap.add_argument("--count-rescales", action="store_true",
+                    help="fixed-length forward: run the workload once with the O-rescale counter on and print the "
+                         "count, the most the launch could count (warps x K/V blocks after a tile's first) and their "
+                         "ratio, instead of timing")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -711,8 +715,42 @@ def run_reference_bwd(args, w, q, k, v):
     }
 
 
+def count_rescales(args) -> dict:
+    """One forward launch of a fixed-length workload with the correction warps'
+    O-rescale counter on (fa_options.debug_flags bit 1)."""
+    import numpy as np
+    import torch
+    import exact_attention_forward_08_gb300 as fa
+    w = get_workload(args.config)
+    if is_varlen(w) or is_decode(args.config):
+        raise SystemExit("--count-rescales takes a fixed-length --config")
+    fa.load_library()
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    q, k, v = (to_dev(a) for a in w.generate())
+    opts = fa.default_options()
+    opts.debug_flags = fa.DEBUG_COUNT_RESCALE
+    opts.exp_emu = 1  # the counter is compiled into the FMA-exp2 kernel only (same rescale decisions)
+    fa.fa_device_status()
+    fa.attention_forward(q, k, v, causal=w.causal, scale=w.softmax_scale, options=opts)
+    n = fa.fa_debug_rescale_count()
+    code = fa.fa_device_status()[0]
+    if code != 0:
+        raise SystemExit(f"device status {code}")
+    plan = fa.fa_make_plan(w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal))
+    total = 0
+    for t in range(plan.num_tasks):
+        task = fa.fa_plan_task(plan, t)
+        total += sum(4 * max(0, task.n_blocks[s] - 1) for s in range(2))
+    return {"config": args.config, "rescales": n, "opportunities": total,
+            "rate": (n / total) if total else 0.0,
+            "unit": "warps of 32 rows x K/V blocks after the first whose O was rescaled"}
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.count_rescales:
+        print(json.dumps(count_rescales(args)), flush=True)
+        return 0
     if args.impl == "reference":
         runner = run_reference
     else:

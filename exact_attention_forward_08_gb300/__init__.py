@@ -95,6 +95,8 @@ def load_library(path: str | None = None):
     lib.fa_options_default.restype = None
     lib.fa_device_status.argtypes = [_P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_uint)]
     lib.fa_device_status.restype = _I
+    lib.fa_debug_rescale_count.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_debug_rescale_count.restype = _I
     lib.fa_status_string.argtypes = [_I]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
@@ -176,6 +178,22 @@ def fa_device_status(stream=None):
     if rc != FA_OK:
         raise FaError(rc, "fa_device_status")
     return out.value, tuple(detail)
+
+
+# fa_options.debug_flags bits
+DEBUG_SKIP_P_ARRIVE = 1
+DEBUG_COUNT_RESCALE = 2
+
+
+def fa_debug_rescale_count(stream=None) -> int:
+    """Synchronise ``stream``, read and clear the count of O rescales (forward
+    calls made with ``debug_flags`` bit 1): one per warp of 32 rows and K/V
+    block whose correction warps rescaled O."""
+    out = ctypes.c_uint(0)
+    rc = load_library().fa_debug_rescale_count(stream, ctypes.byref(out))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_debug_rescale_count")
+    return int(out.value)
 
 
 def fa_selftest_exp2(x, y_fma, y_mufu, n, stream) -> int:

@@ -409,8 +409,11 @@ int validate_common(int heads_q, int heads_kv, int d_qk, int d_v, float scale, c
   if (heads_q % heads_kv != 0) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale)) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (kernel_index(d_qk, d_v, 0, 0) < 0) return FA_ERR_UNSUPPORTED;
-  if (opt.pack < 0 || opt.grid < 0 || (opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
+  if (opt.pack < 0 || opt.grid < 0 || (opt.debug_flags & ~(fa::kDebugSkipPArrive | fa::kDebugCountRescale)) != 0)
+    return FA_ERR_INVALID_ARG;
   if (opt.exp_emu != 0 && opt.exp_emu != 1) return FA_ERR_INVALID_ARG;
+  // the O-rescale counter is compiled into the FMA-exp2 kernels only
+  if ((opt.debug_flags & fa::kDebugCountRescale) != 0 && opt.exp_emu != 1) return FA_ERR_UNSUPPORTED;
   if (opt.store_mode < 0 || opt.store_mode > 2) return FA_ERR_INVALID_ARG;
   // the kept reference may lag the row maximum by up to tau (log2 units), so
   // unnormalised weights reach 2^tau: keep them far inside the fp32 range
@@ -983,6 +986,20 @@ int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]) {
     detail[1] = w[1];
     detail[2] = w[2];
   }
+  return FA_OK;
+}
+
+int fa_debug_rescale_count(fa_stream_t stream, unsigned int* out) {
+  if (out == nullptr) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* st = nullptr;
+  int rc = init_device(dev, &st);
+  if (rc != FA_OK) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpy(out, st->status + 3, sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemset(st->status + 3, 0, sizeof(unsigned int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 

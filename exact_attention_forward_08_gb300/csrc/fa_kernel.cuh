@@ -85,6 +85,7 @@ constexpr int kTaskReaders = 13; // arrivals that free a ring slot: MMA warp + 1
 
 // debug_flags bits
 constexpr int kDebugSkipPArrive = 1;  // softmax never arrives on p_full: exercises the bounded waits
+constexpr int kDebugCountRescale = 2; // count the correction warps' O round trips in status word 3
 
 struct Params {
   CUtensorMap tm_q;  // 5-D view (d, pack, groups, Sq, B) of q (varlen: S = total_q rows, B = 1)
@@ -458,7 +459,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 // ---------------------------------------------------------------------------
 // correction + epilogue (WG2)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool DIRECT>
+// COUNT: the FMA-exp2 ablation kernel also counts O rescales (debug_flags bit
+// 1); the rescale decisions do not depend on how the exponentials are taken,
+// and the default kernels carry no counting code.
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool DIRECT, bool COUNT>
 __device__ __forceinline__ void correction_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                                 uint8_t* smem, float* mbox, const volatile int* ring,
                                                 const WaitCtx& wc) {
@@ -494,6 +498,9 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         // reference.  The softmax posted acc_scale after S_j was ready, and S_j
         // ready implies that P V_{j-1} completed, so O is final here.
         if (j > 0 && __any_sync(0xffffffffu, acc != 1.f)) {
+          if constexpr (COUNT) {
+            if ((p.debug_flags & kDebugCountRescale) && (t & 31) == 0) atomicAdd(p.status + 3, 1u);
+          }
           tc_fence_after();
           const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(s * 128);
 #pragma unroll
@@ -888,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN, SPLIT, DIRECT>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
-    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT>(p, tmem, sbase, smem, mbox, ring, wc);
+    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT, EMU>(p, tmem, sbase, smem, mbox, ring, wc);
   } else {
     setmaxnreg_dec<56>();
     if (warp == 12) {

@@ -94,7 +94,14 @@ typedef struct fa_options {
   double timeout_s;   /* limit of every device-side wait; <= 0 selects 1 s */
   int debug_flags;    /* bit 0: the softmax warps never signal P ready, so the MMA warp's
                          bounded wait expires (tests the failure path; the output is not
-                         valid).  Other bits must be 0. */
+                         valid).  Bit 1 (forward calls): count, per warp of 32 rows and K/V
+                         block after the first, the correction warps' rescales of O (the
+                         TMEM round trip run when some row of the warp moved its reference
+                         by more than tau); read with fa_debug_rescale_count().  Needs
+                         exp_emu = 1 (the counter lives in that ablation kernel only, so the
+                         default kernels carry no counting code; the rescale decisions do not
+                         depend on how the exponentials are computed), else
+                         FA_ERR_UNSUPPORTED.  The output is unchanged.  Other bits must be 0. */
   int exp_emu;        /* 1: compute one in four exponentials of unmasked blocks on the FMA
                          pipe with a degree-3 polynomial instead of the MUFU ex2 unit
                          ("FlashAttention-4 wiki", "Core methods": partial exp emulation);
@@ -314,6 +321,13 @@ int fa_varlen_plan_host(const int* cu_seqlens_q, const int* cu_seqlens_k, int ba
  * {code, site, block or sequence index}.  Returns FA_OK or FA_ERR_CUDA.
  */
 int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's counter of
+ * O rescales (forward calls made with fa_options.debug_flags bit 1; the
+ * counter is also cleared by fa_device_status).  Returns FA_OK or FA_ERR_CUDA.
+ */
+int fa_debug_rescale_count(fa_stream_t stream, unsigned int* out);
 
 /* Human-readable name of a status code (static storage). */
 const char* fa_status_string(int status);

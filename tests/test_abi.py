@@ -82,8 +82,8 @@ def test_empty_problem_is_ok_without_launch(fa, kw):
 def test_bad_options_rejected(fa):
     opts = fa.default_options()
     assert abs(opts.tau - 8.0) < 1e-7 and opts.pack == 0 and opts.grid == 0
-    for field, value in (("pack", 3), ("pack", -1), ("grid", -2), ("debug_flags", 2), ("timeout_s", 1e9), ("tau", 65.0),
-                         ("tau", float("inf")), ("tau", float("nan")), ("exp_emu", 2),
+    for field, value in (("pack", 3), ("pack", -1), ("grid", -2), ("debug_flags", 4), ("debug_flags", 8),
+                         ("timeout_s", 1e9), ("tau", 65.0), ("tau", float("inf")), ("tau", float("nan")), ("exp_emu", 2),
                          ("exp_emu", -1), ("store_mode", 3), ("store_mode", -1)):
         o = fa.default_options()
         setattr(o, field, value)

@@ -353,3 +353,41 @@ def test_partial_l2_section_store_modes_bitwise_equal(fa, shape):
     assert not torch.isnan(outs[0][0].float()).any() and not torch.isnan(outs[0][1]).any()
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
+
+def rescale_opportunities(fa, w):
+    """Warps (32 rows) x K/V blocks after a tile's first: the most O rescales a
+    launch can count (from the host copy of the task list)."""
+    plan = fa.fa_make_plan(w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal))
+    total = 0
+    for t in range(plan.num_tasks):
+        task = fa.fa_plan_task(plan, t)
+        total += sum(4 * max(0, task.n_blocks[s] - 1) for s in range(2))
+    return total
+
+
+def test_rescale_counter(fa):
+    """debug_flags bit 1 (with the FMA-exp2 kernel, which carries the counter)
+    counts the correction warps' O rescales without changing the output: some
+    with Q x4 and keys whose scores rise along the sequence (the asymmetric
+    configuration's inputs), none with Q = 0 (uniform scores never move a
+    reference), none with the flag off; the default kernel refuses the flag."""
+    w = synthetic.Workload("rescale", 1, 4, 4, 700, 700, 192, 128, True, seed=73, q_mul=4.0, k_offset=12.0)
+    q, k, v = (to_dev(a) for a in w.generate())
+    fa.fa_device_status()
+    plain = fa.default_options()
+    plain.exp_emu = 1
+    o0, l0 = fa.attention_forward(q, k, v, causal=True, scale=w.softmax_scale, options=plain)
+    assert fa.fa_debug_rescale_count() == 0
+    opts = fa.default_options()
+    opts.debug_flags = fa.DEBUG_COUNT_RESCALE
+    with pytest.raises(fa.FaError):
+        fa.attention_forward(q, k, v, causal=True, scale=w.softmax_scale, options=opts)
+    opts.exp_emu = 1
+    o1, l1 = fa.attention_forward(q, k, v, causal=True, scale=w.softmax_scale, options=opts)
+    n = fa.fa_debug_rescale_count()
+    assert fa.fa_device_status()[0] == 0
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert 0 < n <= rescale_opportunities(fa, w)
+    fa.attention_forward(torch.zeros_like(q), k, v, causal=True, scale=w.softmax_scale, options=opts)
+    assert fa.fa_debug_rescale_count() == 0
+
