@@ -215,10 +215,6 @@ FA_HD int tile_blocks_len(int sq, int kend, int kshift, int causal, int ppt, int
   return n < kvb ? static_cast<int>(n) : kvb;
 }
 
-FA_HD int tile_blocks(const Problem& p, int pos0) {
-  return tile_blocks_len(p.Sq, p.Sk, p.Sk - p.Sq, p.causal, p.pos_per_tile, pos0);
-}
-
 // Task t (0 <= t < num_tasks < 2^31; the host refuses larger problems).
 // CAUSAL is the mask kind when the caller knows it at compile time (0 or 1),
 // or -1 to read p.causal.  FAST divides with the FastDiv fields; the result is
