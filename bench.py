@@ -277,7 +277,9 @@ def config_of(w, world: int, flops: float, dynamic: bool, splits: int = 1) -> di
               "flops_per_step_per_gpu": flops,
               "l2": "inputs larger than L2 (Q+K+V+O %.0f MiB per GPU), no flush" % (w.algorithmic_bytes() / 2 ** 20),
               "parallelism": f"weak x{world} (independent batches, no collective)",
-              "task_assignment": "dynamic (task counter)" if dynamic or is_varlen(w) else "static round-robin"}
+              "task_assignment": "dynamic (task counter)" if dynamic or is_varlen(w) else
+              ("static round-robin" if w.causal or splits > 1 else
+               "static round-robin; a partial last wave of at most half the CTAs runs as key-split tiles")}
     if splits > 1:
         common["split_kv"] = f"{splits} key ranges per task + merge kernel"
     if is_varlen(w):

@@ -11,7 +11,7 @@ library is missing or a call fails, an exception is raised.
 
 Raw entry points with the C names: ``fa_fwd``, ``fa_fwd_ex``, ``fa_fwd_varlen``,
 ``fa_fwd_varlen_ex``, ``fa_varlen_workspace_size``, ``fa_varlen_plan_host``,
-``fa_device_status``, ``fa_status_string``, ``fa_make_plan``, ``fa_plan_task``,
+``fa_device_status``, ``fa_status_string``, ``fa_make_plan``, ``fa_plan_task``, ``fa_plan_set_grid``,
 ``fa_plan_block_masked``, ``fa_plan_first_masked_block``, ``fa_version``.
 """
 from __future__ import annotations
@@ -26,7 +26,7 @@ __all__ = ["fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_varlen_ex", "fa_varle
            "fa_varlen_plan_host", "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_num_splits",
            "attention_forward_splitkv", "fa_bwd", "fa_bwd_workspace_size", "attention_backward",
            "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
-           "fa_plan_task", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
+           "fa_plan_task", "fa_plan_set_grid", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
            "FaTask", "FaVarlenTask", "attention_forward", "attention_forward_varlen", "FaError", "load_library",
            "LIB_PATH", "STATUS", "VARLEN_HEADER_BYTES"]
 
@@ -45,7 +45,7 @@ class FaError(RuntimeError):
 class FaOptions(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("pack", ctypes.c_int), ("grid", ctypes.c_int),
                 ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int), ("exp_emu", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("store_mode", ctypes.c_int)]
+                ("workspace", ctypes.c_void_p), ("store_mode", ctypes.c_int), ("no_tail_split", ctypes.c_int)]
 
 
 # bytes of the optional fixed-length scheduling workspace (fa_options.workspace)
@@ -55,12 +55,13 @@ SCHED_WORKSPACE_BYTES = 16
 class FaPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("batch", "heads_q", "heads_kv", "seqlen_q", "seqlen_k", "causal",
                                             "pack", "groups", "pos_per_tile", "tiles", "mblocks", "kv_blocks",
-                                            "ratio", "section_units", "heavy_levels")] + [("num_tasks", ctypes.c_int64)]
+                                            "ratio", "section_units", "heavy_levels")] + [("num_tasks", ctypes.c_int64),
+                                                                                          ("tail_first", ctypes.c_int64)]
 
 
 class FaTask(ctypes.Structure):
     _fields_ = [("b", ctypes.c_int), ("g", ctypes.c_int), ("mblock", ctypes.c_int), ("kv_head", ctypes.c_int),
-                ("pos0", ctypes.c_int * 2), ("n_blocks", ctypes.c_int * 2)]
+                ("pos0", ctypes.c_int * 2), ("n_blocks", ctypes.c_int * 2), ("key_split", ctypes.c_int)]
 
 
 class FaVarlenTask(ctypes.Structure):
@@ -105,6 +106,8 @@ def load_library(path: str | None = None):
     lib.fa_make_plan.restype = _I
     lib.fa_plan_task.argtypes = [ctypes.POINTER(FaPlan), ctypes.c_int64, ctypes.POINTER(FaTask)]
     lib.fa_plan_task.restype = _I
+    lib.fa_plan_set_grid.argtypes = [ctypes.POINTER(FaPlan), _I]
+    lib.fa_plan_set_grid.restype = _I
     lib.fa_plan_block_masked.argtypes = [ctypes.POINTER(FaPlan), _I, _I]
     lib.fa_plan_block_masked.restype = _I
     lib.fa_selftest_exp2.argtypes = [_P, _P, _P, _I, _P]
@@ -224,6 +227,14 @@ def fa_plan_task(plan: FaPlan, task: int) -> FaTask:
     if rc != FA_OK:
         raise FaError(rc, "fa_plan_task")
     return t
+
+
+def fa_plan_set_grid(plan: FaPlan, grid: int) -> FaPlan:
+    """Apply the balanced last wave the kernel runs on `grid` CTAs (in place)."""
+    rc = load_library().fa_plan_set_grid(ctypes.byref(plan), grid)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_plan_set_grid")
+    return plan
 
 
 def fa_plan_block_masked(plan: FaPlan, pos0: int, j: int) -> bool:

@@ -415,6 +415,7 @@ int validate_common(int heads_q, int heads_kv, int d_qk, int d_v, float scale, c
   // the O-rescale counter is compiled into the FMA-exp2 kernels only
   if ((opt.debug_flags & fa::kDebugCountRescale) != 0 && opt.exp_emu != 1) return FA_ERR_UNSUPPORTED;
   if (opt.store_mode < 0 || opt.store_mode > 2) return FA_ERR_INVALID_ARG;
+  if (opt.no_tail_split != 0 && opt.no_tail_split != 1) return FA_ERR_INVALID_ARG;
   // the kept reference may lag the row maximum by up to tau (log2 units), so
   // unnormalised weights reach 2^tau: keep them far inside the fp32 range
   if (!(opt.tau >= 0.f && opt.tau <= 64.f)) return FA_ERR_INVALID_ARG;
@@ -456,6 +457,7 @@ void fa_options_default(fa_options* opts) {
   opts->exp_emu = 0;
   opts->workspace = nullptr;
   opts->store_mode = 0;
+  opts->no_tail_split = 0;
 }
 
 int fa_version(void) { return 100; }
@@ -546,6 +548,11 @@ static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float
   if (idx < 0 || !get_entry(d_qk, d_v, causal, variant, &entry)) return FA_ERR_UNSUPPORTED;
   rc = prepare_kernel(st, idx, entry);
   if (rc != FA_OK) return rc;
+  const int64_t ctas = opt.grid > 0 ? opt.grid : st->sms;
+  // balanced last wave (static assignment, non-causal): the tiles of a
+  // partial last wave run as key halves on the two stages of a CTA
+  if ((variant == kVariantFixed || variant == kVariantDirect) && !opt.no_tail_split)
+    fa::set_tail_split(prob, ctas);
 
   fa::Params p;
   std::memset(&p, 0, sizeof(p));
@@ -566,7 +573,7 @@ static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float
   p.timeout_ns = static_cast<unsigned long long>(opt.timeout_s * 1e9);
   p.debug_flags = opt.debug_flags;
 
-  int64_t grid = opt.grid > 0 ? opt.grid : st->sms;
+  int64_t grid = ctas;
   if (grid > p.prob.num_tasks) grid = p.prob.num_tasks;
   if (grid < 1) return FA_OK;
   if (opt.workspace != nullptr) {  // dynamic assignment: the counter starts at 0 for this launch
@@ -1031,6 +1038,7 @@ int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_
   out->causal = p.causal, out->pack = p.pack, out->groups = p.groups, out->pos_per_tile = p.pos_per_tile;
   out->tiles = p.tiles, out->mblocks = p.mblocks, out->kv_blocks = p.kv_blocks, out->ratio = p.ratio;
   out->section_units = p.section_units, out->heavy_levels = p.heavy_levels, out->num_tasks = p.num_tasks;
+  out->tail_first = p.tail_first;
   return FA_OK;
 }
 
@@ -1040,9 +1048,19 @@ static fa::Problem problem_of(const fa_plan* pl) {
   p.causal = pl->causal, p.pack = pl->pack, p.groups = pl->groups, p.pos_per_tile = pl->pos_per_tile;
   p.tiles = pl->tiles, p.mblocks = pl->mblocks, p.kv_blocks = pl->kv_blocks, p.ratio = pl->ratio;
   p.section_units = pl->section_units, p.heavy_levels = pl->heavy_levels, p.num_tasks = pl->num_tasks;
+  p.tail_first = pl->tail_first;
   p.splits = 1, p.split_blocks = pl->kv_blocks;
   fa::set_divisors(p);
   return p;
+}
+
+int fa_plan_set_grid(fa_plan* plan, int grid) {
+  if (plan == nullptr || grid < 1 || plan->tail_first != plan->num_tasks) return FA_ERR_INVALID_ARG;
+  fa::Problem p = problem_of(plan);
+  fa::set_tail_split(p, grid);
+  plan->num_tasks = p.num_tasks;
+  plan->tail_first = p.tail_first;
+  return FA_OK;
 }
 
 int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out) {
@@ -1050,6 +1068,7 @@ int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out) {
   const fa::Task t = fa::decode_task(problem_of(plan), task);
   out->b = t.b, out->g = t.g, out->mblock = t.mb, out->kv_head = t.kvh;
   for (int s = 0; s < 2; ++s) out->pos0[s] = t.pos0[s], out->n_blocks[s] = t.n[s];
+  out->key_split = t.ksplit;
   return FA_OK;
 }
 

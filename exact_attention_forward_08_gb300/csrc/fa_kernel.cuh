@@ -203,8 +203,9 @@ __device__ __forceinline__ Task get_task(const Params& p, int t) {
     rec.q_row0 = b.x, rec.sq = b.y, rec.k_row0 = b.z, rec.sk = b.w;
     return task_from_record(p.prob, rec);
   } else {
-    if constexpr (FD) return decode_task_k<CAUSAL ? 1 : 0, true>(p.prob, t);
-    else return decode_task_k<-1, false>(p.prob, t);
+    // key-split tail tasks exist only without the causal mask
+    if constexpr (FD) return decode_task_k<CAUSAL ? 1 : 0, true, !CAUSAL>(p.prob, t);
+    else return decode_task_k<-1, false, !CAUSAL>(p.prob, t);
   }
 }
 
@@ -333,17 +334,20 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
     const int n = stage ? tk.n[1] : tk.n[0];
     if (n == 0) continue;
     const int pos0 = stage ? tk.pos0[1] : tk.pos0[0];
+    // keys of this stage counted from its first key: a key-split task's stage
+    // 1 starts at block ksplit (non-causal only; 0 otherwise)
+    const int kend = tk.kend - (CAUSAL ? 0 : stage * tk.ksplit * kBN);
     // last key visible to this row (inclusive, counted from the task's first
     // key; keys >= kend are never visible; pos + kshift stays inside 32 bits
     // for the sizes the host accepts; below -1 it means the same as -1), and
     // the first block that needs the element mask
-    int last_key = tk.kend - 1;
+    int last_key = kend - 1;
     if (CAUSAL) {
       const int c = pos0 + (FD ? fdiv(t, pr.fd_pack) : t / pr.pack) + tk.kshift;
       if (c < last_key) last_key = c;
     }
     if (last_key < -1) last_key = -1;
-    const int j_mask = first_masked_block(tk.kend, tk.kshift, CAUSAL, pos0);
+    const int j_mask = first_masked_block(kend, tk.kshift, CAUSAL, pos0);
     float row_max = -INFINITY;  // kept reference, raw score units
     float row_sum = 0.f;
     float ref = 0.f;            // row_max * scale_log2 (0 while the row is empty)
@@ -467,6 +471,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
                                                 uint8_t* smem, float* mbox, const volatile int* ring,
                                                 const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
+  constexpr bool TS = !CAUSAL && !VARLEN && !DYN && !SPLIT;  // key-split tail tasks possible
   const Problem& pr = p.prob;
   const int t = threadIdx.x - 256;  // row == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(t & ~31) << 16;
@@ -531,6 +536,9 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
     if constexpr (VARLEN) tk = get_task<VARLEN, false, CAUSAL, false>(p, opaque_i32(task));
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
+      // key-split tail task: one output tile, both halves merged at s = 0
+      const bool merge = TS && tk.ksplit != 0;
+      if (merge && s == 1) continue;
       const int pos0 = tk.pos0[s];
       if (pos0 >= tk.sq) continue;  // tile past the end of the sequence
       const bool has = tk.n[s] > 0;
@@ -550,7 +558,28 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         tc_fence_after();
       }
       float inv = 0.f, lse = -INFINITY;
-      if (has && fin_sum[s] > 0.f) {
+      float inv1 = 0.f;  // merge: weight of stage 1's O
+      if (merge) {
+        // the two key halves: reference m_s and row sum l_s each (log2
+        // units); with m = max m_s, l = sum 2^(m_s - m) l_s, and
+        // O = sum 2^(m_s - m) O_s / l, LSE = (m + log2 l) ln 2
+        const bool ok =
+            __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + 1), od_count[1] & 1u, wc, kSiteCorrODone));
+        if (!ok) goto out;
+        ++od_count[1];
+        tc_fence_after();
+        const float m0 = fin_sum[0] > 0.f ? fin_ref[0] : -INFINITY;
+        const float m1 = fin_sum[1] > 0.f ? fin_ref[1] : -INFINITY;
+        const float m = fmaxf(m0, m1);
+        if (m != -INFINITY) {
+          const float w0 = ex2_approx(m0 - m), w1 = ex2_approx(m1 - m);  // 2^-inf = 0
+          const float l = w0 * fin_sum[0] + w1 * fin_sum[1];
+          const float il = 1.f / l;
+          inv = w0 * il;
+          inv1 = w1 * il;
+          lse = (m + __log2f(l)) * kLn2;
+        }
+      } else if (has && fin_sum[s] > 0.f) {
         inv = 1.f / fin_sum[s];
         lse = (fin_ref[s] + __log2f(fin_sum[s])) * kLn2;
       }
@@ -598,8 +627,21 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t r[32];
+          float mul = inv;
           if (has) {
             tmem_ld32_wait(tO + static_cast<uint32_t>(c * 64 + half * 32), r);
+            if (merge) {  // r = inv * O_0 + inv1 * O_1 (O_1 is 128 columns on)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t r1[16];
+                tmem_ld16_wait(tO + static_cast<uint32_t>(128 + c * 64 + half * 32 + h * 16), r1);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  r[16 * h + i] = __float_as_uint(
+                      fmaf(__uint_as_float(r1[i]), inv1, __uint_as_float(r[16 * h + i]) * inv));
+              }
+              mul = 1.f;
+            }
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
@@ -607,10 +649,10 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+            v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * mul, __uint_as_float(r[8 * q + 1]) * mul);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * mul, __uint_as_float(r[8 * q + 3]) * mul);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * mul, __uint_as_float(r[8 * q + 5]) * mul);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * mul, __uint_as_float(r[8 * q + 7]) * mul);
             if (direct) {
               if (out_row != nullptr) out_row[c * 8 + half * 4 + q] = v;
             } else {
@@ -684,6 +726,7 @@ template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool F
 __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                          const volatile int* ring, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
+  constexpr bool TS = !CAUSAL && !VARLEN && !DYN && !SPLIT;  // key-split tail tasks possible
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   auto slot_addr = [&](uint32_t it) { return sbase + L::oRing + (it % L::NS) * L::kSlotBytes; };
@@ -707,6 +750,49 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteMmaTask);
     if (task < 0) break;  // no task left, or an abort
     const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD>(p, task);
+    if (TS && tk.ksplit != 0) {
+      // key-split tail task: both stages hold one Q tile and stream their own
+      // key halves.  Ring order: K_0 of stage 0 and of stage 1, then per
+      // block j and stage s: V_j, K_{j+1}.  Each tile is released right after
+      // the MMA that reads it.
+      uint32_t it = kv_it;
+      kv_it += 2u * static_cast<uint32_t>(tk.n[0] + tk.n[1]);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (!wait_tile(it)) goto out;
+        if (!wait(bar(L::bQFull + s), q_phase[s], kSiteMmaQ)) goto out;
+        q_phase[s] ^= 1u;
+        tc_fence_after();
+        issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(it), leader);
+        mma_commit(bar(L::bSFull + s), leader);
+        if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
+        release_tile(it++);
+      }
+      for (int j = 0; j < tk.n[0]; ++j) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (j >= tk.n[s]) continue;
+          if (!wait_tile(it)) goto out;
+          if (!wait(bar(L::bPFull + s), p_phase[s], kSiteMmaP)) goto out;
+          p_phase[s] ^= 1u;
+          tc_fence_after();
+          issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
+                            slot_addr(it), 0, j > 0, leader);
+          issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
+                            slot_addr(it), 1, true, leader);
+          if (j + 1 == tk.n[s]) mma_commit(bar(L::bODone + s), leader);
+          release_tile(it++);
+          if (j + 1 < tk.n[s]) {
+            if (!wait_tile(it)) goto out;
+            issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(it), leader);
+            mma_commit(bar(L::bSFull + s), leader);
+            if (j + 2 == tk.n[s]) mma_commit(bar(L::bQEmpty + s), leader);
+            release_tile(it++);
+          }
+        }
+      }
+      continue;
+    }
     const uint32_t base = kv_it;
     kv_it += 2u * static_cast<uint32_t>(tk.nmax);
     if (tk.nmax == 0) continue;
@@ -776,6 +862,7 @@ template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool F
 __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase, volatile int* ring,
                                           const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
+  constexpr bool TS = !CAUSAL && !VARLEN && !DYN && !SPLIT;  // key-split tail tasks possible
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t q_uses[2] = {0u, 0u};
@@ -801,6 +888,38 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
       for (int c = 0; c < L::NQC; ++c)
         tma_load_5d(dst + c * kChunkBytes, &p.tm_q, qb, c * 64, 0, tk.g, tk.q_row0 + tk.pos0[s], tk.bc);
       ++q_uses[s];
+    }
+    if constexpr (TS) {
+      if (tk.ksplit != 0) {  // key-split tail task: the order the MMA warp reads
+        // the next ring tile: K (which = 0) or V (1) of the block at key row `row`
+        auto issue_tile = [&](int which, int row) -> bool {
+          const uint32_t slot = kv_it % L::NS;
+          if (kv_it >= static_cast<uint32_t>(L::NS) &&
+              !mbar_wait(bar(L::bKvEmpty + static_cast<int>(slot)), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
+            return false;
+          const uint32_t fb = bar(L::bKvFull + static_cast<int>(slot));
+          const uint32_t dst = sbase + L::oRing + slot * L::kSlotBytes;
+          const int nch = which == 0 ? L::NQC : L::NVC;
+          mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nch * kChunkBytes));
+          for (int c = 0; c < nch; ++c)
+            tma_load_4d(dst + c * kChunkBytes, which == 0 ? static_cast<const void*>(&p.tm_k) : &p.tm_v, fb,
+                        c * 64, tk.kvh, row, tk.bc);
+          ++kv_it;
+          return true;
+        };
+        const int row1 = tk.k_row0 + tk.ksplit * kBN;  // stage 1's first key
+        if (!issue_tile(0, tk.k_row0) || !issue_tile(0, row1)) goto out;
+        for (int j = 0; j < tk.n[0]; ++j) {
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            if (j >= tk.n[s]) continue;
+            const int row = (s ? row1 : tk.k_row0) + j * kBN;
+            if (!issue_tile(1, row)) goto out;
+            if (j + 1 < tk.n[s] && !issue_tile(0, row + kBN)) goto out;
+          }
+        }
+        continue;
+      }
     }
     for (int j = 0; j < tk.nmax; ++j) {
 #pragma unroll

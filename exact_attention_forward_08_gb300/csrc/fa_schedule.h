@@ -27,6 +27,15 @@
 //    round-robin over "heaviest first per section" alone left the busiest CTA
 //    with 11-29 % more work than the average; this order halves that, and a
 //    dynamic assignment over it comes within about 1 %).
+//  * Balanced last wave (non-causal fixed-length problems): with P tasks on
+//    G persistent CTAs taken round-robin, the last r = P mod G tasks form a
+//    partial wave that keeps G - r CTAs idle while the others run a whole
+//    task.  When 2r <= G, each tile of those r tasks becomes a task of its
+//    own whose two stages hold the same Q tile and the two halves of the key
+//    blocks; the epilogue merges the two halves' (row max, row sum, O) with
+//    the exact rescaling of the online softmax ("Infra: Flash Attention",
+//    "Prefill and decode": independently computed key segments merge
+//    exactly).  The last wave then takes about half a task instead of one.
 //  * Split-KV (decode and other short-Q problems, where (b, g, m_block) tasks
 //    are too few to fill the GPU): each task also takes one of `splits`
 //    consecutive key ranges of split_blocks blocks ("Infra: Flash Attention",
@@ -96,7 +105,8 @@ struct Problem {
   int heavy_levels;   // causal task order: m_blocks M-1 .. M-heavy_levels go by sections
   int splits;         // split-KV: key ranges per (b, g, m_block) (1 = no split)
   int split_blocks;   // split-KV: K/V blocks per range
-  int64_t num_tasks;  // B * groups * mblocks * splits
+  int64_t num_tasks;  // B * groups * mblocks * splits (+ the key-split tail tasks)
+  int64_t tail_first; // first key-split tail task (= num_tasks when there are none)
   // the divisors of the task decoding (set_divisors)
   FastDiv fd_mblocks, fd_splits, fd_groups, fd_ratio, fd_pack;
   FastDiv fd_units;    // B * groups
@@ -137,6 +147,9 @@ struct Task {
   int k_row0;    // row of the task's first key in the K/V view
   int bc;        // batch coordinate in the TMA views (varlen: 0; else b)
   int split;     // split-KV range index (0 otherwise)
+  int ksplit;    // key-split tail task: both stages hold the tile at pos0[0]; stage 0
+                 // visits key blocks [0, ksplit), stage 1 [ksplit, ksplit + n[1]).
+                 // 0 for every other task.
 };
 
 // One task of a variable-length batch as the planning kernel writes it
@@ -169,6 +182,7 @@ FA_HD Problem make_problem_core(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk
   p.mblocks = ceil_div(p.tiles, 2);
   p.kv_blocks = ceil_div(Sk, kBN);
   p.num_tasks = static_cast<int64_t>(B) * p.groups * p.mblocks;
+  p.tail_first = p.num_tasks;
   // K/V bytes one (b, g) unit streams; units that share a KV head (pack = 1
   // with GQA) share those bytes in L2, which only makes the estimate safe.
   const int64_t kv_bytes = static_cast<int64_t>(Sk) * (d_qk + d_v) * 2;
@@ -198,7 +212,31 @@ FA_HD void set_splits(Problem& p, int splits) {
   p.split_blocks = p.kv_blocks > 0 ? ceil_div(p.kv_blocks, splits) : 0;
   p.splits = p.split_blocks > 0 ? ceil_div(p.kv_blocks, p.split_blocks) : 1;
   p.num_tasks = static_cast<int64_t>(p.B) * p.groups * p.mblocks * p.splits;
+  p.tail_first = p.num_tasks;
   set_divisors(p);
+}
+
+// Balanced last wave: a non-causal problem of P (b, g, m_block) tasks run by
+// `grid` CTAs round-robin (task t on CTA t mod grid) ends with a partial wave
+// of r = P mod grid tasks (r = P when P < grid).  When 0 < 2r <= grid, the
+// last r tasks are replaced by 2r key-split tasks, one per tile: task
+// tail_first + 2i + u runs tile u of pair task tail_first + i with the keys
+// halved over the two stages.  Needs at least kTailSplitMinBlocks K/V blocks
+// (both halves non-empty, and enough keys to pay for the merge).
+constexpr int kTailSplitMinBlocks = 4;
+
+FA_HD int tail_split_pairs(const Problem& p, int64_t grid) {
+  if (p.causal || p.splits != 1 || p.kv_blocks < kTailSplitMinBlocks || grid < 2) return 0;
+  const int64_t P = p.num_tasks;
+  const int64_t r = P >= grid ? P % grid : P;
+  return (r > 0 && 2 * r <= grid) ? static_cast<int>(r) : 0;
+}
+
+FA_HD void set_tail_split(Problem& p, int64_t grid) {
+  const int r = tail_split_pairs(p, grid);
+  if (r == 0) return;
+  p.tail_first = p.num_tasks - r;
+  p.num_tasks += r;
 }
 
 // K/V blocks a Q tile starting at pos0 visits (sq queries, ppt positions per
@@ -218,14 +256,22 @@ FA_HD int tile_blocks_len(int sq, int kend, int kshift, int causal, int ppt, int
 // Task t (0 <= t < num_tasks < 2^31; the host refuses larger problems).
 // CAUSAL is the mask kind when the caller knows it at compile time (0 or 1),
 // or -1 to read p.causal.  FAST divides with the FastDiv fields; the result is
-// the same either way (FastDiv is exact in this range).
-template <int CAUSAL, bool FAST>
+// the same either way (FastDiv is exact in this range).  TAIL decodes the
+// key-split tasks of a balanced last wave (callers that never see them, such
+// as the causal kernels, leave that code out).
+template <int CAUSAL, bool FAST, bool TAIL = true>
 FA_HD Task decode_task_k(const Problem& p, int t) {
   const bool causal = CAUSAL < 0 ? p.causal != 0 : CAUSAL != 0;
   Task k;
   const int M = p.mblocks;
   int unit, mb;
+  int tail_tile = -1;  // key-split tail task: the tile (0 or 1) of its pair task
   if (!causal) {
+    if (TAIL && t >= p.tail_first) {
+      const int u = t - static_cast<int>(p.tail_first);
+      tail_tile = u & 1;
+      t = static_cast<int>(p.tail_first) + (u >> 1);
+    }
     unit = FAST ? fdiv(t, p.fd_mblocks) : t / M;
     mb = t - unit * M;
   } else {
@@ -253,7 +299,19 @@ FA_HD Task decode_task_k(const Problem& p, int t) {
   k.mb = mb;
   k.kvh = FAST ? fdiv(k.g * p.pack, p.fd_ratio) : (k.g * p.pack) / p.ratio;
   k.sq = p.Sq, k.kend = p.Sk, k.kshift = p.Sk - p.Sq, k.q_row0 = 0, k.k_row0 = 0, k.bc = k.b, k.split = 0;
+  k.ksplit = 0;
   k.nmax = 0;
+  if (tail_tile >= 0) {  // one tile, its key blocks halved over the two stages
+    const int pos0 = (2 * k.mb + tail_tile) * p.pos_per_tile;
+    const int nb = tile_blocks_len(p.Sq, p.Sk, p.Sk - p.Sq, 0, p.pos_per_tile, pos0);
+    k.pos0[0] = k.pos0[1] = pos0;
+    k.n[0] = (nb + 1) / 2;
+    k.n[1] = nb - k.n[0];
+    k.nmax = k.n[0];
+    k.ksplit = k.n[1] > 0 ? k.n[0] : 0;
+    if (k.ksplit == 0) k.n[1] = 0;
+    return k;
+  }
   for (int s = 0; s < 2; ++s) {
     k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
     k.n[s] = tile_blocks_len(p.Sq, p.Sk, p.Sk - p.Sq, causal ? 1 : 0, p.pos_per_tile, k.pos0[s]);
@@ -305,6 +363,7 @@ FA_HD Task decode_split_task(const Problem& p, int t) {
   if (k1 > p.Sk) k1 = p.Sk;
   k.sq = p.Sq, k.kend = k1 - k0, k.kshift = p.Sk - p.Sq - k0;
   k.q_row0 = 0, k.k_row0 = k0, k.bc = k.b;
+  k.ksplit = 0;
   k.nmax = 0;
   for (int s = 0; s < 2; ++s) {
     k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;
@@ -374,7 +433,7 @@ FA_HD Problem varlen_sequence_problem(const Problem& base, int sq, int sk, int d
 
 // Record of the i-th task of sequence b (rows q_row0.., k_row0.. of the packed views).
 FA_HD VarlenTask varlen_record(const Problem& seq, int b, int q_row0, int k_row0, int i) {
-  const Task t = decode_task_k<-1, false>(seq, i);
+  const Task t = decode_task_k<-1, false, false>(seq, i);
   VarlenTask r;
   r.b = b, r.g = t.g, r.mb = t.mb, r.reserved = 0;
   r.q_row0 = q_row0, r.sq = seq.Sq, r.k_row0 = k_row0, r.sk = seq.Sk;
@@ -389,6 +448,7 @@ FA_HD Task task_from_record(const Problem& p, const VarlenTask& r) {
   k.kvh = FAST ? fdiv(k.g * p.pack, p.fd_ratio) : (k.g * p.pack) / p.ratio;
   k.sq = r.sq, k.kend = r.sk, k.kshift = r.sk - r.sq, k.q_row0 = r.q_row0, k.k_row0 = r.k_row0, k.bc = 0;
   k.split = 0;
+  k.ksplit = 0;
   k.nmax = 0;
   for (int s = 0; s < 2; ++s) {
     k.pos0[s] = (2 * k.mb + s) * p.pos_per_tile;

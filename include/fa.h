@@ -120,6 +120,15 @@ typedef struct fa_options {
                          the direct stores.  Results are identical; only the speed differs.
                          Other values are rejected.  Ignored by the varlen, split-KV, dynamic
                          and exp_emu paths. */
+  int no_tail_split;  /* non-causal fixed-length calls with static assignment: 0 (default)
+                         balances a partial last wave.  With P tasks on G CTAs (task t on CTA
+                         t mod G) and r = P mod G (P when P < G), if 0 < 2r <= G and there
+                         are at least 4 K/V blocks, the last r tasks are replaced by 2r tasks
+                         of one tile each whose two stages take the two halves of the key
+                         blocks; the epilogue merges the halves exactly (row max, row sum
+                         and O rescaled to the common maximum).  O and LSE agree with the
+                         unsplit result up to fp32 rounding.  1 keeps whole tasks.  Other
+                         values are rejected. */
 } fa_options;
 
 #define FA_SCHED_WORKSPACE_BYTES 16
@@ -357,18 +366,27 @@ typedef struct fa_plan {
   int heavy_levels;    /* causal order: the top heavy_levels m_blocks go section by section,
                           the rest level by level over all units */
   int64_t num_tasks;
+  int64_t tail_first;  /* first key-split task of a balanced last wave (= num_tasks: none) */
 } fa_plan;
 
 typedef struct fa_task {
   int b, g, mblock, kv_head;
   int pos0[2];         /* first sequence position of each stage's tile */
   int n_blocks[2];     /* K/V blocks each stage visits */
+  int key_split;       /* key-split task: both stages hold the tile at pos0[0]; stage 0 visits
+                          key blocks [0, key_split), stage 1 the next n_blocks[1]; else 0 */
 } fa_task;
 
 /* l2_bytes: L2 budget used to size causal sections (0 selects 64 MiB). */
 int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v,
                  int causal, int64_t l2_bytes, int pack, fa_plan* out);
 int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out);
+
+/* The balanced last wave fa_fwd runs on `grid` persistent CTAs (the SM count by
+   default; see fa_options.no_tail_split): updates num_tasks and tail_first of a
+   plan made by fa_make_plan (FA_ERR_INVALID_ARG if already applied or grid < 1).
+   Causal plans, and plans whose last wave gains nothing, are left unchanged. */
+int fa_plan_set_grid(fa_plan* plan, int grid);
 
 /* Does block j need the element mask for a tile starting at pos0? (host view) */
 int fa_plan_block_masked(const fa_plan* plan, int pos0, int j);

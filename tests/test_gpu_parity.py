@@ -270,14 +270,17 @@ DYN_CASES = ["ragged", "causal384", "causal_empty_rows", "gqa4", "ratio3", "d128
 @pytest.mark.parametrize("name", DYN_CASES)
 def test_dynamic_assignment_matches_static_bitwise(fa, name):
     """With a scheduling workspace the CTAs take tasks from a counter instead
-    of round-robin; every task computes the same tiles, so O and LSE must be
-    bit-identical.  The workspace is reused (the call clears the counter) and
-    small grids are covered."""
+    of round-robin; every task computes the same tiles (static assignment with
+    whole tasks, no key-split last wave), so O and LSE must be
+    bit-identical.  The workspace is reused (the call clears the counter)
+    and small grids are covered."""
     case = next(c for c in SMALL if c[0] == name)
     _, B, Hq, Hkv, Sq, Sk, dq, dv, causal, extra = case
     w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, seed=zlib.crc32(name.encode()) % 1000, **extra)
     q, k, v = (to_dev(a) for a in w.generate())
-    o_s, l_s = fa.attention_forward(q, k, v, causal=causal, scale=w.softmax_scale)
+    whole = fa.default_options()
+    whole.no_tail_split = 1  # dynamic assignment keeps whole tasks
+    o_s, l_s = fa.attention_forward(q, k, v, causal=causal, scale=w.softmax_scale, options=whole)
     ws = torch.full((fa.SCHED_WORKSPACE_BYTES,), 0x7F, dtype=torch.uint8, device="cuda")  # stale contents
     for grid in (0, 0, 3, 1):
         opts = fa.default_options()
@@ -391,3 +394,63 @@ def test_rescale_counter(fa):
     fa.attention_forward(torch.zeros_like(q), k, v, causal=True, scale=w.softmax_scale, options=opts)
     assert fa.fa_debug_rescale_count() == 0
 
+
+
+# Balanced last wave: non-causal problems whose last wave holds r <= grid / 2
+# tasks run each tile of those tasks as a key-split task (the two stages take
+# the two key halves of one Q tile; the epilogue merges them).  `grid` forces
+# sequences that mix whole tasks and split tasks on one CTA.
+TAIL_SPLIT = [
+    # name, B, Hq, Hkv, Sq, Sk, dq, dv, grid
+    ("ts_all_split", 1, 2, 2, 1024, 1024, 128, 128, 0),
+    ("ts_mixed_ragged", 1, 4, 4, 1000, 1000, 128, 128, 7),
+    ("ts_odd_tiles_blocks", 1, 3, 3, 384, 640, 128, 128, 5),
+    ("ts_gqa_pack4", 1, 8, 2, 512, 512, 128, 128, 3),
+    ("ts_d64", 2, 3, 3, 600, 900, 64, 64, 4),
+    ("ts_d192", 1, 4, 4, 512, 1024, 192, 128, 6),
+    ("ts_d192_64", 1, 2, 2, 700, 700, 192, 64, 0),
+    ("ts_2k_all_split", 1, 8, 8, 2048, 2048, 128, 128, 0),
+]
+
+
+@pytest.mark.parametrize("case", TAIL_SPLIT, ids=[c[0] for c in TAIL_SPLIT])
+def test_tail_split_parity(fa, case):
+    """Key-split tail tasks against the oracle (every element), with and
+    without the split; the two runs differ only by fp32 rounding of the
+    merge."""
+    name, B, Hq, Hkv, Sq, Sk, dq, dv, grid = case
+    plan = fa.fa_make_plan(B, Hq, Hkv, Sq, Sk, dq, dv, 0)
+    fa.fa_plan_set_grid(plan, grid if grid > 0 else torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan.tail_first < plan.num_tasks, "the case must exercise split tasks"
+    w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, dq, dv, False, seed=zlib.crc32(name.encode()) % 1000)
+    q, k, v = w.generate()
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal=False, scale=w.softmax_scale)
+    lr = lse_ref.transpose(0, 2, 1).reshape(-1)
+    outs = []
+    for off in (0, 1):
+        opts = fa.default_options()
+        opts.grid = grid
+        opts.no_tail_split = off
+        o, lse = run_gpu(fa, w, q, k, v, opts)
+        og = o.float().cpu().numpy().astype(np.float64).reshape(-1, dv)
+        lg = lse.cpu().numpy().astype(np.float64).transpose(0, 2, 1).reshape(-1)
+        compare(og, lg, o_ref.reshape(-1, dv), lr, f"{name} no_tail_split={off}")
+        outs.append((og, lg))
+    assert np.abs(outs[0][0] - outs[1][0]).max() <= 2e-2
+    assert np.abs(outs[0][1] - outs[1][1]).max() <= 1e-4
+
+
+def test_tail_split_store_modes_bitwise_equal(fa):
+    """The merged epilogue gives the same bits through the staged TMA store
+    and the direct row stores."""
+    w = synthetic.Workload("ts_modes", 1, 4, 4, 1000, 1000, 128, 128, False, seed=41)
+    q, k, v = (to_dev(a) for a in w.generate())
+    outs = []
+    for mode in (1, 2):
+        opts = fa.default_options()
+        opts.grid = 7
+        opts.store_mode = mode
+        outs.append(fa.attention_forward(q, k, v, causal=False, scale=w.softmax_scale, options=opts))
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
