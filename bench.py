@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-balance", action="store_true",
+                    help="ablation: the plain static task order (fa_options.no_balance = 1)")
     ap.add_argument("--dynamic", action="store_true",
                     help="fixed-length workloads: assign tasks dynamically (scheduling workspace)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
@@ -272,14 +274,30 @@ def oracle_sample(w, q, k, v, n, rng, threads):
     return time.perf_counter() - t0
 
 
-def config_of(w, world: int, flops: float, dynamic: bool, splits: int = 1) -> dict:
+def balance_of(w, sms: int) -> str:
+    """The balanced static order the library runs for this workload on `sms` CTAs
+    (from its host copy of the schedule)."""
+    import exact_attention_forward_08_gb300 as fa
+    plan = fa.fa_make_plan(w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal))
+    n = plan.num_tasks
+    fa.fa_plan_set_grid(plan, sms)
+    if plan.tail_first < plan.num_tasks:
+        r = plan.num_tasks - n
+        return f"a partial last wave of {r} tasks runs as {2 * r} key-split tiles"
+    if w.causal and plan.mblocks >= 2 and plan.mblocks % 2 == 0 and sms >= 2:
+        return "heavy and light m_blocks paired on one CTA"
+    return "plain order"
+
+
+def config_of(w, world: int, flops: float, dynamic: bool, splits: int = 1, balance: str = "") -> dict:
+    assign = "dynamic (task counter)" if dynamic or is_varlen(w) else "static round-robin"
+    if balance and not (dynamic or is_varlen(w) or splits > 1):
+        assign += "; " + balance
     common = {"heads_q": w.heads_q, "heads_kv": w.heads_kv, "d_qk": w.d_qk, "d_v": w.d_v, "causal": w.causal,
               "flops_per_step_per_gpu": flops,
               "l2": "inputs larger than L2 (Q+K+V+O %.0f MiB per GPU), no flush" % (w.algorithmic_bytes() / 2 ** 20),
               "parallelism": f"weak x{world} (independent batches, no collective)",
-              "task_assignment": "dynamic (task counter)" if dynamic or is_varlen(w) else
-              ("static round-robin" if w.causal or splits > 1 else
-               "static round-robin; a partial last wave of at most half the CTAs runs as key-split tiles")}
+              "task_assignment": assign}
     if splits > 1:
         common["split_kv"] = f"{splits} key ranges per task + merge kernel"
     if is_varlen(w):
@@ -432,6 +450,9 @@ def run_ours(args):
             ws = torch.zeros(fa.SCHED_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
             opts = fa.default_options()
             opts.workspace = ws.data_ptr()
+        if args.no_balance:
+            opts = opts or fa.default_options()
+            opts.no_balance = 1
         launches_per_step = 1
 
         def launch(ins, outs, stream):
@@ -493,7 +514,9 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, world, flops, args.dynamic, splits),
+        "config": config_of(w, world, flops, args.dynamic, splits,
+                            "plain order (ablation)" if args.no_balance else
+                            balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count)),
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
         "gpu_launches": args.steps * launches_per_step,
@@ -739,6 +762,8 @@ def count_rescales(args) -> dict:
     if code != 0:
         raise SystemExit(f"device status {code}")
     plan = fa.fa_make_plan(w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal))
+    # the order the launch ran (key-split tasks count each half's blocks after its first)
+    fa.fa_plan_set_grid(plan, torch.cuda.get_device_properties(0).multi_processor_count)
     total = 0
     for t in range(plan.num_tasks):
         task = fa.fa_plan_task(plan, t)

@@ -45,7 +45,7 @@ class FaError(RuntimeError):
 class FaOptions(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("pack", ctypes.c_int), ("grid", ctypes.c_int),
                 ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int), ("exp_emu", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("store_mode", ctypes.c_int), ("no_tail_split", ctypes.c_int)]
+                ("workspace", ctypes.c_void_p), ("store_mode", ctypes.c_int), ("no_balance", ctypes.c_int)]
 
 
 # bytes of the optional fixed-length scheduling workspace (fa_options.workspace)
@@ -56,7 +56,8 @@ class FaPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("batch", "heads_q", "heads_kv", "seqlen_q", "seqlen_k", "causal",
                                             "pack", "groups", "pos_per_tile", "tiles", "mblocks", "kv_blocks",
                                             "ratio", "section_units", "heavy_levels")] + [("num_tasks", ctypes.c_int64),
-                                                                                          ("tail_first", ctypes.c_int64)]
+                                                                                          ("tail_first", ctypes.c_int64),
+                                                                                          ("grid", ctypes.c_int)]
 
 
 class FaTask(ctypes.Structure):
@@ -230,7 +231,7 @@ def fa_plan_task(plan: FaPlan, task: int) -> FaTask:
 
 
 def fa_plan_set_grid(plan: FaPlan, grid: int) -> FaPlan:
-    """Apply the balanced last wave the kernel runs on `grid` CTAs (in place)."""
+    """Apply the balanced static order the kernel runs on `grid` CTAs (in place)."""
     rc = load_library().fa_plan_set_grid(ctypes.byref(plan), grid)
     if rc != FA_OK:
         raise FaError(rc, "fa_plan_set_grid")

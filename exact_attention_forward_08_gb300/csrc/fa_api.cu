@@ -415,7 +415,7 @@ int validate_common(int heads_q, int heads_kv, int d_qk, int d_v, float scale, c
   // the O-rescale counter is compiled into the FMA-exp2 kernels only
   if ((opt.debug_flags & fa::kDebugCountRescale) != 0 && opt.exp_emu != 1) return FA_ERR_UNSUPPORTED;
   if (opt.store_mode < 0 || opt.store_mode > 2) return FA_ERR_INVALID_ARG;
-  if (opt.no_tail_split != 0 && opt.no_tail_split != 1) return FA_ERR_INVALID_ARG;
+  if (opt.no_balance != 0 && opt.no_balance != 1) return FA_ERR_INVALID_ARG;
   // the kept reference may lag the row maximum by up to tau (log2 units), so
   // unnormalised weights reach 2^tau: keep them far inside the fp32 range
   if (!(opt.tau >= 0.f && opt.tau <= 64.f)) return FA_ERR_INVALID_ARG;
@@ -457,7 +457,7 @@ void fa_options_default(fa_options* opts) {
   opts->exp_emu = 0;
   opts->workspace = nullptr;
   opts->store_mode = 0;
-  opts->no_tail_split = 0;
+  opts->no_balance = 0;
 }
 
 int fa_version(void) { return 100; }
@@ -549,10 +549,11 @@ static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float
   rc = prepare_kernel(st, idx, entry);
   if (rc != FA_OK) return rc;
   const int64_t ctas = opt.grid > 0 ? opt.grid : st->sms;
-  // balanced last wave (static assignment, non-causal): the tiles of a
-  // partial last wave run as key halves on the two stages of a CTA
-  if ((variant == kVariantFixed || variant == kVariantDirect) && !opt.no_tail_split)
-    fa::set_tail_split(prob, ctas);
+  // balanced static order: without the mask the tiles of a partial last wave
+  // run as key halves on the two stages of a CTA; with it, heavy and light
+  // m_blocks are paired on one CTA
+  if ((variant == kVariantFixed || variant == kVariantDirect || variant == kVariantEmu) && !opt.no_balance)
+    fa::set_balance(prob, ctas);
 
   fa::Params p;
   std::memset(&p, 0, sizeof(p));
@@ -1039,6 +1040,7 @@ int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_
   out->tiles = p.tiles, out->mblocks = p.mblocks, out->kv_blocks = p.kv_blocks, out->ratio = p.ratio;
   out->section_units = p.section_units, out->heavy_levels = p.heavy_levels, out->num_tasks = p.num_tasks;
   out->tail_first = p.tail_first;
+  out->grid = 0;
   return FA_OK;
 }
 
@@ -1047,17 +1049,20 @@ static fa::Problem problem_of(const fa_plan* pl) {
   p.B = pl->batch, p.Hq = pl->heads_q, p.Hkv = pl->heads_kv, p.Sq = pl->seqlen_q, p.Sk = pl->seqlen_k;
   p.causal = pl->causal, p.pack = pl->pack, p.groups = pl->groups, p.pos_per_tile = pl->pos_per_tile;
   p.tiles = pl->tiles, p.mblocks = pl->mblocks, p.kv_blocks = pl->kv_blocks, p.ratio = pl->ratio;
-  p.section_units = pl->section_units, p.heavy_levels = pl->heavy_levels, p.num_tasks = pl->num_tasks;
-  p.tail_first = pl->tail_first;
+  p.section_units = pl->section_units, p.heavy_levels = pl->heavy_levels;
+  p.num_tasks = static_cast<int64_t>(pl->batch) * pl->groups * pl->mblocks;  // the plain order
+  p.tail_first = p.num_tasks;
+  p.pair_grid = p.pair_body = p.pair_r = p.pair_split_tail = 0;
   p.splits = 1, p.split_blocks = pl->kv_blocks;
   fa::set_divisors(p);
+  if (pl->grid > 0) fa::set_balance(p, pl->grid);
   return p;
 }
 
 int fa_plan_set_grid(fa_plan* plan, int grid) {
-  if (plan == nullptr || grid < 1 || plan->tail_first != plan->num_tasks) return FA_ERR_INVALID_ARG;
-  fa::Problem p = problem_of(plan);
-  fa::set_tail_split(p, grid);
+  if (plan == nullptr || grid < 1 || plan->grid != 0) return FA_ERR_INVALID_ARG;
+  plan->grid = grid;
+  const fa::Problem p = problem_of(plan);
   plan->num_tasks = p.num_tasks;
   plan->tail_first = p.tail_first;
   return FA_OK;

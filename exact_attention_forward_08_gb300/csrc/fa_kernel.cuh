@@ -190,8 +190,10 @@ __device__ __forceinline__ int task_count(const Params& p) {
 }
 
 // FD: decode with the FastDiv fields (short-task kernels, where the decoding
-// sits on the path between tasks); otherwise plain division.
-template <bool VARLEN, bool SPLIT, bool CAUSAL, bool FD>
+// sits on the path between tasks); otherwise plain division.  BAL: the
+// balanced static orders (key-split last wave without the mask, paired order
+// with it) may be in use; dynamically scheduled kernels leave them out.
+template <bool VARLEN, bool SPLIT, bool CAUSAL, bool FD, bool BAL>
 __device__ __forceinline__ Task get_task(const Params& p, int t) {
   if constexpr (SPLIT) {
     return decode_split_task(p.prob, t);
@@ -203,9 +205,9 @@ __device__ __forceinline__ Task get_task(const Params& p, int t) {
     rec.q_row0 = b.x, rec.sq = b.y, rec.k_row0 = b.z, rec.sk = b.w;
     return task_from_record(p.prob, rec);
   } else {
-    // key-split tail tasks exist only without the causal mask
-    if constexpr (FD) return decode_task_k<CAUSAL ? 1 : 0, true, !CAUSAL>(p.prob, t);
-    else return decode_task_k<-1, false, !CAUSAL>(p.prob, t);
+    if constexpr (FD) return decode_task_k<CAUSAL ? 1 : 0, true, BAL && !CAUSAL, BAL && CAUSAL>(p.prob, t);
+    else if constexpr (CAUSAL) return decode_task_k<1, false, false, BAL>(p.prob, t);
+    else return decode_task_k<-1, false, BAL, false>(p.prob, t);
   }
 }
 
@@ -330,7 +332,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, sbase + L::oBar, ring, wc, kSiteSoftmaxTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
     const int n = stage ? tk.n[1] : tk.n[0];
     if (n == 0) continue;
     const int pos0 = stage ? tk.pos0[1] : tk.pos0[0];
@@ -487,7 +489,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteCorrTask);
     if (task < 0) break;  // no task left, or an abort
-    Task tk = get_task<VARLEN, SPLIT, CAUSAL, DIRECT>(p, task);
+    Task tk = get_task<VARLEN, SPLIT, CAUSAL, DIRECT, !DYN>(p, task);
     float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
 
     for (int j = 0; j < tk.nmax; ++j) {
@@ -533,7 +535,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
     // epilogue: O / row_sum -> bf16 -> staging -> TMA store; LSE.  A varlen
     // task record is read again here rather than kept in registers across
     // the K/V loop (this role runs at 104 registers).
-    if constexpr (VARLEN) tk = get_task<VARLEN, false, CAUSAL, false>(p, opaque_i32(task));
+    if constexpr (VARLEN) tk = get_task<VARLEN, false, CAUSAL, false, false>(p, opaque_i32(task));
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       // key-split tail task: one output tile, both halves merged at s = 0
@@ -749,7 +751,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteMmaTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
     if (TS && tk.ksplit != 0) {
       // key-split tail task: both stages hold one Q tile and stream their own
       // key halves.  Ring order: K_0 of stage 0 and of stage 1, then per
@@ -876,7 +878,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
   for (int kt = 0;; ++kt) {
     const int task = post_task<DQ, DV, DYN>(p, kt, num_tasks, bar0, ring, wc);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD>(p, task);
+    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
     if (tk.nmax == 0) continue;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {

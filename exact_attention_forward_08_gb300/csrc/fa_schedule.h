@@ -36,6 +36,18 @@
 //    the exact rescaling of the online softmax ("Infra: Flash Attention",
 //    "Prefill and decode": independently computed key segments merge
 //    exactly).  The last wave then takes about half a task instead of one.
+//  * Paired causal order (static assignment): m_blocks m and M-1-m of a unit
+//    see (2m + 1.5) and (2M - 2m - 0.5) key blocks on average, a constant
+//    sum.  With M even, the list is laid out for G CTAs in blocks of 2G
+//    entries: G heavy tasks (pair i: the i-th task of the heavier half in
+//    the L2-section order above) followed by their G light complements, so
+//    that CTA c runs the heavy task of pair bG + c and then its complement;
+//    every CTA then gets the same work per two waves.  The r = P mod G pairs
+//    left over (P = units * M / 2) go last: each pair's two tasks to two
+//    CTAs when 2r <= G, else both to one CTA (the list then holds G - r
+//    empty entries).  A host simulation of per-CTA key blocks put the
+//    busiest CTA 6-13 % above the average with the plain order on the causal
+//    benchmark problems and 2-4 % with this one.
 //  * Split-KV (decode and other short-Q problems, where (b, g, m_block) tasks
 //    are too few to fill the GPU): each task also takes one of `splits`
 //    consecutive key ranges of split_blocks blocks ("Infra: Flash Attention",
@@ -107,12 +119,18 @@ struct Problem {
   int split_blocks;   // split-KV: K/V blocks per range
   int64_t num_tasks;  // B * groups * mblocks * splits (+ the key-split tail tasks)
   int64_t tail_first; // first key-split tail task (= num_tasks when there are none)
+  // paired causal order (set_pairing): 0 = the plain longest-first order
+  int pair_grid;       // CTAs the paired list is laid out for
+  int pair_body;       // entries of the whole blocks (2 * G * (P / G))
+  int pair_r;          // pairs left over (P mod G)
+  int pair_split_tail; // 1: each left-over pair's two tasks go to two CTAs
   // the divisors of the task decoding (set_divisors)
   FastDiv fd_mblocks, fd_splits, fd_groups, fd_ratio, fd_pack;
   FastDiv fd_units;    // B * groups
   FastDiv fd_section;  // section_units * heavy_levels
   FastDiv fd_su;       // section_units
   FastDiv fd_last;     // units of the last causal section
+  FastDiv fd_pair2g;   // 2 * pair_grid
 };
 
 // Fill the FastDiv fields from the integer fields; call after any change.
@@ -129,6 +147,7 @@ FA_HD void set_divisors(Problem& p) {
   const int su = p.section_units > 0 ? p.section_units : 1;
   const int last_first = units > 0 ? ((units - 1) / su) * su : 0;
   p.fd_last = make_fastdiv(units - last_first);
+  p.fd_pair2g = make_fastdiv(2 * (p.pair_grid > 0 ? p.pair_grid : 1));
 }
 
 struct Task {
@@ -239,6 +258,31 @@ FA_HD void set_tail_split(Problem& p, int64_t grid) {
   p.num_tasks += r;
 }
 
+// Paired causal order for `grid` CTAs taken round-robin (see the header
+// comment): needs an even m_block count and a list that stays below 2^31.
+FA_HD void set_pairing(Problem& p, int64_t grid) {
+  if (!p.causal || p.splits != 1 || p.mblocks < 2 || (p.mblocks & 1) || grid < 2 || p.pair_grid != 0) return;
+  const int64_t P = static_cast<int64_t>(p.B) * p.groups * (p.mblocks / 2);
+  const int64_t full = P / grid, r = P % grid;
+  const bool split_tail = 2 * r <= grid;
+  const int64_t n = 2 * full * grid + (r == 0 ? 0 : (split_tail ? 2 * r : grid + r));
+  if (n >= (int64_t(1) << 31)) return;
+  p.pair_grid = static_cast<int>(grid);
+  p.pair_body = static_cast<int>(2 * full * grid);
+  p.pair_r = static_cast<int>(r);
+  p.pair_split_tail = split_tail ? 1 : 0;
+  p.num_tasks = n;
+  p.tail_first = n;
+  set_divisors(p);
+}
+
+// The balanced static order for `grid` CTAs: the key-split last wave without
+// the causal mask, the paired order with it.
+FA_HD void set_balance(Problem& p, int64_t grid) {
+  if (p.causal) set_pairing(p, grid);
+  else set_tail_split(p, grid);
+}
+
 // K/V blocks a Q tile starting at pos0 visits (sq queries, ppt positions per
 // tile; kend / kshift as in Task).
 FA_HD int tile_blocks_len(int sq, int kend, int kshift, int causal, int ppt, int pos0) {
@@ -257,9 +301,10 @@ FA_HD int tile_blocks_len(int sq, int kend, int kshift, int causal, int ppt, int
 // CAUSAL is the mask kind when the caller knows it at compile time (0 or 1),
 // or -1 to read p.causal.  FAST divides with the FastDiv fields; the result is
 // the same either way (FastDiv is exact in this range).  TAIL decodes the
-// key-split tasks of a balanced last wave (callers that never see them, such
-// as the causal kernels, leave that code out).
-template <int CAUSAL, bool FAST, bool TAIL = true>
+// key-split last wave (no mask), PAIR the paired order (causal mask); callers
+// that never see them, such as the dynamically scheduled kernels, leave that
+// code out.
+template <int CAUSAL, bool FAST, bool TAIL = true, bool PAIR = true>
 FA_HD Task decode_task_k(const Problem& p, int t) {
   const bool causal = CAUSAL < 0 ? p.causal != 0 : CAUSAL != 0;
   Task k;
@@ -275,6 +320,30 @@ FA_HD Task decode_task_k(const Problem& p, int t) {
     unit = FAST ? fdiv(t, p.fd_mblocks) : t / M;
     mb = t - unit * M;
   } else {
+    bool light = false;  // paired order: the light complement of pair t
+    if (PAIR && p.pair_grid > 0) {
+      const int G = p.pair_grid;
+      if (t < p.pair_body) {  // blocks of G heavy tasks and their G complements
+        const int blk = FAST ? fdiv(t, p.fd_pair2g) : t / (2 * G);
+        const int w = t - blk * 2 * G;
+        light = w >= G;
+        t = blk * G + (light ? w - G : w);
+      } else {  // the pairs left over
+        const int tt = t - p.pair_body;
+        const int half = p.pair_split_tail ? p.pair_r : G;
+        light = tt >= half;
+        const int pos = light ? tt - half : tt;
+        if (pos >= p.pair_r) {  // an empty entry: no rows, no keys
+          k.b = 0, k.g = 0, k.mb = 0, k.kvh = 0;
+          k.sq = p.Sq, k.kend = p.Sk, k.kshift = p.Sk - p.Sq, k.q_row0 = 0, k.k_row0 = 0, k.bc = 0;
+          k.split = 0, k.ksplit = 0, k.nmax = 0;
+          k.pos0[0] = k.pos0[1] = p.Sq;
+          k.n[0] = k.n[1] = 0;
+          return k;
+        }
+        t = p.pair_body / 2 + pos;
+      }
+    }
     const int units = p.B * p.groups;
     const int Mh = p.heavy_levels;
     if (t < units * Mh) {  // heavier half: L2 sections, m_block decreasing inside each
@@ -293,6 +362,7 @@ FA_HD Task decode_task_k(const Problem& p, int t) {
       mb = M - 1 - Mh - q;
       unit = idx - q * units;
     }
+    if (light) mb = M - 1 - mb;
   }
   k.b = FAST ? fdiv(unit, p.fd_groups) : unit / p.groups;
   k.g = unit - k.b * p.groups;
@@ -433,7 +503,7 @@ FA_HD Problem varlen_sequence_problem(const Problem& base, int sq, int sk, int d
 
 // Record of the i-th task of sequence b (rows q_row0.., k_row0.. of the packed views).
 FA_HD VarlenTask varlen_record(const Problem& seq, int b, int q_row0, int k_row0, int i) {
-  const Task t = decode_task_k<-1, false, false>(seq, i);
+  const Task t = decode_task_k<-1, false, false, false>(seq, i);
   VarlenTask r;
   r.b = b, r.g = t.g, r.mb = t.mb, r.reserved = 0;
   r.q_row0 = q_row0, r.sq = seq.Sq, r.k_row0 = k_row0, r.sk = seq.Sk;

@@ -120,15 +120,18 @@ typedef struct fa_options {
                          the direct stores.  Results are identical; only the speed differs.
                          Other values are rejected.  Ignored by the varlen, split-KV, dynamic
                          and exp_emu paths. */
-  int no_tail_split;  /* non-causal fixed-length calls with static assignment: 0 (default)
-                         balances a partial last wave.  With P tasks on G CTAs (task t on CTA
-                         t mod G) and r = P mod G (P when P < G), if 0 < 2r <= G and there
-                         are at least 4 K/V blocks, the last r tasks are replaced by 2r tasks
-                         of one tile each whose two stages take the two halves of the key
-                         blocks; the epilogue merges the halves exactly (row max, row sum
-                         and O rescaled to the common maximum).  O and LSE agree with the
-                         unsplit result up to fp32 rounding.  1 keeps whole tasks.  Other
-                         values are rejected. */
+  int no_balance;     /* fixed-length calls with static assignment: 0 (default) balances the
+                         work of the G persistent CTAs (task t on CTA t mod G).  Without the
+                         causal mask: with P tasks and r = P mod G (P when P < G), if
+                         0 < 2r <= G and there are at least 4 K/V blocks, the last r tasks
+                         are replaced by 2r tasks of one tile each whose two stages take the
+                         two halves of the key blocks, merged exactly in the epilogue (row
+                         max, row sum and O rescaled to the common maximum); O and LSE agree
+                         with the unsplit result up to fp32 rounding.  With the causal mask
+                         and an even number of m_blocks: heavy and light m_blocks (m and
+                         M-1-m, a constant total of key blocks) are paired on one CTA in
+                         consecutive waves; the output is bit-identical.  1 keeps the plain
+                         order and whole tasks.  Other values are rejected. */
 } fa_options;
 
 #define FA_SCHED_WORKSPACE_BYTES 16
@@ -367,6 +370,8 @@ typedef struct fa_plan {
                           the rest level by level over all units */
   int64_t num_tasks;
   int64_t tail_first;  /* first key-split task of a balanced last wave (= num_tasks: none) */
+  int grid;            /* 0: the plain order; else the balanced static order for this many
+                          CTAs (set by fa_plan_set_grid) */
 } fa_plan;
 
 typedef struct fa_task {
@@ -382,10 +387,12 @@ int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_
                  int causal, int64_t l2_bytes, int pack, fa_plan* out);
 int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out);
 
-/* The balanced last wave fa_fwd runs on `grid` persistent CTAs (the SM count by
-   default; see fa_options.no_tail_split): updates num_tasks and tail_first of a
-   plan made by fa_make_plan (FA_ERR_INVALID_ARG if already applied or grid < 1).
-   Causal plans, and plans whose last wave gains nothing, are left unchanged. */
+/* The balanced static order fa_fwd runs on `grid` persistent CTAs (the SM count
+   by default; see fa_options.no_balance): sets plan->grid and updates num_tasks
+   and tail_first of a plan made by fa_make_plan (FA_ERR_INVALID_ARG if already
+   applied or grid < 1).  fa_plan_task then returns the tasks in that order
+   (empty entries of the paired causal order have n_blocks = {0, 0} and
+   pos0 = {seqlen_q, seqlen_q}).  Plans that gain nothing are left unchanged. */
 int fa_plan_set_grid(fa_plan* plan, int grid);
 
 /* Does block j need the element mask for a tile starting at pos0? (host view) */

@@ -279,7 +279,7 @@ def test_dynamic_assignment_matches_static_bitwise(fa, name):
     w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, dq, dv, causal, seed=zlib.crc32(name.encode()) % 1000, **extra)
     q, k, v = (to_dev(a) for a in w.generate())
     whole = fa.default_options()
-    whole.no_tail_split = 1  # dynamic assignment keeps whole tasks
+    whole.no_balance = 1  # dynamic assignment keeps whole tasks
     o_s, l_s = fa.attention_forward(q, k, v, causal=causal, scale=w.softmax_scale, options=whole)
     ws = torch.full((fa.SCHED_WORKSPACE_BYTES,), 0x7F, dtype=torch.uint8, device="cuda")  # stale contents
     for grid in (0, 0, 3, 1):
@@ -430,11 +430,11 @@ def test_tail_split_parity(fa, case):
     for off in (0, 1):
         opts = fa.default_options()
         opts.grid = grid
-        opts.no_tail_split = off
+        opts.no_balance = off
         o, lse = run_gpu(fa, w, q, k, v, opts)
         og = o.float().cpu().numpy().astype(np.float64).reshape(-1, dv)
         lg = lse.cpu().numpy().astype(np.float64).transpose(0, 2, 1).reshape(-1)
-        compare(og, lg, o_ref.reshape(-1, dv), lr, f"{name} no_tail_split={off}")
+        compare(og, lg, o_ref.reshape(-1, dv), lr, f"{name} no_balance={off}")
         outs.append((og, lg))
     assert np.abs(outs[0][0] - outs[1][0]).max() <= 2e-2
     assert np.abs(outs[0][1] - outs[1][1]).max() <= 1e-4
@@ -454,3 +454,43 @@ def test_tail_split_store_modes_bitwise_equal(fa):
     torch.cuda.synchronize()
     assert fa.fa_device_status()[0] == 0
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+# Paired causal order: m_blocks m and M-1-m of a unit on one CTA in
+# consecutive waves.  Every tile is computed as in the plain longest-first
+# order, so the outputs must be bit-identical to it; `grid` covers whole
+# blocks, left-over pairs split over two CTAs (2r <= G) and kept on one CTA
+# with empty list entries (2r > G).
+PAIRED = [
+    # name, B, Hq, Hkv, Sq, Sk, dq, dv, grids
+    ("pair_direct", 2, 4, 4, 2048, 2048, 128, 128, (0, 5, 7, 13)),
+    ("pair_fixed", 1, 2, 2, 4608, 4608, 128, 128, (0, 5, 11)),
+    ("pair_gqa", 1, 16, 4, 1024, 1024, 128, 128, (0, 3, 6)),
+    ("pair_sq_lt_sk", 1, 4, 2, 1000, 1500, 64, 64, (0, 3)),
+    ("pair_asym", 1, 4, 4, 1024, 1024, 192, 128, (0, 3, 5)),
+]
+
+
+@pytest.mark.parametrize("case", PAIRED, ids=[c[0] for c in PAIRED])
+def test_paired_order_bitwise_equal_to_plain_order(fa, case):
+    name, B, Hq, Hkv, Sq, Sk, dq, dv, grids = case
+    w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, dq, dv, True, seed=zlib.crc32(name.encode()) % 1000)
+    q, k, v = w.generate()
+    plain = fa.default_options()
+    plain.no_balance = 1
+    o0, l0 = run_gpu(fa, w, q, k, v, plain)
+    for grid in grids:
+        base = fa.fa_make_plan(B, Hq, Hkv, Sq, Sk, dq, dv, 1)
+        plan = fa.fa_make_plan(B, Hq, Hkv, Sq, Sk, dq, dv, 1)
+        fa.fa_plan_set_grid(plan, grid if grid > 0 else torch.cuda.get_device_properties(0).multi_processor_count)
+        key = lambda t: (t.b, t.g, t.mblock, t.n_blocks[0])
+        assert [key(fa.fa_plan_task(plan, t)) for t in range(min(plan.num_tasks, base.num_tasks))] != \
+            [key(fa.fa_plan_task(base, t)) for t in range(min(plan.num_tasks, base.num_tasks))], "order unchanged"
+        opts = fa.default_options()
+        opts.grid = grid
+        o1, l1 = run_gpu(fa, w, q, k, v, opts)
+        assert torch.equal(o0, o1) and torch.equal(l0, l1), (name, grid)
+    o_ref, lse_ref = oracle.attn_fwd(q, k, v, causal=True, scale=w.softmax_scale)
+    og = o1.float().cpu().numpy().astype(np.float64).reshape(-1, dv)
+    lg = l1.cpu().numpy().astype(np.float64).transpose(0, 2, 1).reshape(-1)
+    compare(og, lg, o_ref.reshape(-1, dv), lse_ref.transpose(0, 2, 1).reshape(-1), name)

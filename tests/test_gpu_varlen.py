@@ -146,7 +146,7 @@ def test_equal_lengths_match_fixed_length_kernel_bitwise(fa, causal):
     w = synthetic.Workload("eq", B, Hq, Hkv, S, S, d, d, causal, seed=77)
     q, k, v = w.generate()
     whole = fa.default_options()
-    whole.no_tail_split = 1  # the varlen kernel runs whole tasks
+    whole.no_balance = 1  # the varlen kernel runs whole tasks
     o_f, l_f = fa.attention_forward(to_dev(q), to_dev(k), to_dev(v), causal=causal, options=whole)
     cu = np.arange(B + 1) * S
     o_v, l_v = fa.attention_forward_varlen(to_dev(q.reshape(B * S, Hq, d)), to_dev(k.reshape(B * S, Hkv, d)),
