@@ -593,11 +593,17 @@ def run_ours_bwd(args):
     sp = torch.cuda.current_stream(dev).cuda_stream
     scale = w.softmax_scale
 
+    bopts = None
+    if args.no_balance:
+        bopts = fa.default_options()
+        bopts.no_balance = 1
+
     def launch(ins, outs, stream):
         q_, k_, v_, o_, l_, g_ = ins
         rc = fa.fa_bwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), l_.data_ptr(), g_.data_ptr(),
                        outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), w.batch, w.heads_q, w.heads_kv,
-                       w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, stream)
+                       w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, stream,
+                       bopts)
         if rc != 0:
             raise fa.FaError(rc, "fa_bwd")
 
@@ -643,7 +649,10 @@ def run_ours_bwd(args):
     d2h = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
     peak, peak_src = load_peak()
     achieved = flops / (ms_step * 1e-3) / 1e12
-    cfg = config_of(w, world, flops, False)
+    blocks_even = -(-w.seqlen_q // 128) % 2 == 0 and -(-w.seqlen_k // 128) % 2 == 0
+    cfg = config_of(w, world, flops, False, 1,
+                    "plain order (ablation)" if args.no_balance else
+                    ("heavy and light blocks paired on one CTA" if w.causal and blocks_even else "plain order"))
     cfg["pass"] = "backward (dQ, dK, dV; flops = 2.5x forward, 5 GEMMs; the kernels run 7)"
     result = {
         "metric": METRIC_BWD, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,

@@ -964,6 +964,14 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     if (tasks >= big) return FA_ERR_INVALID_ARG;
     int64_t grid = opt.grid > 0 ? opt.grid : st->sms;
     if (grid > tasks) grid = tasks;
+    // paired causal order: heavy and light blocks of a unit on one CTA
+    p.pair_grid = p.pair_body = p.pair_r = 0;
+    if (causal && !opt.no_balance && p.blocks >= 2 && p.blocks % 2 == 0 && grid >= 2) {
+      const int64_t pairs = tasks / 2;
+      p.pair_grid = static_cast<int>(grid);
+      p.pair_body = static_cast<int>(2 * (pairs / grid) * grid);
+      p.pair_r = static_cast<int>(pairs % grid);
+    }
     if (ent[kind].launch(p, static_cast<int>(grid), stream) != cudaSuccess) return FA_ERR_CUDA;
   }
   return FA_OK;

@@ -66,6 +66,10 @@ struct BwdParams {
   int mq, nk;                // ceil(Sq / 128), ceil(Sk / 128)
   int units, blocks;         // tasks = units * blocks: (b, head) units x 128-row blocks
   int section_units;         // causal order: units per L2 section
+  // paired causal order (0 = the plain order): blocks of pair_grid heavy tasks
+  // followed by their complements (heaviness ranks q and blocks - 1 - q of a
+  // unit), then the pair_r pairs left over, heavy tasks first
+  int pair_grid, pair_body, pair_r;
   float scale, scale_log2;
   unsigned long long timeout_ns;
   int debug_flags;           // kDebugSkipPArrive: the row warps never signal p_ready (failure-path test)
@@ -138,7 +142,10 @@ struct BwdTask {
 // blocks.  Non-causal: unit by unit.  Causal: sections of `section_units`
 // units whose streamed tiles fit in L2 together, heaviest block first inside
 // a section (for dK/dV the first key blocks, which every later query sees;
-// for dQ the last query blocks, which see every earlier key).
+// for dQ the last query blocks, which see every earlier key).  With the
+// paired order (an even block count, static assignment over pair_grid CTAs)
+// the task of heaviness rank q and its complement blocks - 1 - q, whose
+// streamed blocks sum to a constant, run on one CTA in consecutive waves.
 template <int KIND>
 __device__ __forceinline__ BwdTask bwd_task(const BwdParams& p, int t) {
   BwdTask k;
@@ -147,6 +154,30 @@ __device__ __forceinline__ BwdTask bwd_task(const BwdParams& p, int t) {
   if (!p.causal) {
     unit = t / M;
     q = t - unit * M;
+  } else if (p.pair_grid > 0) {
+    const int G = p.pair_grid;
+    bool light;
+    if (t < p.pair_body) {
+      const int blk = t / (2 * G);
+      const int w = t - blk * 2 * G;
+      light = w >= G;
+      t = blk * G + (light ? w - G : w);
+    } else {
+      const int tt = t - p.pair_body;
+      light = tt >= p.pair_r;
+      t = p.pair_body / 2 + (light ? tt - p.pair_r : tt);
+    }
+    // pair t: the heavier half (ranks 0 .. M/2 - 1) in section order
+    const int Mh = M / 2;
+    const int su = p.section_units;
+    const int section = t / (su * Mh);
+    const int first = section * su;
+    int in_section = p.units - first;
+    if (in_section > su) in_section = su;
+    const int idx = t - section * su * Mh;
+    q = idx / in_section;
+    unit = first + (idx - q * in_section);
+    if (light) q = M - 1 - q;
   } else {
     const int su = p.section_units;
     const int section = t / (su * M);

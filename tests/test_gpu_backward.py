@@ -113,3 +113,50 @@ def test_backward_mid_size_full(fa, causal):
     w = synthetic.Workload("bmid", 1, 4, 2, 4096, 4096, 128, 128, causal, seed=21 + int(causal))
     inputs, grads = run(fa, w, 17)
     check(w, inputs, grads, f"mid causal={causal}")
+
+
+# Paired causal order of the backward kernels: the task of heaviness rank q
+# and its complement (blocks - 1 - q) on one CTA in consecutive waves.  Every
+# task computes what it computes in the plain order, so the gradients (written
+# over NaN, so a task left out would show) must be bit-identical to it.
+PAIRED = [
+    # name, B, Hq, Hkv, S, d, grids
+    ("bp_even", 2, 4, 2, 1024, 128, (0, 5, 7)),      # 8 blocks
+    ("bp_gqa", 1, 8, 2, 2048, 64, (0, 3, 11)),       # 16 blocks, 4 query heads per K/V head
+    ("bp_odd_blocks", 1, 4, 4, 640, 128, (0, 3)),    # 5 blocks: plain order
+    ("bp_sq_lt_sk", 1, 4, 4, 1000, 1500, 64, (0, 6)),
+]
+
+
+@pytest.mark.parametrize("case", PAIRED, ids=[c[0] for c in PAIRED])
+def test_backward_paired_order_bitwise(fa, case):
+    if len(case) == 8:
+        name, B, Hq, Hkv, Sq, Sk, d, grids = case
+    else:
+        name, B, Hq, Hkv, Sq, d, grids = case
+        Sk = Sq
+    w = synthetic.Workload(name, B, Hq, Hkv, Sq, Sk, d, d, True, seed=zlib.crc32(name.encode()) % 1000)
+    q, k, v = w.generate()
+    g = synthetic.normal_bf16(w.shapes["o"], 13, 7)
+    qd, kd, vd, gd = (to_dev(a) for a in (q, k, v, g))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=True, scale=w.softmax_scale)
+
+    def grads(no_balance, grid):
+        opts = fa.default_options()
+        opts.no_balance = no_balance
+        opts.grid = grid
+        outs = [torch.full_like(t, float("nan")) for t in (qd, kd, vd)]
+        fa.attention_backward(qd, kd, vd, o, lse, gd, causal=True, scale=w.softmax_scale, dq=outs[0], dk=outs[1],
+                              dv=outs[2], options=opts)
+        torch.cuda.synchronize()
+        code, detail = fa.fa_device_status()
+        assert code == 0, f"device status {code} {detail}"
+        return outs
+
+    plain = grads(1, 0)
+    for t in plain:
+        assert torch.isfinite(t.float()).all()
+    for grid in grids:
+        for a, b in zip(grads(0, grid), plain):
+            assert torch.equal(a, b), (name, grid)
+    check(w, (q, k, v, g), plain, name)
