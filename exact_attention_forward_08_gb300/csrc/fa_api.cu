@@ -1053,14 +1053,13 @@ int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_
 }
 
 static fa::Problem problem_of(const fa_plan* pl) {
-  fa::Problem p;
+  fa::Problem p{};
   p.B = pl->batch, p.Hq = pl->heads_q, p.Hkv = pl->heads_kv, p.Sq = pl->seqlen_q, p.Sk = pl->seqlen_k;
   p.causal = pl->causal, p.pack = pl->pack, p.groups = pl->groups, p.pos_per_tile = pl->pos_per_tile;
   p.tiles = pl->tiles, p.mblocks = pl->mblocks, p.kv_blocks = pl->kv_blocks, p.ratio = pl->ratio;
   p.section_units = pl->section_units, p.heavy_levels = pl->heavy_levels;
   p.num_tasks = static_cast<int64_t>(pl->batch) * pl->groups * pl->mblocks;  // the plain order
   p.tail_first = p.num_tasks;
-  p.pair_grid = p.pair_body = p.pair_r = p.pair_split_tail = 0;
   p.splits = 1, p.split_blocks = pl->kv_blocks;
   fa::set_divisors(p);
   if (pl->grid > 0) fa::set_balance(p, pl->grid);

@@ -190,9 +190,12 @@ __device__ __forceinline__ int task_count(const Params& p) {
 }
 
 // FD: decode with the FastDiv fields (short-task kernels, where the decoding
-// sits on the path between tasks); otherwise plain division.  BAL: the
-// balanced static orders (key-split last wave without the mask, paired order
-// with it) may be in use; dynamically scheduled kernels leave them out.
+// sits on the path between tasks); the causal kernels always do (their paired
+// order takes several divisions per task, and a run-time division is a
+// reciprocal on the SFU, queued behind the softmax's exponentials); the
+// non-causal long-task kernels divide plainly.  BAL: the balanced static
+// orders (key-split last wave without the mask, paired order with it) may be
+// in use; dynamically scheduled kernels leave them out.
 template <bool VARLEN, bool SPLIT, bool CAUSAL, bool FD, bool BAL>
 __device__ __forceinline__ Task get_task(const Params& p, int t) {
   if constexpr (SPLIT) {
@@ -206,7 +209,7 @@ __device__ __forceinline__ Task get_task(const Params& p, int t) {
     return task_from_record(p.prob, rec);
   } else {
     if constexpr (FD) return decode_task_k<CAUSAL ? 1 : 0, true, BAL && !CAUSAL, BAL && CAUSAL>(p.prob, t);
-    else if constexpr (CAUSAL) return decode_task_k<1, false, false, BAL>(p.prob, t);
+    else if constexpr (CAUSAL) return decode_task_k<1, true, false, BAL>(p.prob, t);
     else return decode_task_k<-1, false, BAL, false>(p.prob, t);
   }
 }

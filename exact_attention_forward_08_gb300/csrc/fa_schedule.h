@@ -43,11 +43,18 @@
 //    the L2-section order above) followed by their G light complements, so
 //    that CTA c runs the heavy task of pair bG + c and then its complement;
 //    every CTA then gets the same work per two waves.  The r = P mod G pairs
-//    left over (P = units * M / 2) go last: each pair's two tasks to two
-//    CTAs when 2r <= G, else both to one CTA (the list then holds G - r
-//    empty entries).  A host simulation of per-CTA key blocks put the
-//    busiest CTA 6-13 % above the average with the plain order on the causal
-//    benchmark problems and 2-4 % with this one.
+//    left over (P = units * M / 2) go last.  When 2r <= G each pair's two
+//    tasks go to two CTAs.  Otherwise the left-over pairs are taken from the
+//    heaviness levels whose heavy task costs about r / G of a pair: their
+//    heavy tasks run on CTAs 0 .. r-1 and their light complements are dealt
+//    round-robin over the G - r other CTAs (about r / (G - r) each), so the
+//    last wave costs about r / G of a pair instead of a whole one; the list
+//    then holds empty entries where a CTA has nothing left.  The levels are
+//    chosen on the host with a cost model (key blocks of the two tiles / 2
+//    plus a fixed start-up per task); when no choice beats keeping each pair
+//    on one CTA, that is what runs.  The model put the busiest CTA 6-13 %
+//    above the average with the plain order on the causal benchmark problems,
+//    3.9 % with pairs alone and 0.5-1.8 % with the packed last wave.
 //  * Split-KV (decode and other short-Q problems, where (b, g, m_block) tasks
 //    are too few to fill the GPU): each task also takes one of `splits`
 //    consecutive key ranges of split_blocks blocks ("Infra: Flash Attention",
@@ -124,6 +131,8 @@ struct Problem {
   int pair_body;       // entries of the whole blocks (2 * G * (P / G))
   int pair_r;          // pairs left over (P mod G)
   int pair_split_tail; // 1: each left-over pair's two tasks go to two CTAs
+  int pair_pack;       // 1: left-over heavy tasks on r CTAs, their complements on the others
+  int pair_q0, pair_nt;// pair_nt > 0: heaviness levels q0 .. q0+nt-1 go last (the left-over pairs)
   // the divisors of the task decoding (set_divisors)
   FastDiv fd_mblocks, fd_splits, fd_groups, fd_ratio, fd_pack;
   FastDiv fd_units;    // B * groups
@@ -131,6 +140,8 @@ struct Problem {
   FastDiv fd_su;       // section_units
   FastDiv fd_last;     // units of the last causal section
   FastDiv fd_pair2g;   // 2 * pair_grid
+  FastDiv fd_grid;     // pair_grid
+  FastDiv fd_section_main;  // section_units * (heavy_levels - pair_nt)
 };
 
 // Fill the FastDiv fields from the integer fields; call after any change.
@@ -148,6 +159,8 @@ FA_HD void set_divisors(Problem& p) {
   const int last_first = units > 0 ? ((units - 1) / su) * su : 0;
   p.fd_last = make_fastdiv(units - last_first);
   p.fd_pair2g = make_fastdiv(2 * (p.pair_grid > 0 ? p.pair_grid : 1));
+  p.fd_grid = make_fastdiv(p.pair_grid > 0 ? p.pair_grid : 1);
+  p.fd_section_main = make_fastdiv(p.section_units * (p.heavy_levels - p.pair_nt));
 }
 
 struct Task {
@@ -258,30 +271,6 @@ FA_HD void set_tail_split(Problem& p, int64_t grid) {
   p.num_tasks += r;
 }
 
-// Paired causal order for `grid` CTAs taken round-robin (see the header
-// comment): needs an even m_block count and a list that stays below 2^31.
-FA_HD void set_pairing(Problem& p, int64_t grid) {
-  if (!p.causal || p.splits != 1 || p.mblocks < 2 || (p.mblocks & 1) || grid < 2 || p.pair_grid != 0) return;
-  const int64_t P = static_cast<int64_t>(p.B) * p.groups * (p.mblocks / 2);
-  const int64_t full = P / grid, r = P % grid;
-  const bool split_tail = 2 * r <= grid;
-  const int64_t n = 2 * full * grid + (r == 0 ? 0 : (split_tail ? 2 * r : grid + r));
-  if (n >= (int64_t(1) << 31)) return;
-  p.pair_grid = static_cast<int>(grid);
-  p.pair_body = static_cast<int>(2 * full * grid);
-  p.pair_r = static_cast<int>(r);
-  p.pair_split_tail = split_tail ? 1 : 0;
-  p.num_tasks = n;
-  p.tail_first = n;
-  set_divisors(p);
-}
-
-// The balanced static order for `grid` CTAs: the key-split last wave without
-// the causal mask, the paired order with it.
-FA_HD void set_balance(Problem& p, int64_t grid) {
-  if (p.causal) set_pairing(p, grid);
-  else set_tail_split(p, grid);
-}
 
 // K/V blocks a Q tile starting at pos0 visits (sq queries, ppt positions per
 // tile; kend / kshift as in Task).
@@ -295,6 +284,79 @@ FA_HD int tile_blocks_len(int sq, int kend, int kshift, int causal, int ppt, int
   if (max_key < 0) return 0;
   const int64_t n = max_key / kBN + 1;
   return n < kvb ? static_cast<int>(n) : kvb;
+}
+
+// Paired causal order for `grid` CTAs taken round-robin (see the header
+// comment): needs an even m_block count and a list that stays below 2^31.
+// Modelled cost of m_block m: key blocks of its two tiles / 2 + a start-up.
+constexpr double kPairTaskStartup = 2.5;
+
+FA_HD double pair_task_cost(const Problem& p, int m) {
+  const int kshift = p.Sk - p.Sq;
+  const int a = tile_blocks_len(p.Sq, p.Sk, kshift, 1, p.pos_per_tile, (2 * m) * p.pos_per_tile);
+  const int b = tile_blocks_len(p.Sq, p.Sk, kshift, 1, p.pos_per_tile, (2 * m + 1) * p.pos_per_tile);
+  return 0.5 * (a + b) + kPairTaskStartup;
+}
+
+// Modelled last wave when the r left-over pairs come from heaviness levels
+// q0 .. q0+nt-1 (the last r pairs of those levels, level-major over units):
+// heavy tasks one per CTA, light complements round-robin over G - r CTAs.
+FA_HD double packed_tail_cost(const Problem& p, int G, int r, int q0, int nt) {
+  const int M = p.mblocks, units = p.B * p.groups;
+  double worst = 0.0;
+  for (int j = 0; j < r; ++j) {  // heavy tasks
+    const int q = q0 + (nt * units - r + j) / units;
+    const double h = pair_task_cost(p, M - 1 - q);
+    if (h > worst) worst = h;
+  }
+  const int free = G - r;
+  for (int c = 0; c < free; ++c) {  // light loads
+    double load = 0.0;
+    for (int j = c; j < r; j += free) load += pair_task_cost(p, q0 + (nt * units - r + j) / units);
+    if (load > worst) worst = load;
+  }
+  return worst;
+}
+
+FA_HD void set_pairing(Problem& p, int64_t grid) {
+  if (!p.causal || p.splits != 1 || p.mblocks < 2 || (p.mblocks & 1) || grid < 2 || p.pair_grid != 0) return;
+  const int64_t P = static_cast<int64_t>(p.B) * p.groups * (p.mblocks / 2);
+  const int64_t full = P / grid, r = P % grid;
+  const bool split_tail = 2 * r <= grid;
+  int pack = 0, q0 = 0, nt = 0;
+  int64_t tail = r == 0 ? 0 : (split_tail ? 2 * r : grid + r);
+  if (!split_tail && grid <= (int64_t(1) << 20)) {  // try packing the light complements
+    const int units = p.B * p.groups, Mh = p.mblocks / 2, G = static_cast<int>(grid), R = static_cast<int>(r);
+    const int need = (R + units - 1) / units;  // heaviness levels that hold r pairs
+    const int M = p.mblocks;
+    double best = pair_task_cost(p, M - 1) + pair_task_cost(p, 0);  // a whole pair on one CTA
+    if (need <= Mh) {
+      for (int c = 0; c + need <= Mh; ++c) {
+        const double cost = packed_tail_cost(p, G, R, c, need);
+        if (cost < 0.999 * best) best = cost, pack = 1, q0 = c, nt = need;
+      }
+    }
+    if (pack) tail = ((r + (grid - r) - 1) / (grid - r)) * grid;
+  }
+  const int64_t n = 2 * full * grid + tail;
+  if (n >= (int64_t(1) << 31)) return;
+  p.pair_grid = static_cast<int>(grid);
+  p.pair_body = static_cast<int>(2 * full * grid);
+  p.pair_r = static_cast<int>(r);
+  p.pair_split_tail = split_tail ? 1 : 0;
+  p.pair_pack = pack;
+  p.pair_q0 = q0;
+  p.pair_nt = nt;
+  p.num_tasks = n;
+  p.tail_first = n;
+  set_divisors(p);
+}
+
+// The balanced static order for `grid` CTAs: the key-split last wave without
+// the mask, the paired order with it.
+FA_HD void set_balance(Problem& p, int64_t grid) {
+  if (p.causal) set_pairing(p, grid);
+  else set_tail_split(p, grid);
 }
 
 // Task t (0 <= t < num_tasks < 2^31; the host refuses larger problems).
@@ -330,9 +392,17 @@ FA_HD Task decode_task_k(const Problem& p, int t) {
         t = blk * G + (light ? w - G : w);
       } else {  // the pairs left over
         const int tt = t - p.pair_body;
-        const int half = p.pair_split_tail ? p.pair_r : G;
-        light = tt >= half;
-        const int pos = light ? tt - half : tt;
+        int pos;
+        if (!p.pair_pack) {  // both tasks of pair pos: positions pos and pos + half
+          const int half = p.pair_split_tail ? p.pair_r : G;
+          light = tt >= half;
+          pos = light ? tt - half : tt;
+        } else {  // heavy tasks on CTAs 0 .. r-1, light ones dealt over the other CTAs
+          const int w = FAST ? fdiv(tt, p.fd_grid) : tt / G;
+          const int c = tt - w * G;
+          light = c >= p.pair_r;
+          pos = light ? w * (G - p.pair_r) + (c - p.pair_r) : (w > 0 ? p.pair_r : c);
+        }
         if (pos >= p.pair_r) {  // an empty entry: no rows, no keys
           k.b = 0, k.g = 0, k.mb = 0, k.kvh = 0;
           k.sq = p.Sq, k.kend = p.Sk, k.kshift = p.Sk - p.Sq, k.q_row0 = 0, k.k_row0 = 0, k.bc = 0;
@@ -346,7 +416,28 @@ FA_HD Task decode_task_k(const Problem& p, int t) {
     }
     const int units = p.B * p.groups;
     const int Mh = p.heavy_levels;
-    if (t < units * Mh) {  // heavier half: L2 sections, m_block decreasing inside each
+    if (PAIR && p.pair_grid > 0 && p.pair_nt > 0) {  // pair t; levels q0 .. q0+nt-1 go after all others
+      const int Mm = Mh - p.pair_nt;
+      const int n_main = units * Mm;
+      int q;
+      if (t < n_main) {  // L2 sections over the other levels
+        const int su = p.section_units;
+        const int section = FAST ? fdiv(t, p.fd_section_main) : t / (su * Mm);
+        const int first_unit = section * su;
+        int in_section = units - first_unit;
+        if (in_section > su) in_section = su;
+        const int idx = t - section * su * Mm;
+        const int qq = FAST ? fdiv(idx, in_section == su ? p.fd_su : p.fd_last) : idx / in_section;
+        unit = first_unit + (idx - qq * in_section);
+        q = qq < p.pair_q0 ? qq : qq + p.pair_nt;
+      } else {  // the left-over levels, level-major over all units
+        const int k = t - n_main;
+        const int lv = FAST ? fdiv(k, p.fd_units) : k / units;
+        unit = k - lv * units;
+        q = p.pair_q0 + lv;
+      }
+      mb = M - 1 - q;
+    } else if (t < units * Mh) {  // heavier half: L2 sections, m_block decreasing inside each
       const int su = p.section_units;
       const int section = FAST ? fdiv(t, p.fd_section) : t / (su * Mh);
       const int first_unit = section * su;
