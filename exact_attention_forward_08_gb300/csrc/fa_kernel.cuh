@@ -751,10 +751,26 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   auto release_tile = [&](uint32_t it) { mma_commit(bar(L::bKvEmpty + static_cast<int>(it % L::NS)), leader); };
 
   const int num_tasks = task_count<VARLEN>(p);
+  // short-task kernels with static assignment: the next task is decoded while
+  // the current one runs, off the path from one task's last P V to the next
+  // task's first Q K^T
+  constexpr bool kPre = FD && !DYN;
+  Task nxt{};
+  if constexpr (kPre) {
+    const int t0 = read_task<DQ, DV, DYN>(0, num_tasks, bar0, ring, wc, kSiteMmaTask);
+    if (t0 >= 0) nxt = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, t0);
+  }
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteMmaTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    const Task tk = kPre ? nxt : get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    // decode task kt + 1 (called once the first Q K^T of task kt are issued)
+    auto pre_next = [&]() {
+      if constexpr (kPre) {
+        const int t1 = read_task<DQ, DV, DYN>(kt + 1, num_tasks, bar0, ring, wc, kSiteMmaTask);
+        if (t1 >= 0) nxt = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, t1);
+      }
+    };
     if (TS && tk.ksplit != 0) {
       // key-split tail task: both stages hold one Q tile and stream their own
       // key halves.  Ring order: K_0 of stage 0 and of stage 1, then per
@@ -773,6 +789,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
         if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
         release_tile(it++);
       }
+      pre_next();
       for (int j = 0; j < tk.n[0]; ++j) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -800,7 +817,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
     }
     const uint32_t base = kv_it;
     kv_it += 2u * static_cast<uint32_t>(tk.nmax);
-    if (tk.nmax == 0) continue;
+    if (tk.nmax == 0) {
+      pre_next();
+      continue;
+    }
 
     // prologue: S_s = Q_s K_0^T for both stages
     if (!wait_tile(base)) goto out;
@@ -815,6 +835,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
       if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
     }
     release_tile(base);  // K_0, once both Q K^T have finished
+    pre_next();
 
     for (int j = 0; j < tk.nmax; ++j) {
       const uint32_t v_it = base + 2u * static_cast<uint32_t>(j) + 1u;
