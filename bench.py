@@ -278,6 +278,8 @@ def balance_of(w, sms: int) -> str:
     """The balanced static order the library runs for this workload on `sms` CTAs
     (from its host copy of the schedule)."""
     import exact_attention_forward_08_gb300 as fa
+    if is_varlen(w):
+        return ""  # varlen batches take their tasks dynamically
     plan = fa.fa_make_plan(w.batch, w.heads_q, w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal))
     n = plan.num_tasks
     fa.fa_plan_set_grid(plan, sms)
