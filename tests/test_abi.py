@@ -81,10 +81,11 @@ def test_empty_problem_is_ok_without_launch(fa, kw):
 
 def test_bad_options_rejected(fa):
     opts = fa.default_options()
-    assert abs(opts.tau - 8.0) < 1e-7 and opts.pack == 0 and opts.grid == 0
+    assert abs(opts.tau - 8.0) < 1e-7 and opts.pack == 0 and opts.grid == 0 and opts.no_balance == 0
     for field, value in (("pack", 3), ("pack", -1), ("grid", -2), ("debug_flags", 4), ("debug_flags", 8),
                          ("timeout_s", 1e9), ("tau", 65.0), ("tau", float("inf")), ("tau", float("nan")), ("exp_emu", 2),
-                         ("exp_emu", -1), ("store_mode", 3), ("store_mode", -1)):
+                         ("exp_emu", -1), ("store_mode", 3), ("store_mode", -1), ("no_balance", 2),
+                         ("no_balance", -1)):
         o = fa.default_options()
         setattr(o, field, value)
         rc = fa.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 1, 64, 64, 128, 128, 0, 0.0, o, None)
