@@ -251,3 +251,20 @@ def test_set_grid_rejects_bad_calls():
     fa.fa_plan_set_grid(plan, 152)
     with pytest.raises(fa.FaError):  # already applied
         fa.fa_plan_set_grid(plan, 152)
+
+
+def test_packing_only_when_the_light_tasks_fit():
+    """With r close to G the light complements of the left-over heavy tasks
+    would pile up on the few free CTAs beyond a whole pair's cost: the cost
+    model then keeps each pair on one CTA."""
+    # 1 x 16 heads, 64 m_blocks: 512 pairs; grid 257 leaves r = 255 (G - r = 2)
+    plan = fa.fa_make_plan(1, 16, 16, 16384, 16384, 128, 128, 1)
+    fa.fa_plan_set_grid(plan, 257)
+    pairs, grid = 512, 257
+    full, r = divmod(pairs, grid)
+    assert r == 255
+    assert plan.num_tasks == 2 * full * grid + grid + r  # whole pairs on one CTA each
+    # a grid that leaves few enough light tasks per free CTA packs them
+    plan = fa.fa_make_plan(4, 16, 16, 8192, 8192, 128, 128, 1)
+    fa.fa_plan_set_grid(plan, 152)
+    assert plan.num_tasks == 2 * 6 * 152 + 3 * 152  # 112 left over: 3 waves of light tasks
