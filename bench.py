@@ -50,11 +50,16 @@ def parse_args(argv=None):
     ap.add_argument("--config", default="mha8k")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--launch-samples", type=int, default=50,
+                    help="launches timed one by one after the timed region (mean and median; at least 50; 0 "
+                         "skips this pass, for profiler runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-balance", action="store_true",
                     help="ablation: the plain static task order (fa_options.no_balance = 1)")
+    ap.add_argument("--stagger", action="store_true",
+                    help="ablation: the softmax warpgroups take turns for their exponentials (fa_options.stagger)")
     ap.add_argument("--dynamic", action="store_true",
                     help="fixed-length workloads: assign tasks dynamically (scheduling workspace)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
@@ -62,6 +67,12 @@ def parse_args(argv=None):
                          "forward's")
     ap.add_argument("--splitkv", type=int, default=0,
                     help="split-KV ranges for fixed-length workloads (decode workloads always split; 0 = auto there)")
+    ap.add_argument("--trace", action="store_true",
+                    help="fixed-length forward: run the workload once with the kernel's event log (trace build) on "
+                         "the first --trace-ctas CTAs and print the interval summary (cycles), with the mean launch "
+                         "time of the trace build beside the default kernel's, instead of timing")
+    ap.add_argument("--trace-ctas", type=int, default=8)
+    ap.add_argument("--trace-cap", type=int, default=16384)
     ap.add_argument("--count-rescales", action="store_true",
                     help="fixed-length forward: run the workload once with the O-rescale counter on and print the "
                          "count, the most the launch could count (warps x K/V blocks after a tile's first) and their "
@@ -192,6 +203,36 @@ def stored_traffic(config: str):
         return float(kv["dram_bytes_per_launch"])
     except Exception:
         return None
+
+
+TC_FLOP_PER_CLK_PER_SM = 8192  # dense bf16 tensor-core rate per SM and clock ("FlashAttention-4 wiki",
+                                # "Key observations", observation 1)
+
+
+def per_launch_times(torch, stream, step, n: int):
+    """Mean and median over n launches, each bracketed by its own CUDA events
+    on the launching stream (recorded back to back, so the launches still run
+    one after the other as in the timed region)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
+        step()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    return {"n": n, "mean_ms": round(statistics.fmean(ms), 4), "median_ms": round(statistics.median(ms), 4),
+            "min_ms": round(min(ms), 4), "max_ms": round(max(ms), 4)}
+
+
+def clock_peak(flops: float, ms: float, sms: int, clk):
+    """The tensor-core rate implied by the clocks seen during the timed region:
+    8192 flop per clock per SM x SMs x the median SM clock under load."""
+    if not clk or not clk.get("sm_mhz"):
+        return None
+    peak = TC_FLOP_PER_CLK_PER_SM * sms * clk["sm_mhz"] * 1e6 / 1e12
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"value": round(peak, 1), "unit": "TFLOP/s", "sm_mhz": clk["sm_mhz"], "sms": sms,
+            "flop_per_clk_per_sm": TC_FLOP_PER_CLK_PER_SM, "frac": round(achieved / peak, 4)}
 
 
 # ---------------------------------------------------------------------------
@@ -455,6 +496,9 @@ def run_ours(args):
         if args.no_balance:
             opts = opts or fa.default_options()
             opts.no_balance = 1
+        if args.stagger:
+            opts = opts or fa.default_options()
+            opts.stagger = 1
         launches_per_step = 1
 
         def launch(ins, outs, stream):
@@ -491,12 +535,15 @@ def run_ours(args):
     clocks.mark("stop")
     barrier()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    # the same launches timed one by one (mean and median), after the timed region
+    launches = per_launch_times(torch, stream, step, max(50, args.launch_samples)) if args.launch_samples else None
     clk = clocks.stop()
     code, detail = fa.fa_device_status()
     if code != 0:
         raise fa.FaError(code, f"device status after timed region {detail}")
     ms_step = ms_total / args.steps
     flops = w.flops()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     value = world * flops / (ms_step * 1e-3) / 1e12
 
     # end to end: pinned host inputs -> device, forward, O and LSE back to host
@@ -518,6 +565,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, world, flops, args.dynamic, splits,
                             "plain order (ablation)" if args.no_balance else
+                            (balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count) +
+                             "; staggered exponentials (ablation)") if args.stagger else
                             balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count)),
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
@@ -526,7 +575,9 @@ def run_ours(args):
                      "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
                      "peak_source": f"{peak_src} ({'copy bandwidth' if hbm_bound else 'bf16 dense, burst'})",
-                     "algorithmic_bytes": w.algorithmic_bytes()},
+                     "algorithmic_bytes": w.algorithmic_bytes(),
+                     "clock_peak": None if hbm_bound else clock_peak(flops, ms_step, sms, clk)},
+        "launches": launches,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -636,12 +687,15 @@ def run_ours_bwd(args):
     clocks.mark("stop")
     barrier()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    # the same launches timed one by one (mean and median), after the timed region
+    launches = per_launch_times(torch, stream, step, max(50, args.launch_samples)) if args.launch_samples else None
     clk = clocks.stop()
     code, detail = fa.fa_device_status()
     if code != 0:
         raise fa.FaError(code, f"device status after timed region {detail}")
     ms_step = ms_total / args.steps
     flops = 2.5 * w.flops()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     value = world * flops / (ms_step * 1e-3) / 1e12
 
     # end to end: the backward's inputs in, the three gradients out
@@ -665,7 +719,9 @@ def run_ours_bwd(args):
         "gpu_launches": args.steps * 3,  # row preparation, dK/dV kernel, dQ kernel
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
-                     "peak_source": f"{peak_src} (bf16 dense, burst)", "algorithmic_flops": flops},
+                     "peak_source": f"{peak_src} (bf16 dense, burst)", "algorithmic_flops": flops,
+                     "clock_peak": clock_peak(flops, ms_step, sms, clk)},
+        "launches": launches,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -751,6 +807,64 @@ def run_reference_bwd(args, w, q, k, v):
     }
 
 
+def trace_run(args) -> dict:
+    """One forward launch of a fixed-length workload with the event log on
+    (fa_options.trace) and the interval summary of exact_attention_forward_08_gb300.trace."""
+    import numpy as np
+    import torch
+    import exact_attention_forward_08_gb300 as fa
+    from exact_attention_forward_08_gb300 import trace as tr
+    w = get_workload(args.config)
+    if is_varlen(w) or is_decode(args.config):
+        raise SystemExit("--trace takes a fixed-length --config")
+    fa.load_library()
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    q, k, v = (to_dev(a) for a in w.generate())
+    o = torch.empty(w.shapes["o"], dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(w.shapes["lse"], dtype=torch.float32, device="cuda")
+    words = tr.trace_words(args.trace_ctas, args.trace_cap)
+    buf = torch.zeros(words, dtype=torch.int64, device="cuda")
+    topts = fa.default_options()
+    topts.trace = buf.data_ptr()
+    topts.trace_ctas = args.trace_ctas
+    topts.trace_cap = args.trace_cap
+    stream = torch.cuda.current_stream()
+
+    def launch(opts):
+        rc = fa.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.batch, w.heads_q,
+                          w.heads_kv, w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), w.softmax_scale, opts,
+                          stream.cuda_stream)
+        if rc != 0:
+            raise fa.FaError(rc, "fa_fwd_ex")
+
+    def mean_ms(opts, n=10):
+        for _ in range(3):
+            launch(opts)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            launch(opts)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    base_ms = mean_ms(None)
+    trace_ms = mean_ms(topts)
+    buf.zero_()
+    launch(topts)
+    torch.cuda.synchronize()
+    code, detail = fa.fa_device_status()
+    if code != 0:
+        raise SystemExit(f"device status {code} {detail}")
+    host = buf.cpu().numpy().view(np.uint64)
+    ctas = tr.decode(host, args.trace_ctas, args.trace_cap)
+    dropped = sum(max(0, n - args.trace_cap) for c in ctas for n in c["_counts"].values())
+    return {"config": args.config, "workload": f"{w.name}: {w.notes}", "trace_ctas": args.trace_ctas,
+            "records_dropped": dropped, "kernel_ms_default": round(base_ms, 4),
+            "kernel_ms_trace_build": round(trace_ms, 4), "unit": "SM clock cycles",
+            "summary": tr.summarize(ctas)}
+
+
 def count_rescales(args) -> dict:
     """One forward launch of a fixed-length workload with the correction warps'
     O-rescale counter on (fa_options.debug_flags bit 1)."""
@@ -788,6 +902,9 @@ def main(argv=None):
     args = parse_args(argv)
     if args.count_rescales:
         print(json.dumps(count_rescales(args)), flush=True)
+        return 0
+    if args.trace:
+        print(json.dumps(trace_run(args)), flush=True)
         return 0
     if args.impl == "reference":
         runner = run_reference

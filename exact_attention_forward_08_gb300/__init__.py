@@ -25,15 +25,15 @@ from . import _build
 __all__ = ["fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_varlen_ex", "fa_varlen_workspace_size",
            "fa_varlen_plan_host", "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_num_splits",
            "attention_forward_splitkv", "fa_bwd", "fa_bwd_workspace_size", "attention_backward",
-           "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
+           "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_device_status_code", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
            "fa_plan_task", "fa_plan_set_grid", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
            "FaTask", "FaVarlenTask", "attention_forward", "attention_forward_varlen", "FaError", "load_library",
            "LIB_PATH", "STATUS", "VARLEN_HEADER_BYTES"]
 
 LIB_PATH = _build.LIB
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
-          4: "FA_ERR_DEVICE_TIMEOUT"}
-FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(5)
+          4: "FA_ERR_DEVICE_TIMEOUT", 5: "FA_ERR_DEVICE_CHECK"}
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_CHECK = range(6)
 
 
 class FaError(RuntimeError):
@@ -45,7 +45,9 @@ class FaError(RuntimeError):
 class FaOptions(ctypes.Structure):
     _fields_ = [("tau", ctypes.c_float), ("pack", ctypes.c_int), ("grid", ctypes.c_int),
                 ("timeout_s", ctypes.c_double), ("debug_flags", ctypes.c_int), ("exp_emu", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("store_mode", ctypes.c_int), ("no_balance", ctypes.c_int)]
+                ("workspace", ctypes.c_void_p), ("store_mode", ctypes.c_int), ("no_balance", ctypes.c_int),
+                ("trace", ctypes.c_void_p), ("trace_ctas", ctypes.c_int), ("trace_cap", ctypes.c_int),
+                ("stagger", ctypes.c_int)]
 
 
 # bytes of the optional fixed-length scheduling workspace (fa_options.workspace)
@@ -95,8 +97,10 @@ def load_library(path: str | None = None):
     lib.fa_fwd_ex.restype = _I
     lib.fa_options_default.argtypes = [ctypes.POINTER(FaOptions)]
     lib.fa_options_default.restype = None
-    lib.fa_device_status.argtypes = [_P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_device_status.argtypes = [_P, ctypes.POINTER(_I)]
     lib.fa_device_status.restype = _I
+    lib.fa_device_status_detail.argtypes = [_P, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_uint)]
+    lib.fa_device_status_detail.restype = _I
     lib.fa_debug_rescale_count.argtypes = [_P, ctypes.POINTER(ctypes.c_uint)]
     lib.fa_debug_rescale_count.restype = _I
     lib.fa_status_string.argtypes = [_I]
@@ -175,18 +179,30 @@ def fa_fwd_ex(q, k, v, o, lse, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_q
 
 
 def fa_device_status(stream=None):
-    """Synchronise ``stream`` and read/clear the device status: (code, (code, site, block))."""
+    """Synchronise ``stream`` and read/clear the device status through
+    ``fa_device_status_detail``: (code, (code, site, block))."""
     out = _I(0)
     detail = (ctypes.c_uint * 3)()
-    rc = load_library().fa_device_status(stream, ctypes.byref(out), detail)
+    rc = load_library().fa_device_status_detail(stream, ctypes.byref(out), detail)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_device_status_detail")
+    return out.value, tuple(detail)
+
+
+def fa_device_status_code(stream=None) -> int:
+    """``fa_device_status``: synchronise ``stream``, read and clear the status code."""
+    out = _I(0)
+    rc = load_library().fa_device_status(stream, ctypes.byref(out))
     if rc != FA_OK:
         raise FaError(rc, "fa_device_status")
-    return out.value, tuple(detail)
+    return out.value
 
 
 # fa_options.debug_flags bits
 DEBUG_SKIP_P_ARRIVE = 1
 DEBUG_COUNT_RESCALE = 2
+DEBUG_CHECKS = 4        # the checking build of the forward kernel
+DEBUG_PLANT_BAD_TASK = 8  # with DEBUG_CHECKS: task 0 decodes out of range (the checks must catch it)
 
 
 def fa_debug_rescale_count(stream=None) -> int:

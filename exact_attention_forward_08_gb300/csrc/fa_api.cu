@@ -57,6 +57,7 @@ struct DeviceState {
   unsigned int* status = nullptr;
   void* noalloc_scratch = nullptr;  // g_fa_noalloc_scratch on this device
   bool kernel_ready[kNumKernels] = {};
+  bool debug_ready[5 * 2 * 2 * 3] = {};  // (d_qk, d_v) pair x causal x (fixed, direct) x (trace, check, stagger)
   bool bwd_ready[2 * 2 * 2] = {};   // (d 64 / 128) x (dK/dV, dQ) x (non-causal, causal)
   bool plan_ready = false;
 };
@@ -79,6 +80,15 @@ bool get_entry(int dq, int dv, int causal, int variant, fa::KernelEntry* e) {
   if (dq == 64) return fa::entry_d64(dv, causal, variant, e);
   if (dq == 128) return fa::entry_d128(dv, causal, variant, e);
   if (dq == 192) return fa::entry_d192(dv, causal, variant, e);
+  return false;
+}
+
+// build variants: var = fa::kVarTrace, fa::kVarCheck or fa::kVarStagger, variant fixed or direct
+bool get_debug_entry(int dq, int dv, int causal, int variant, int var, fa::KernelEntry* e) {
+  if (var == fa::kVarTrace) return fa::entry_trace(dq, dv, causal, variant, e);
+  if (var == fa::kVarStagger) return fa::entry_stagger(dq, dv, causal, variant, e);
+  if (var == fa::kVarCheck)
+    return dq == 192 ? fa::entry_check_b(dq, dv, causal, variant, e) : fa::entry_check_a(dq, dv, causal, variant, e);
   return false;
 }
 
@@ -115,6 +125,11 @@ int init_device(int dev, DeviceState** out) {
     // the header (task count, task counter) starts cleared; every call's
     // planning kernel rewrites both before the attention kernel reads them
     if (cudaMemset(st.noalloc_scratch, 0, kVarlenHeaderBytes) != cudaSuccess) return FA_ERR_CUDA;
+    // the two clears above run on the legacy default stream, which is not
+    // ordered against a caller's non-blocking stream: finish them before this
+    // call enqueues anything, so that neither lands after a kernel on the
+    // caller's stream has written the status word or the scratch header
+    if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
     if (g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -133,9 +148,9 @@ int init_device(int dev, DeviceState** out) {
 // Per device and kernel: allow the large dynamic shared memory and check the
 // register count the warp-role split assumes (the roles move registers with
 // setmaxnreg; their total must fit what the CTA is launched with).
-int prepare_kernel(DeviceState* st, int idx, const fa::KernelEntry& e) {
+int prepare_kernel(DeviceState* st, bool* ready, const fa::KernelEntry& e) {
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (st->kernel_ready[idx]) return FA_OK;
+  if (*ready) return FA_OK;
   if (e.smem > st->smem_optin) return FA_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(e.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, e.smem) != cudaSuccess)
     return FA_ERR_CUDA;
@@ -144,7 +159,7 @@ int prepare_kernel(DeviceState* st, int idx, const fa::KernelEntry& e) {
   // setmaxnreg.inc would wait forever if the launch left fewer registers than the split needs
   if (attr.numRegs * fa::kThreads < fa::kRegBudgetPerCta || attr.maxThreadsPerBlock < fa::kThreads)
     return FA_ERR_UNSUPPORTED;
-  st->kernel_ready[idx] = true;
+  *ready = true;
   return FA_OK;
 }
 
@@ -409,13 +424,21 @@ int validate_common(int heads_q, int heads_kv, int d_qk, int d_v, float scale, c
   if (heads_q % heads_kv != 0) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale)) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (kernel_index(d_qk, d_v, 0, 0) < 0) return FA_ERR_UNSUPPORTED;
-  if (opt.pack < 0 || opt.grid < 0 || (opt.debug_flags & ~(fa::kDebugSkipPArrive | fa::kDebugCountRescale)) != 0)
+  if (opt.pack < 0 || opt.grid < 0 ||
+      (opt.debug_flags & ~(fa::kDebugSkipPArrive | fa::kDebugCountRescale | fa::kDebugChecks |
+                           fa::kDebugPlantBadTask)) != 0)
+    return FA_ERR_INVALID_ARG;
+  // the planted fault is for the checking build only
+  if ((opt.debug_flags & fa::kDebugPlantBadTask) && !(opt.debug_flags & fa::kDebugChecks)) return FA_ERR_INVALID_ARG;
+  if (opt.trace != nullptr &&
+      (opt.trace_ctas < 1 || opt.trace_cap < 1 || (reinterpret_cast<uintptr_t>(opt.trace) & 7u) != 0))
     return FA_ERR_INVALID_ARG;
   if (opt.exp_emu != 0 && opt.exp_emu != 1) return FA_ERR_INVALID_ARG;
   // the O-rescale counter is compiled into the FMA-exp2 kernels only
   if ((opt.debug_flags & fa::kDebugCountRescale) != 0 && opt.exp_emu != 1) return FA_ERR_UNSUPPORTED;
   if (opt.store_mode < 0 || opt.store_mode > 2) return FA_ERR_INVALID_ARG;
   if (opt.no_balance != 0 && opt.no_balance != 1) return FA_ERR_INVALID_ARG;
+  if (opt.stagger != 0 && opt.stagger != 1) return FA_ERR_INVALID_ARG;
   // the kept reference may lag the row maximum by up to tau (log2 units), so
   // unnormalised weights reach 2^tau: keep them far inside the fp32 range
   if (!(opt.tau >= 0.f && opt.tau <= 64.f)) return FA_ERR_INVALID_ARG;
@@ -458,6 +481,10 @@ void fa_options_default(fa_options* opts) {
   opts->workspace = nullptr;
   opts->store_mode = 0;
   opts->no_balance = 0;
+  opts->trace = nullptr;
+  opts->trace_ctas = 0;
+  opts->trace_cap = 0;
+  opts->stagger = 0;
 }
 
 int fa_version(void) { return 100; }
@@ -474,6 +501,8 @@ const char* fa_status_string(int status) {
       return "FA_ERR_CUDA";
     case FA_ERR_DEVICE_TIMEOUT:
       return "FA_ERR_DEVICE_TIMEOUT";
+    case FA_ERR_DEVICE_CHECK:
+      return "FA_ERR_DEVICE_CHECK";
     default:
       return "FA_ERR_UNKNOWN";
   }
@@ -543,10 +572,27 @@ static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float
                             : (opt.workspace != nullptr ? kVariantDyn
                                                         : (opt.exp_emu ? kVariantEmu
                                                                        : (direct ? kVariantDirect : kVariantFixed)));
+  // the build variants (event log, checks, stagger) exist for the fixed-length
+  // static modes only, one at a time
+  const int nvar = (opt.trace != nullptr ? 1 : 0) + ((opt.debug_flags & fa::kDebugChecks) ? 1 : 0) +
+                   (opt.stagger ? 1 : 0);
+  const int dbg = opt.trace != nullptr ? fa::kVarTrace
+                                       : ((opt.debug_flags & fa::kDebugChecks) ? fa::kVarCheck
+                                                                                : (opt.stagger ? fa::kVarStagger : 0));
+  if (dbg != 0 && (nvar > 1 || (variant != kVariantFixed && variant != kVariantDirect))) return FA_ERR_UNSUPPORTED;
   const int idx = kernel_index(d_qk, d_v, causal, variant);
   fa::KernelEntry entry;
-  if (idx < 0 || !get_entry(d_qk, d_v, causal, variant, &entry)) return FA_ERR_UNSUPPORTED;
-  rc = prepare_kernel(st, idx, entry);
+  bool* ready = nullptr;
+  if (dbg == 0) {
+    if (idx < 0 || !get_entry(d_qk, d_v, causal, variant, &entry)) return FA_ERR_UNSUPPORTED;
+    ready = &st->kernel_ready[idx];
+  } else {
+    if (idx < 0 || !get_debug_entry(d_qk, d_v, causal, variant, dbg, &entry)) return FA_ERR_UNSUPPORTED;
+    ready = &st->debug_ready[((idx / kVariants) * 2 + (variant == kVariantDirect ? 1 : 0)) * 3 +
+                             (dbg == fa::kVarTrace ? 0 : (dbg == fa::kVarCheck ? 1 : 2))];
+    if (opt.trace != nullptr && !is_device_ptr(opt.trace, dev)) return FA_ERR_INVALID_ARG;
+  }
+  rc = prepare_kernel(st, ready, entry);
   if (rc != FA_OK) return rc;
   const int64_t ctas = opt.grid > 0 ? opt.grid : st->sms;
   // balanced static order: without the mask the tiles of a partial last wave
@@ -568,11 +614,15 @@ static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float
   p.lse_bstride = static_cast<int64_t>(heads_q) * seqlen_q;
   p.o = static_cast<uint16_t*>(o);
   p.o_row_stride = static_cast<int64_t>(heads_q) * d_v;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   p.status = st->status;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.tau = opt.tau;
   p.timeout_ns = static_cast<unsigned long long>(opt.timeout_s * 1e9);
   p.debug_flags = opt.debug_flags;
+  p.trace = opt.trace;
+  p.trace_ctas = opt.trace_ctas;
+  p.trace_cap = opt.trace_cap;
 
   int64_t grid = ctas;
   if (grid > p.prob.num_tasks) grid = p.prob.num_tasks;
@@ -671,6 +721,8 @@ static int varlen_fwd(const void* q, const void* k, const void* v, void* o, floa
   int rc = validate_common(heads_q, heads_kv, d_qk, d_v, scale, opt);
   if (rc != FA_OK) return rc;
   if (opt.exp_emu != 0) return FA_ERR_UNSUPPORTED;  // the FMA-pipe exp2 is built for fixed-length batches only
+  // so are the debug builds
+  if (opt.trace != nullptr || (opt.debug_flags & fa::kDebugChecks) || opt.stagger) return FA_ERR_UNSUPPORTED;
   if (opt.workspace != nullptr) return FA_ERR_INVALID_ARG;  // varlen calls take their workspace as an argument
   if (batch == 0 || total_q == 0) return FA_OK;
   // TMA coordinates (row + 128) and the task count stay inside 32 bits
@@ -724,7 +776,7 @@ static int varlen_fwd(const void* q, const void* k, const void* v, void* o, floa
   const int idx = kernel_index(d_qk, d_v, causal, kVariantVarlen);
   fa::KernelEntry entry;
   if (idx < 0 || !get_entry(d_qk, d_v, causal, kVariantVarlen, &entry)) return FA_ERR_UNSUPPORTED;
-  rc = prepare_kernel(st, idx, entry);
+  rc = prepare_kernel(st, &st->kernel_ready[idx], entry);
   if (rc != FA_OK) return rc;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -750,6 +802,7 @@ static int varlen_fwd(const void* q, const void* k, const void* v, void* o, floa
   p.lse_bstride = 0;
   p.o = static_cast<uint16_t*>(o);
   p.o_row_stride = static_cast<int64_t>(heads_q) * d_v;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   int* count = static_cast<int*>(workspace);
   fa::VarlenTask* tasks =
       reinterpret_cast<fa::VarlenTask*>(static_cast<uint8_t*>(workspace) + kVarlenHeaderBytes);
@@ -859,7 +912,8 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (opt.grid < 0 || !std::isfinite(opt.timeout_s) || opt.timeout_s > 3600.0) return FA_ERR_INVALID_ARG;
   if ((opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
-  if (opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1) return FA_ERR_UNSUPPORTED;
+  if (opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1 || opt.trace != nullptr || opt.stagger)
+    return FA_ERR_UNSUPPORTED;
   if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return FA_ERR_UNSUPPORTED;
   if (batch == 0) return FA_OK;
   const int64_t big = int64_t(1) << 31;
@@ -984,7 +1038,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                    scale, workspace, workspace_bytes, nullptr, stream);
 }
 
-int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]) {
+int fa_device_status(fa_stream_t stream, int* out) { return fa_device_status_detail(stream, out, nullptr); }
+
+int fa_device_status_detail(fa_stream_t stream, int* out, unsigned int detail[3]) {
   if (out == nullptr) return FA_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -996,7 +1052,10 @@ int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]) {
   if (cudaMemcpy(w, st->status, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaMemset(st->status, 0, sizeof(w)) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
-  *out = w[0] == 0 ? FA_OK : (w[0] == fa::kStatusTimeout ? FA_ERR_DEVICE_TIMEOUT : static_cast<int>(w[0]));
+  *out = w[0] == 0 ? FA_OK
+                   : (w[0] == fa::kStatusTimeout ? FA_ERR_DEVICE_TIMEOUT
+                                                 : (w[0] == fa::kStatusCheck ? FA_ERR_DEVICE_CHECK
+                                                                             : static_cast<int>(w[0])));
   if (detail) {
     detail[0] = w[0];
     detail[1] = w[1];

@@ -53,6 +53,25 @@
 // Every wait is bounded (see ptx.cuh); on a timeout the CTA records the
 // failing site in the status word, every role leaves its loop, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed.
+//
+// Build variants (template argument VAR, fixed-length and direct epilogue
+// modes only; the default kernels compile none of this code):
+//   VAR & kVarTrace    an event log: lane 0 of each role's first warp stamps
+//                      clock64 at the hand-offs of the protocol (waits and
+//                      arrivals only, so the softmax's instruction schedule
+//                      between them is untouched) into a caller buffer (one
+//                      track per role and CTA).
+//   VAR & kVarStagger  an ablation: the two softmax warpgroups take turns
+//                      for their exponentials ("FlashAttention-4 wiki", "Core
+//                      methods": the staggered exp sections of S0 and S1).
+//   VAR & kVarCheck  device-side checks: every decoded task, TMA coordinate,
+//                    TMEM base and lane quadrant, shared-memory extent and
+//                    epilogue store index is checked before use, and at exit
+//                    the roles' counts of every hand-off (tiles loaded and
+//                    consumed, S commits and waits, P arrivals and waits,
+//                    O-done commits and waits) must agree.  A failed check
+//                    records FA_ERR_DEVICE_CHECK and its site in the status
+//                    word, skips the access and aborts the CTA like a timeout.
 #pragma once
 #include <cuda.h>
 
@@ -86,6 +105,13 @@ constexpr int kTaskReaders = 13; // arrivals that free a ring slot: MMA warp + 1
 // debug_flags bits
 constexpr int kDebugSkipPArrive = 1;  // softmax never arrives on p_full: exercises the bounded waits
 constexpr int kDebugCountRescale = 2; // count the correction warps' O round trips in status word 3
+constexpr int kDebugChecks = 4;       // run the checking instantiation (VAR & kVarCheck)
+constexpr int kDebugPlantBadTask = 8; // checking instantiation: task 0 decodes to batch B (out of range)
+
+// VAR template bits (build variants)
+constexpr int kVarTrace = 1;
+constexpr int kVarCheck = 2;
+constexpr int kVarStagger = 4;
 
 struct Params {
   CUtensorMap tm_q;  // 5-D view (d, pack, groups, Sq, B) of q (varlen: S = total_q rows, B = 1)
@@ -96,6 +122,7 @@ struct Params {
   int64_t lse_bstride, lse_hstride;  // element strides of lse per batch and per head
   uint16_t* o;                       // o (bf16 bits): direct stores of ragged varlen tiles
   int64_t o_row_stride;              // elements between consecutive positions of o (Hq * dv)
+  int o_align32;                     // o is 32-byte aligned: direct stores of 32 bytes
   const VarlenTask* vtasks;          // varlen: the planned task list
   const int* vtask_count;            // varlen: its length
   unsigned int* sched_next;          // DYN: next task index (cleared before the launch)
@@ -107,6 +134,9 @@ struct Params {
   float tau;         // conditional-rescale threshold, log2 units
   unsigned long long timeout_ns;
   int debug_flags;
+  uint64_t* trace;   // VAR & kVarTrace: [trace_ctas][kTraceTracks][1 + trace_cap] words
+  int trace_ctas;    // CTAs 0 .. trace_ctas-1 record
+  int trace_cap;     // records kept per track
 };
 
 template <int DQ, int DV>
@@ -140,7 +170,8 @@ struct Layout {
   static constexpr int bODone = bPFull + 2;
   static constexpr int bCorrFull = bODone + 2;
   static constexpr int bFinFull = bCorrFull + 2;  // final row_sum / reference posted (count 128)
-  static constexpr int bEpiFull = bFinFull + 2;  // WG2: staging tile written (count 128)
+  static constexpr int bStagger = bFinFull + 2;   // [2] (VAR & kVarStagger) stage s finished its exps (count 128)
+  static constexpr int bEpiFull = bStagger + 2;   // WG2: staging tile written (count 128)
   static constexpr int bStageFree = bEpiFull + 1; // WG2: TMA store finished reading staging (count 1)
   static constexpr int bDrain = bStageFree + 1;   // MMA drain at exit
   static constexpr int bTaskFull = bDrain + 1;               // [kTaskRing] (DYN) count 1
@@ -149,7 +180,8 @@ struct Layout {
 
   static constexpr int oMisc = oBar + kNumBars * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int oTaskRing = oMisc + 16;       // int[kTaskRing] (DYN)
-  static constexpr int kBytes = oTaskRing + 4 * kTaskRing;
+  static constexpr int oDbgCount = oTaskRing + 4 * kTaskRing;  // uint32[kDbgCounts] (VAR & kVarCheck)
+  static constexpr int kBytes = oDbgCount + 4 * 24;
   static constexpr int kDynSmem = kBytes + 1024;     // slack to align the base to 1024 B
   static_assert(kDynSmem <= kMaxSmem, "shared memory budget");
 };
@@ -158,6 +190,7 @@ struct Layout {
 enum : unsigned int {
   kSiteSoftmaxS = 101,
   kSiteSoftmaxTask = 102,
+  kSiteSoftmaxStagger = 103,
   kSiteCorrCorr = 201,
   kSiteCorrODone = 202,
   kSiteCorrEpiFull = 203,
@@ -275,6 +308,133 @@ __device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, c
 }
 
 // ---------------------------------------------------------------------------
+// debug instantiations: the event log and the checks
+// ---------------------------------------------------------------------------
+// Event log: track = role (softmax stage 0, softmax stage 1, correction, MMA,
+// TMA); a record is one 64-bit word {code (bits 56-63), argument (bits
+// 32-55), clock64 low 32 bits}.  Word 0 of a track holds its record count
+// (records past trace_cap are counted, not kept).
+constexpr int kTraceTracks = 5;
+enum : uint32_t {
+  // softmax (argument: block j; task: task index)
+  kEvSmTask = 1, kEvSmWait = 2, kEvSmS = 3, kEvSmLd = 4, kEvSmMax = 5, kEvSmExp0 = 6, kEvSmExp1 = 7, kEvSmP = 8,
+  // correction (argument: stage << 16 | block, or stage)
+  kEvCoTask = 16, kEvCoCorr = 17, kEvCoRescaled = 18, kEvCoArrive = 19, kEvCoODone = 20, kEvCoEpi = 21,
+  // MMA (argument: ring tile, stage, or stage << 16 | block)
+  kEvMmTask = 32, kEvMmKv = 33, kEvMmQ = 34, kEvMmP = 35, kEvMmPV = 36, kEvMmQK = 37,
+  // TMA (argument: stage or ring tile)
+  kEvLdTask = 48, kEvLdQ = 49, kEvLdKvWait = 50, kEvLdKv = 51,
+};
+
+// Keeps two registers per recording role (the record count and the on
+// flag; a third for the track when TRACK < 0, i.e. chosen at run time): the
+// track's address is recomputed from the kernel parameters, which live in
+// parameter space, at each record.
+template <bool ON, int TRACK>
+struct Tracer {
+  uint32_t n = 0;
+  bool on = false;
+  int track = TRACK;
+  __device__ __forceinline__ void init(const Params& p, bool recorder, int trk = TRACK) {
+    if constexpr (ON) {
+      on = recorder && p.trace != nullptr && static_cast<int>(blockIdx.x) < p.trace_ctas;
+      if constexpr (TRACK < 0) track = trk;
+    }
+  }
+  __device__ __forceinline__ uint64_t* base(const Params& p) const {
+    const int tr = TRACK < 0 ? track : TRACK;
+    return p.trace + (static_cast<int64_t>(blockIdx.x) * kTraceTracks + tr) * (p.trace_cap + 1);
+  }
+  __device__ __forceinline__ void ev(const Params& p, uint32_t code, uint32_t arg) {
+    if constexpr (ON) {
+      if (on) {
+        if (n < static_cast<uint32_t>(p.trace_cap))
+          base(p)[1 + n] = (static_cast<uint64_t>(code) << 56) | (static_cast<uint64_t>(arg & 0xFFFFFFu) << 32) |
+                           static_cast<uint32_t>(clock64());
+        ++n;
+      }
+    }
+  }
+  __device__ __forceinline__ void finish(const Params& p) {
+    if constexpr (ON) {
+      if (on) base(p)[0] = n;
+    }
+  }
+};
+
+// Hand-off counts each role keeps in the checking build (slots of the shared
+// counter area, written by one lane at exit and compared by thread 0).
+enum : int {
+  kCntLdKv = 0, kCntLdQ = 1,                   // [2]: tiles / Q tiles loaded
+  kCntMmKv = 3, kCntMmQ = 4,                   // [2]: tiles / Q tiles consumed
+  kCntMmS = 6, kCntMmP = 8, kCntMmODone = 10,  // [2] each: S commits, P waits, O-done commits
+  kCntSmS = 12, kCntSmP = 14,                  // [2] each: S waits, P arrivals
+  kCntCoCorr = 16, kCntCoP = 18, kCntCoODone = 20,  // [2] each
+  kNumCounts = 22
+};
+static_assert(kNumCounts <= 24, "counter area");
+
+template <bool ON>
+struct Counts {
+  uint32_t c[ON ? kNumCounts : 1] = {};
+  __device__ __forceinline__ void inc(int i) {
+    if constexpr (ON) ++c[i];
+  }
+  __device__ __forceinline__ void add(int i, uint32_t v) {
+    if constexpr (ON) c[i] += v;
+  }
+  // store slots [lo, hi) (one lane)
+  __device__ __forceinline__ void store(uint32_t* area, int lo, int hi, bool writer) const {
+    if constexpr (ON) {
+      if (writer)
+        for (int i = lo; i < hi; ++i) area[i] = c[i];
+    }
+  }
+};
+
+// Check sites recorded with FA_ERR_DEVICE_CHECK
+enum : unsigned int {
+  kSiteCheckTask = 601,      // a decoded task outside the problem
+  kSiteCheckQCoord = 602,    // a Q tile coordinate outside the tensor
+  kSiteCheckKvCoord = 603,   // a K/V tile coordinate outside the tensor
+  kSiteCheckSmem = 604,      // the shared-memory layout past the launch's dynamic size
+  kSiteCheckTmem = 605,      // TMEM base not at lane 0 / column 0, or a lane quadrant off its warp
+  kSiteCheckOStore = 606,    // an output row or tile outside O
+  kSiteCheckLse = 607,       // an LSE index outside lse
+  kSiteCheckCounts = 610,    // + i: the i-th hand-off count comparison failed
+};
+
+__device__ __forceinline__ bool dbg_check(bool ok, const WaitCtx& wc, unsigned site) {
+  if (!ok) raise_abort(wc, kStatusCheck, site);
+  return ok;
+}
+
+// Is a decoded fixed-length task inside the problem?
+__device__ __forceinline__ bool task_in_problem(const Problem& pr, const Task& tk) {
+  const int kb = (tk.kend + kBN - 1) / kBN;
+  bool ok = tk.bc >= 0 && tk.bc < pr.B && tk.g >= 0 && tk.g < pr.groups && tk.kvh >= 0 && tk.kvh < pr.Hkv &&
+            tk.q_row0 >= 0 && tk.k_row0 >= 0 && tk.nmax == max(tk.n[0], tk.n[1]) && tk.sq == pr.Sq;
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+    ok = ok && tk.n[s] >= 0 && tk.n[s] <= kb && tk.pos0[s] >= 0 && (tk.n[s] == 0 || tk.pos0[s] < tk.sq);
+  if (tk.ksplit != 0) ok = ok && tk.ksplit == tk.n[0] && tk.n[0] + tk.n[1] <= kb;
+  return ok;
+}
+
+// The checking build's view of a decoded task: the planted fault (debug
+// flag), then the range check.  Warp-uniform (every lane decodes the same
+// task).  Returns false after recording the failure.
+template <bool CK>
+__device__ __forceinline__ bool check_task(const Params& p, Task& tk, int task, const WaitCtx& wc) {
+  if constexpr (CK) {
+    if ((p.debug_flags & kDebugPlantBadTask) && task == 0) tk.bc = p.prob.B;
+    return dbg_check(task_in_problem(p.prob, tk), wc, kSiteCheckTask);
+  } else {
+    return true;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // 2^x on the FMA pipe ("FlashAttention-4 wiki", "Core methods": Cody-Waite
 // range reduction and a degree-3 Horner polynomial, the integer part added to
 // the exponent field).  x = j + f with j = rint(x) (adding 1.5 * 2^23 rounds
@@ -311,11 +471,12 @@ __device__ __forceinline__ void ex2_fma_x2(uint64_t x2, float& y0, float& y1) {
 // ---------------------------------------------------------------------------
 // EMU: one in four exponentials of unmasked blocks on the FMA pipe (an option;
 // its own instantiation, so the default kernel carries no extra code)
-template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN, bool SPLIT, bool FD>
+template <int DQ, int DV, bool CAUSAL, bool EMU, bool VARLEN, bool DYN, bool SPLIT, bool FD, int VAR>
 __device__ __forceinline__ void softmax_role(const Params& p, const int stage, const uint32_t tmem,
                                              const uint32_t sbase, float* mbox, const volatile int* ring,
-                                             const WaitCtx& wc) {
+                                             uint32_t* dbg_area, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
+  constexpr bool CK = (VAR & kVarCheck) != 0;
   const Problem& pr = p.prob;
   const int t = threadIdx.x - stage * 128;  // row of the Q tile == TMEM lane
   const uint32_t tS = tmem + (static_cast<uint32_t>(t & ~31) << 16) + static_cast<uint32_t>(stage * 128);
@@ -323,6 +484,8 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   const uint32_t bar_corr = sbase + L::oBar + 8 * (L::bCorrFull + stage);
   const uint32_t bar_p = sbase + L::oBar + 8 * (L::bPFull + stage);
   const uint32_t bar_fin = sbase + L::oBar + 8 * (L::bFinFull + stage);
+  constexpr bool STAG = (VAR & kVarStagger) != 0;
+  uint32_t stag_k = 0;  // staggered blocks of this stage so far (STAG)
   float* mb_acc = mbox + (stage * 3 + 0) * 128;
   float* mb_sum = mbox + (stage * 3 + 1) * 128;
   float* mb_ref = mbox + (stage * 3 + 2) * 128;
@@ -331,11 +494,19 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   const bool skip_p = (p.debug_flags & kDebugSkipPArrive) != 0;
   uint32_t phase = 0;
   const int num_tasks = task_count<VARLEN>(p);
+  Tracer<(VAR & kVarTrace) != 0, -1> tr;  // track = stage
+  tr.init(p, t == 0, stage);
+  Counts<CK> cnt;
+  if constexpr (CK) {  // this warp's TMEM lane quadrant is (warp % 4)
+    if (!dbg_check((t & ~31) == 32 * ((threadIdx.x >> 5) & 3), wc, kSiteCheckTmem)) return;
+  }
 
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, sbase + L::oBar, ring, wc, kSiteSoftmaxTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    if (!check_task<CK>(p, tk, task, wc)) break;
+    tr.ev(p, kEvSmTask, static_cast<uint32_t>(task));
     const int n = stage ? tk.n[1] : tk.n[0];
     if (n == 0) continue;
     const int pos0 = stage ? tk.pos0[1] : tk.pos0[0];
@@ -358,10 +529,16 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
     float ref = 0.f;            // row_max * scale_log2 (0 while the row is empty)
 
     for (int j = 0; j < n; ++j) {
+      tr.ev(p, kEvSmWait, static_cast<uint32_t>(j));
       const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_s, phase, wc, kSiteSoftmaxS));
-      if (!ok) return;
+      if (!ok) {
+        tr.finish(p);
+        return;
+      }
       phase ^= 1u;
+      cnt.inc(kCntSmS + stage);
       tc_fence_after();
+      tr.ev(p, kEvSmS, static_cast<uint32_t>(j));
 
       uint32_t r[128];
       tmem_ld128_wait(tS, r);
@@ -443,11 +620,32 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
           tmem_st32(tS + static_cast<uint32_t>(32 * half), pk);
         }
       };
+      // staggered exponential sections (ablation): in the blocks both stages
+      // visit, stage 1 starts its exponentials after stage 0 finished those of
+      // the same block, and stage 0 after stage 1 finished those of the
+      // previous such block
+      const bool staggered = STAG && j < min(tk.n[0], tk.n[1]);
+      if constexpr (STAG) {
+        if (staggered && (stage == 1 || stag_k > 0)) {
+          const uint32_t other = sbase + L::oBar + 8 * (L::bStagger + (stage ^ 1));
+          const uint32_t par = (stage == 1 ? stag_k : stag_k - 1u) & 1u;
+          if (!__all_sync(0xffffffffu, mbar_wait(other, par, wc, kSiteSoftmaxStagger))) {
+            tr.finish(p);
+            return;
+          }
+        }
+      }
       if constexpr (EMU) {
         if (!masked_block) exps(std::true_type{});
         else exps(std::false_type{});
       } else {
         exps(std::false_type{});
+      }
+      if constexpr (STAG) {
+        if (staggered) {
+          mbar_arrive(sbase + L::oBar + 8 * (L::bStagger + stage));
+          ++stag_k;
+        }
       }
       tmem_wait_st();
       float sa0, sa1;
@@ -460,8 +658,17 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
         mbar_arrive(bar_fin);
       }
       tc_fence_before();
-      if (!skip_p) mbar_arrive(bar_p);
+      if (!skip_p) {
+        mbar_arrive(bar_p);
+        cnt.inc(kCntSmP + stage);
+      }
+      tr.ev(p, kEvSmP, static_cast<uint32_t>(j));
     }
+  }
+  tr.finish(p);
+  if (!*wc.abort_flag) {
+    cnt.store(dbg_area, kCntSmS + stage, kCntSmS + stage + 1, t == 0);
+    cnt.store(dbg_area, kCntSmP + stage, kCntSmP + stage + 1, t == 0);
   }
 }
 
@@ -471,11 +678,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 // COUNT: the FMA-exp2 ablation kernel also counts O rescales (debug_flags bit
 // 1); the rescale decisions do not depend on how the exponentials are taken,
 // and the default kernels carry no counting code.
-template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool DIRECT, bool COUNT>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool DIRECT, bool COUNT, int VAR>
 __device__ __forceinline__ void correction_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                                 uint8_t* smem, float* mbox, const volatile int* ring,
-                                                const WaitCtx& wc) {
+                                                uint32_t* dbg_area, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
+  constexpr bool CK = (VAR & kVarCheck) != 0;
   constexpr bool TS = !CAUSAL && !VARLEN && !DYN && !SPLIT;  // key-split tail tasks possible
   const Problem& pr = p.prob;
   const int t = threadIdx.x - 256;  // row == TMEM lane
@@ -488,11 +696,20 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   uint32_t od_count[2] = {0u, 0u};  // o_done phases consumed (one per task with blocks)
   uint32_t chunks = 0;              // epilogue chunks stored through the staging tile so far
   const int num_tasks = task_count<VARLEN>(p);
+  Tracer<(VAR & kVarTrace) != 0, 2> tr;
+  tr.init(p, t == 0);
+  Counts<CK> cnt;
+  if constexpr (CK) {  // this warp's TMEM lane quadrant is (warp % 4)
+    if (!__all_sync(0xffffffffu, dbg_check((t & ~31) == 32 * ((threadIdx.x >> 5) & 3), wc, kSiteCheckTmem)))
+      goto out;
+  }
 
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteCorrTask);
     if (task < 0) break;  // no task left, or an abort
     Task tk = get_task<VARLEN, SPLIT, CAUSAL, DIRECT, !DYN>(p, task);
+    if (!check_task<CK>(p, tk, task, wc)) break;
+    tr.ev(p, kEvCoTask, static_cast<uint32_t>(task));
     float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
 
     for (int j = 0; j < tk.nmax; ++j) {
@@ -503,6 +720,8 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
                              mbar_wait(bar0 + 8 * (L::bCorrFull + s), corr_phase[s], wc, kSiteCorrCorr));
         if (!ok) goto out;
         corr_phase[s] ^= 1u;
+        cnt.inc(kCntCoCorr + s);
+        tr.ev(p, kEvCoCorr, static_cast<uint32_t>(s << 16 | j));
         const float acc = mbox[(s * 3 + 0) * 128 + t];
         // warp-uniform skip of the O round trip when no row moved its
         // reference.  The softmax posted acc_scale after S_j was ready, and S_j
@@ -522,6 +741,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
             tmem_st32(tO + c, r);
           }
           tmem_wait_st();
+          tr.ev(p, kEvCoRescaled, static_cast<uint32_t>(s << 16 | j));
         }
         if (j == tk.n[s] - 1) {  // last block: the final row sum and reference
           ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bFinFull + s), fin_phase[s], wc, kSiteCorrFin));
@@ -532,6 +752,8 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         }
         tc_fence_before();
         mbar_arrive(bar0 + 8 * (L::bPFull + s));
+        cnt.inc(kCntCoP + s);
+        tr.ev(p, kEvCoArrive, static_cast<uint32_t>(s << 16 | j));
       }
     }
 
@@ -561,6 +783,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         if (!ok) goto out;
         ++od_count[s];
         tc_fence_after();
+        tr.ev(p, kEvCoODone, static_cast<uint32_t>(s));
       }
       float inv = 0.f, lse = -INFINITY;
       float inv1 = 0.f;  // merge: weight of stage 1's O
@@ -617,6 +840,12 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         continue;
       }
       uint4* out_row = nullptr;
+      if constexpr (CK) {  // the row this lane stores lies inside O
+        const bool in_o = !direct || pos >= tk.sq ||
+                          (static_cast<int64_t>(tk.bc) * tk.sq + tk.q_row0 + pos < static_cast<int64_t>(pr.B) * pr.Sq &&
+                           head >= 0 && head < pr.Hq);
+        if (!__all_sync(0xffffffffu, dbg_check(in_o, wc, kSiteCheckOStore))) goto out;
+      }
       if (direct && pos < tk.sq)
         out_row = reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(tk.bc) * tk.sq + tk.q_row0 + pos) *
                                                      p.o_row_stride +
@@ -651,18 +880,29 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0u;
           }
+          uint4 v[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * mul, __uint_as_float(r[8 * q + 1]) * mul);
-            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * mul, __uint_as_float(r[8 * q + 3]) * mul);
-            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * mul, __uint_as_float(r[8 * q + 5]) * mul);
-            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * mul, __uint_as_float(r[8 * q + 7]) * mul);
-            if (direct) {
-              if (out_row != nullptr) out_row[c * 8 + half * 4 + q] = v;
-            } else {
-              row[(half * 4 + q) ^ (t & 7)] = v;  // 128-byte swizzle of the TMA box
+            v[q].x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * mul, __uint_as_float(r[8 * q + 1]) * mul);
+            v[q].y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * mul, __uint_as_float(r[8 * q + 3]) * mul);
+            v[q].z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * mul, __uint_as_float(r[8 * q + 5]) * mul);
+            v[q].w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * mul, __uint_as_float(r[8 * q + 7]) * mul);
+          }
+          if (direct) {
+            // a row's 64 bytes of this half: whole 32-byte sectors when O allows it
+            if (out_row != nullptr) {
+              uint4* dst = out_row + c * 8 + half * 4;
+              if (p.o_align32) {
+                st_global_v8(dst, v[0], v[1]);
+                st_global_v8(dst + 2, v[2], v[3]);
+              } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) dst[q] = v[q];
+              }
             }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) row[(half * 4 + q) ^ (t & 7)] = v[q];  // 128-byte swizzle of the TMA box
           }
         }
         if (direct) continue;
@@ -671,6 +911,10 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         bool stored = true;
         if (t == 0) {
           stored = mbar_wait(bar0 + 8 * L::bEpiFull, chunks & 1u, wc, kSiteCorrEpiFull);
+          if constexpr (CK)  // the stored tile starts inside O
+            stored = stored && dbg_check(tk.q_row0 + pos0 >= 0 && tk.q_row0 + pos0 < pr.Sq && tk.g >= 0 &&
+                                             tk.g < pr.groups && tk.bc >= 0 && tk.bc < pr.B,
+                                         wc, kSiteCheckOStore);
           if (stored) {
             tma_store_5d(&p.tm_o, staging_s, c * 64, 0, tk.g, tk.q_row0 + pos0, tk.bc);
             bulk_commit_group();
@@ -683,12 +927,28 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
         ++chunks;
         if (!stored) goto out;
       }
-      if (p.lse != nullptr && pos < tk.sq)
-        p.lse[tk.b * p.lse_bstride + head * p.lse_hstride + tk.q_row0 + pos] = lse;
+      if (p.lse != nullptr && pos < tk.sq) {
+        const int64_t li = tk.b * p.lse_bstride + head * p.lse_hstride + tk.q_row0 + pos;
+        bool ok = true;
+        if constexpr (CK) ok = dbg_check(li >= 0 && li < static_cast<int64_t>(pr.B) * pr.Hq * pr.Sq, wc, kSiteCheckLse);
+        if (ok) p.lse[li] = lse;
+      }
+      tr.ev(p, kEvCoEpi, static_cast<uint32_t>(s));
     }
   }
 out:
   if (t == 0) bulk_wait_group0();
+  tr.finish(p);
+  if (!*wc.abort_flag) {
+    cnt.store(dbg_area, kCntCoCorr, kCntCoCorr + 2, t == 0);
+    cnt.store(dbg_area, kCntCoP, kCntCoP + 2, t == 0);
+    if constexpr (CK) {
+      if (t == 0) {
+        dbg_area[kCntCoODone] = od_count[0];
+        dbg_area[kCntCoODone + 1] = od_count[1];
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -727,10 +987,11 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 // o_done[s] is committed once per task, after the stage's last P V: inside a
 // task, "S_j ready" already implies that P V_{j-1} has completed (a commit
 // tracks every earlier MMA of the issuing thread).
-template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool FD>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool FD, int VAR>
 __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
-                                         const volatile int* ring, const WaitCtx& wc) {
+                                         const volatile int* ring, uint32_t* dbg_area, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
+  constexpr bool CK = (VAR & kVarCheck) != 0;
   constexpr bool TS = !CAUSAL && !VARLEN && !DYN && !SPLIT;  // key-split tail tasks possible
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -740,13 +1001,18 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   uint32_t kv_it = 0;  // first ring tile of the current task
   constexpr bool kEarlyV = L::NS <= 3;
   const uint32_t leader = (threadIdx.x & 31) == 0 ? 1u : 0u;  // the lane that issues MMAs and commits
+  Tracer<(VAR & kVarTrace) != 0, 3> tr;
+  tr.init(p, leader != 0);
+  Counts<CK> cnt;
   // every lane waits; a timeout seen by any lane ends the role for the whole warp
   auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
   };
   // full / empty barriers of ring tile `it`
   auto wait_tile = [&](uint32_t it) {
-    return wait(bar(L::bKvFull + static_cast<int>(it % L::NS)), (it / L::NS) & 1u, kSiteMmaKv);
+    const bool ok = wait(bar(L::bKvFull + static_cast<int>(it % L::NS)), (it / L::NS) & 1u, kSiteMmaKv);
+    tr.ev(p, kEvMmKv, it);
+    return ok;
   };
   auto release_tile = [&](uint32_t it) { mma_commit(bar(L::bKvEmpty + static_cast<int>(it % L::NS)), leader); };
 
@@ -763,7 +1029,9 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteMmaTask);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = kPre ? nxt : get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    Task tk = kPre ? nxt : get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    if (!check_task<CK>(p, tk, task, wc)) break;
+    tr.ev(p, kEvMmTask, static_cast<uint32_t>(task));
     // decode task kt + 1 (called once the first Q K^T of task kt are issued)
     auto pre_next = [&]() {
       if constexpr (kPre) {
@@ -783,9 +1051,13 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
         if (!wait_tile(it)) goto out;
         if (!wait(bar(L::bQFull + s), q_phase[s], kSiteMmaQ)) goto out;
         q_phase[s] ^= 1u;
+        cnt.inc(kCntMmQ + s);
         tc_fence_after();
+        tr.ev(p, kEvMmQ, static_cast<uint32_t>(s));
         issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(it), leader);
         mma_commit(bar(L::bSFull + s), leader);
+        cnt.inc(kCntMmS + s);
+        tr.ev(p, kEvMmQK, static_cast<uint32_t>(s << 16));
         if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
         release_tile(it++);
       }
@@ -797,17 +1069,25 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
           if (!wait_tile(it)) goto out;
           if (!wait(bar(L::bPFull + s), p_phase[s], kSiteMmaP)) goto out;
           p_phase[s] ^= 1u;
+          cnt.inc(kCntMmP + s);
           tc_fence_after();
+          tr.ev(p, kEvMmP, static_cast<uint32_t>(s << 16 | j));
           issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
                             slot_addr(it), 0, j > 0, leader);
           issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
                             slot_addr(it), 1, true, leader);
-          if (j + 1 == tk.n[s]) mma_commit(bar(L::bODone + s), leader);
+          tr.ev(p, kEvMmPV, static_cast<uint32_t>(s << 16 | j));
+          if (j + 1 == tk.n[s]) {
+            mma_commit(bar(L::bODone + s), leader);
+            cnt.inc(kCntMmODone + s);
+          }
           release_tile(it++);
           if (j + 1 < tk.n[s]) {
             if (!wait_tile(it)) goto out;
             issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(it), leader);
             mma_commit(bar(L::bSFull + s), leader);
+            cnt.inc(kCntMmS + s);
+            tr.ev(p, kEvMmQK, static_cast<uint32_t>(s << 16 | (j + 1)));
             if (j + 2 == tk.n[s]) mma_commit(bar(L::bQEmpty + s), leader);
             release_tile(it++);
           }
@@ -829,9 +1109,13 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
       if (tk.n[s] == 0) continue;
       if (!wait(bar(L::bQFull + s), q_phase[s], kSiteMmaQ)) goto out;
       q_phase[s] ^= 1u;
+      cnt.inc(kCntMmQ + s);
       tc_fence_after();
+      tr.ev(p, kEvMmQ, static_cast<uint32_t>(s));
       issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(base), leader);
       mma_commit(bar(L::bSFull + s), leader);
+      cnt.inc(kCntMmS + s);
+      tr.ev(p, kEvMmQK, static_cast<uint32_t>(s << 16));
       if (tk.n[s] == 1) mma_commit(bar(L::bQEmpty + s), leader);
     }
     release_tile(base);  // K_0, once both Q K^T have finished
@@ -847,12 +1131,18 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
         if (j >= tk.n[s]) continue;
         if (!wait(bar(L::bPFull + s), p_phase[s], kSiteMmaP)) goto out;
         p_phase[s] ^= 1u;
+        cnt.inc(kCntMmP + s);
         tc_fence_after();
+        tr.ev(p, kEvMmP, static_cast<uint32_t>(s << 16 | j));
         issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
                           slot_addr(v_it), 0, j > 0, leader);
         issue_pv_half<DV>(tmem + 256u + static_cast<uint32_t>(s * 128), tmem + static_cast<uint32_t>(s * 128),
                           slot_addr(v_it), 1, true, leader);
-        if (j + 1 == tk.n[s]) mma_commit(bar(L::bODone + s), leader);
+        tr.ev(p, kEvMmPV, static_cast<uint32_t>(s << 16 | j));
+        if (j + 1 == tk.n[s]) {
+          mma_commit(bar(L::bODone + s), leader);
+          cnt.inc(kCntMmODone + s);
+        }
         // with a shallow ring (d_qk = 192: two slots) V_j's slot is released
         // by the last P V that reads it, so that V_{j+1} can be loaded while
         // the next Q K^T runs; with a deeper ring the release waits for the
@@ -867,6 +1157,8 @@ __device__ __forceinline__ void mma_role(const Params& p, const uint32_t tmem, c
           }
           issue_qk<DQ, DV>(tmem + static_cast<uint32_t>(s * 128), q_addr(s), slot_addr(k_it), leader);
           mma_commit(bar(L::bSFull + s), leader);
+          cnt.inc(kCntMmS + s);
+          tr.ev(p, kEvMmQK, static_cast<uint32_t>(s << 16 | (j + 1)));
           if (j + 2 == tk.n[s]) mma_commit(bar(L::bQEmpty + s), leader);
         }
       }
@@ -879,15 +1171,24 @@ out:
   // every MMA issued by the leader lane has completed once the drain barrier fires
   mma_commit(bar(L::bDrain), leader);
   mbar_drain_wait(bar(L::bDrain), 0u, wc, kSiteMmaDrain);
+  tr.finish(p);
+  if (!*wc.abort_flag) {
+    cnt.add(kCntMmKv, kv_it);
+    cnt.store(dbg_area, kCntMmKv, kCntMmODone + 2, leader != 0);
+  }
 }
 
 // ---------------------------------------------------------------------------
 // TMA loads (warp 13, one thread)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool FD>
+template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool FD, int VAR>
 __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase, volatile int* ring,
-                                          const WaitCtx& wc) {
+                                          uint32_t* dbg_area, const WaitCtx& wc) {
   using L = Layout<DQ, DV>;
+  constexpr bool CK = (VAR & kVarCheck) != 0;
+  const Problem& pr = p.prob;
+  Tracer<(VAR & kVarTrace) != 0, 4> tr;
+  tr.init(p, true);
   constexpr bool TS = !CAUSAL && !VARLEN && !DYN && !SPLIT;  // key-split tail tasks possible
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -902,27 +1203,42 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
   for (int kt = 0;; ++kt) {
     const int task = post_task<DQ, DV, DYN>(p, kt, num_tasks, bar0, ring, wc);
     if (task < 0) break;  // no task left, or an abort
-    const Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    Task tk = get_task<VARLEN, SPLIT, CAUSAL, FD, !DYN>(p, task);
+    if (!check_task<CK>(p, tk, task, wc)) break;
+    tr.ev(p, kEvLdTask, static_cast<uint32_t>(task));
     if (tk.nmax == 0) continue;
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       if (tk.n[s] == 0) continue;
       if (q_uses[s] > 0 && !mbar_wait(bar(L::bQEmpty + s), (q_uses[s] - 1u) & 1u, wc, kSiteLoadQ)) goto out;
+      if constexpr (CK) {  // the Q tile starts inside q
+        const int row = tk.q_row0 + tk.pos0[s];
+        if (!dbg_check(row >= 0 && row < pr.Sq && tk.g >= 0 && tk.g < pr.groups && tk.bc >= 0 && tk.bc < pr.B, wc,
+                       kSiteCheckQCoord))
+          goto out;
+      }
       const uint32_t qb = bar(L::bQFull + s);
       mbar_arrive_expect_tx(qb, L::NQC * kChunkBytes);
       const uint32_t dst = sbase + L::oQ + static_cast<uint32_t>(s * L::kQBytes);
       for (int c = 0; c < L::NQC; ++c)
         tma_load_5d(dst + c * kChunkBytes, &p.tm_q, qb, c * 64, 0, tk.g, tk.q_row0 + tk.pos0[s], tk.bc);
       ++q_uses[s];
+      tr.ev(p, kEvLdQ, static_cast<uint32_t>(s));
     }
     if constexpr (TS) {
       if (tk.ksplit != 0) {  // key-split tail task: the order the MMA warp reads
         // the next ring tile: K (which = 0) or V (1) of the block at key row `row`
         auto issue_tile = [&](int which, int row) -> bool {
           const uint32_t slot = kv_it % L::NS;
+          tr.ev(p, kEvLdKvWait, kv_it);
           if (kv_it >= static_cast<uint32_t>(L::NS) &&
               !mbar_wait(bar(L::bKvEmpty + static_cast<int>(slot)), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
             return false;
+          if constexpr (CK) {  // the K/V tile starts inside k / v
+            if (!dbg_check(row >= 0 && row < pr.Sk && tk.kvh >= 0 && tk.kvh < pr.Hkv && tk.bc >= 0 && tk.bc < pr.B,
+                           wc, kSiteCheckKvCoord))
+              return false;
+          }
           const uint32_t fb = bar(L::bKvFull + static_cast<int>(slot));
           const uint32_t dst = sbase + L::oRing + slot * L::kSlotBytes;
           const int nch = which == 0 ? L::NQC : L::NVC;
@@ -930,6 +1246,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
           for (int c = 0; c < nch; ++c)
             tma_load_4d(dst + c * kChunkBytes, which == 0 ? static_cast<const void*>(&p.tm_k) : &p.tm_v, fb,
                         c * 64, tk.kvh, row, tk.bc);
+          tr.ev(p, kEvLdKv, kv_it);
           ++kv_it;
           return true;
         };
@@ -951,9 +1268,16 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // K_j then V_j
         const uint32_t slot = kv_it % L::NS;
+        tr.ev(p, kEvLdKvWait, kv_it);
         if (kv_it >= static_cast<uint32_t>(L::NS) &&
             !mbar_wait(bar(L::bKvEmpty + static_cast<int>(slot)), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
           goto out;
+        if constexpr (CK) {  // the K/V tile starts inside k / v
+          const int row = tk.k_row0 + j * kBN;
+          if (!dbg_check(row >= 0 && row < pr.Sk && tk.kvh >= 0 && tk.kvh < pr.Hkv && tk.bc >= 0 && tk.bc < pr.B, wc,
+                         kSiteCheckKvCoord))
+            goto out;
+        }
         const uint32_t fb = bar(L::bKvFull + static_cast<int>(slot));
         const uint32_t dst = sbase + L::oRing + slot * L::kSlotBytes;
         const int nch = which == 0 ? L::NQC : L::NVC;
@@ -961,6 +1285,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
         for (int c = 0; c < nch; ++c)
           tma_load_4d(dst + c * kChunkBytes, which == 0 ? static_cast<const void*>(&p.tm_k) : &p.tm_v, fb,
                       c * 64, tk.kvh, tk.k_row0 + j * kBN, tk.bc);
+        tr.ev(p, kEvLdKv, kv_it);
         ++kv_it;
       }
     }
@@ -974,14 +1299,25 @@ out:
     const uint32_t uses = (kv_it - i + L::NS - 1) / L::NS;  // copies issued into slot i
     mbar_drain_wait(bar(L::bKvFull + static_cast<int>(i)), (uses - 1u) & 1u, wc, kSiteLoadDrain);
   }
+  tr.finish(p);
+  if constexpr (CK) {
+    if (!*wc.abort_flag) {
+      dbg_area[kCntLdKv] = kv_it;
+      dbg_area[kCntLdQ] = q_uses[0];
+      dbg_area[kCntLdQ + 1] = q_uses[1];
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, bool CAUSAL, int MODE>
+template <int DQ, int DV, bool CAUSAL, int MODE, int VAR>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ Params p) {
   using L = Layout<DQ, DV>;
+  static_assert(VAR == 0 || MODE == kModeFixed || MODE == kModeDirect, "build variants: fixed-length modes only");
+  static_assert(256 + 128 + DV <= static_cast<int>(kTmemCols), "S0, S1, O0 and O1 fit in TMEM");
+  constexpr bool CK = (VAR & kVarCheck) != 0;
   constexpr bool EMU = MODE == kModeEmu;
   constexpr bool VARLEN = MODE == kModeVarlen;
   constexpr bool DYN = MODE == kModeVarlen || MODE == kModeDyn;
@@ -995,11 +1331,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::oMisc + 4);
   float* mbox = reinterpret_cast<float*>(smem + L::oMbox);
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::oTaskRing);
+  uint32_t* dbg_area = reinterpret_cast<uint32_t*>(smem + L::oDbgCount);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    if constexpr (CK) {
+      for (int i = 0; i < kNumCounts; ++i) dbg_area[i] = 0u;
+    }
     const uint32_t b = sbase + L::oBar;
     for (int s = 0; s < 2; ++s) {
       mbar_init(b + 8 * (L::bQFull + s), 1);
@@ -1009,6 +1349,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(b + 8 * (L::bODone + s), 1);
       mbar_init(b + 8 * (L::bCorrFull + s), 128);
       mbar_init(b + 8 * (L::bFinFull + s), 128);
+      mbar_init(b + 8 * (L::bStagger + s), 128);
     }
     for (int i = 0; i < L::NS; ++i) {
       mbar_init(b + 8 * (L::bKvFull + i), 1);
@@ -1033,27 +1374,57 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
+  if constexpr (CK) {
+    if (threadIdx.x == 0) {
+      // the aligned layout ends inside the launch's dynamic shared memory
+      uint32_t dyn_bytes;
+      asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+      dbg_check(static_cast<uint32_t>(smem - smem_raw) + static_cast<uint32_t>(L::kBytes) <= dyn_bytes, wc,
+                kSiteCheckSmem);
+      // all 512 columns were allocated, so the base is lane 0, column 0
+      dbg_check(tmem == 0u, wc, kSiteCheckTmem);
+    }
+    __syncthreads();
+  }
 
   // register budget: 128 x (176 + 176 + 104 + 56) = 65536
   if (warp < 8) {
     setmaxnreg_inc<176>();
-    softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN, SPLIT, DIRECT>(p, warp >> 2, tmem, sbase, mbox, ring, wc);
+    softmax_role<DQ, DV, CAUSAL, EMU, VARLEN, DYN, SPLIT, DIRECT, VAR>(p, warp >> 2, tmem, sbase, mbox, ring,
+                                                                      dbg_area, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
-    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT, EMU>(p, tmem, sbase, smem, mbox, ring, wc);
+    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT, EMU, VAR>(p, tmem, sbase, smem, mbox, ring,
+                                                                           dbg_area, wc);
   } else {
     setmaxnreg_dec<56>();
     if (warp == 12) {
-      mma_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT>(p, tmem, sbase, ring, wc);
+      mma_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT, VAR>(p, tmem, sbase, ring, dbg_area, wc);
       __syncwarp();
     } else if (warp == 13) {
-      if (lane == 0) load_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT>(p, sbase, ring, wc);
+      if (lane == 0) load_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT, VAR>(p, sbase, ring, dbg_area, wc);
       __syncwarp();
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CK) {
+    // every hand-off was produced as often as it was consumed
+    if (threadIdx.x == 0 && !*abort_flag) {
+      const uint32_t* c = dbg_area;
+      const bool same[] = {
+          c[kCntLdKv] == c[kCntMmKv],           c[kCntLdQ] == c[kCntMmQ],
+          c[kCntLdQ + 1] == c[kCntMmQ + 1],     c[kCntMmS] == c[kCntSmS],
+          c[kCntMmS + 1] == c[kCntSmS + 1],     c[kCntSmS] == c[kCntCoCorr],
+          c[kCntSmS + 1] == c[kCntCoCorr + 1],  c[kCntSmP] == c[kCntMmP],
+          c[kCntSmP + 1] == c[kCntMmP + 1],     c[kCntCoP] == c[kCntMmP],
+          c[kCntCoP + 1] == c[kCntMmP + 1],     c[kCntMmODone] == c[kCntCoODone],
+          c[kCntMmODone + 1] == c[kCntCoODone + 1]};
+      for (int i = 0; i < static_cast<int>(sizeof(same) / sizeof(same[0])); ++i)
+        if (!dbg_check(same[i], wc, kSiteCheckCounts + static_cast<unsigned>(i))) break;
+    }
+  }
   if (warp == 12) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

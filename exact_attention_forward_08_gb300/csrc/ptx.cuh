@@ -108,7 +108,9 @@ struct WaitCtx {
   uint64_t timeout_ns;
 };
 
-enum : unsigned int { kStatusTimeout = 4u };
+// status codes recorded by the kernels (the same values as the C ABI's
+// FA_ERR_DEVICE_TIMEOUT and FA_ERR_DEVICE_CHECK)
+enum : unsigned int { kStatusTimeout = 4u, kStatusCheck = 5u };
 
 __device__ __forceinline__ void raise_abort(const WaitCtx& w, unsigned int code, unsigned int site) {
   *w.abort_flag = 1;
@@ -170,6 +172,14 @@ __device__ __forceinline__ void tma_store_5d(const void* tmap, uint32_t src, int
       " [%0, {%1, %2, %3, %4, %5}], [%6];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
       "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(src)
       : "memory");
+}
+
+// 32-byte store to global memory (sm_100+): one whole L2 sector; the address
+// must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

@@ -39,6 +39,12 @@
  * allocates no memory for the caller; it keeps a per-device cache of device
  * properties and a 16-byte device status word.
  *
+ * Set-up: the first call of any entry point on a device looks up the
+ * library's device arrays, clears the status word and the no-alloc scratch
+ * header, and synchronises the device once so that those clears cannot land
+ * after later work on a caller's stream.  Make that first call before any
+ * stream capture.
+ *
  * Ordering: calls are asynchronous and stream-ordered on `stream`; no host
  * synchronisation happens inside.  Argument errors are reported before any
  * CUDA call.  A device-side timeout of the kernel's bounded waits is recorded
@@ -65,7 +71,9 @@ enum fa_status {
   FA_ERR_UNSUPPORTED = 2,     /* head dims outside {(64,64), (128,64), (128,128), (192,64), (192,128)},
                                  or a device that is not sm_103 / sm_100 family */
   FA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed (cudaGetLastError is left set) */
-  FA_ERR_DEVICE_TIMEOUT = 4   /* a bounded device wait expired (from fa_device_status) */
+  FA_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device wait expired (from fa_device_status) */
+  FA_ERR_DEVICE_CHECK = 5     /* a device-side check of the checking build failed (from
+                                 fa_device_status; fa_options.debug_flags bit 2) */
 };
 
 /*
@@ -101,7 +109,19 @@ typedef struct fa_options {
                          exp_emu = 1 (the counter lives in that ablation kernel only, so the
                          default kernels carry no counting code; the rescale decisions do not
                          depend on how the exponentials are computed), else
-                         FA_ERR_UNSUPPORTED.  The output is unchanged.  Other bits must be 0. */
+                         FA_ERR_UNSUPPORTED.  The output is unchanged.
+                         Bit 2 (fixed-length forward with static assignment, no exp_emu):
+                         run the checking build of the kernel, which checks every decoded
+                         task, TMA tile coordinate, TMEM base and lane quadrant, shared-
+                         memory extent and output index before use and, at exit, that each
+                         hand-off between the roles was produced as often as it was
+                         consumed.  A failed check skips the access, aborts the CTA and
+                         records FA_ERR_DEVICE_CHECK with its site (601-607 for the range
+                         checks, 610 + i for the hand-off counts) in the status word; the
+                         output is then not valid.  The output of a clean run is identical
+                         to the default kernel's.  Bit 3 (with bit 2 only): plant a fault
+                         for the checks to catch: task 0 decodes to batch index = batch.
+                         Other bits must be 0. */
   int exp_emu;        /* 1: compute one in four exponentials of unmasked blocks on the FMA
                          pipe with a degree-3 polynomial instead of the MUFU ex2 unit
                          ("FlashAttention-4 wiki", "Core methods": partial exp emulation);
@@ -132,6 +152,28 @@ typedef struct fa_options {
                          M-1-m, a constant total of key blocks) are paired on one CTA in
                          consecutive waves; the output is bit-identical.  1 keeps the plain
                          order and whole tasks.  Other values are rejected. */
+  uint64_t* trace;    /* NULL (default), or the event log of a fixed-length forward with
+                         static assignment, head dims (128, 128) or (192, 128) and no
+                         exp_emu or debug bit 2 (else FA_ERR_UNSUPPORTED): device memory of
+                         trace_ctas * 5 * (trace_cap + 1) 64-bit words, 8-byte aligned.
+                         CTA c < trace_ctas writes five tracks (softmax stage 0, softmax
+                         stage 1, correction, MMA, TMA) at word (c * 5 + track) *
+                         (trace_cap + 1): the record count, then up to trace_cap records
+                         {event code in bits 56-63, argument in bits 32-55, SM clock low
+                         32 bits}, stamped by lane 0 of the role's first warp at each step
+                         of the hand-off protocol: the waits and arrivals of each role (codes
+                         in csrc/fa_kernel.cuh).  A separate kernel build; the output is
+                         identical to the default kernel's. */
+  int trace_ctas;     /* CTAs that record (>= 1 when trace is set) */
+  int trace_cap;      /* records kept per track (>= 1 when trace is set) */
+  int stagger;        /* 1: an ablation build in which the two softmax warpgroups take turns
+                         for their exponentials in the K/V blocks both Q tiles visit (stage 1
+                         after stage 0's of the same block, stage 0 after stage 1's of the
+                         previous one: the staggered exp sections of "FlashAttention-4 wiki",
+                         "Core methods"); fixed-length forward with static assignment, head
+                         dims (128, 128) or (192, 128), not with trace, exp_emu or debug bit 2
+                         (else FA_ERR_UNSUPPORTED).  The output is identical to the default
+                         kernel's.  0 (default): no stagger.  Other values are rejected. */
 } fa_options;
 
 #define FA_SCHED_WORKSPACE_BYTES 16
@@ -293,7 +335,14 @@ int fa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float
  * file-scope device array of the library (fa_noalloc_scratch_bytes() bytes,
  * 1 MiB, one per device; its address is looked up once per device at set-up).
  * The pages have no counterpart: this is a convenience of this library for
- * callers that cannot hand it scratch memory.  Nothing is allocated.
+ * callers that cannot hand it scratch memory, such as runtimes that own all
+ * device memory through a fixed arena or pool and give a kernel library only
+ * its input and output tensors, or code that must not call cudaMalloc (which
+ * may synchronise the device) on its serving path.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.  The first
+ * call on a device does the one-time set-up described at the top of this
+ * file (the array's address, its header cleared), so make it before any
+ * stream capture.
  *
  * A call whose task list needs more than the array holds
  * (fa_varlen_workspace_size(batch, heads_q, total_q) > 1 MiB, about 32 760
@@ -329,10 +378,16 @@ int fa_varlen_plan_host(const int* cu_seqlens_q, const int* cu_seqlens_k, int ba
 /*
  * Synchronise `stream`, then read and clear the current device's status
  * word.  *out receives FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_INVALID_ARG (a
- * varlen call found bad cu_seqlens); detail (may be NULL) receives
- * {code, site, block or sequence index}.  Returns FA_OK or FA_ERR_CUDA.
+ * varlen call found bad cu_seqlens).  Returns FA_OK or FA_ERR_CUDA.
  */
-int fa_device_status(fa_stream_t stream, int* out, unsigned int detail[3]);
+int fa_device_status(fa_stream_t stream, int* out);
+
+/*
+ * The same, with the recorded detail: detail (may be NULL) receives {code,
+ * site, block or sequence index}, the site being the wait or check that
+ * failed (role * 100 + barrier for a timed-out wait).
+ */
+int fa_device_status_detail(fa_stream_t stream, int* out, unsigned int detail[3]);
 
 /*
  * Synchronise `stream`, then read and clear the current device's counter of

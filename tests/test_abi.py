@@ -30,7 +30,8 @@ def _declared_functions():
 
 def test_header_declares_entry_points():
     names = _declared_functions()
-    for required in ("fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_status_string", "fa_make_plan",
+    for required in ("fa_fwd", "fa_fwd_ex", "fa_device_status", "fa_device_status_detail", "fa_status_string",
+                     "fa_make_plan",
                      "fa_plan_task", "fa_options_default", "fa_version", "fa_plan_block_masked",
                      "fa_selftest_exp2", "fa_plan_first_masked_block", "fa_fwd_varlen", "fa_fwd_varlen_ex",
                      "fa_varlen_workspace_size", "fa_varlen_plan_host"):
@@ -82,7 +83,7 @@ def test_empty_problem_is_ok_without_launch(fa, kw):
 def test_bad_options_rejected(fa):
     opts = fa.default_options()
     assert abs(opts.tau - 8.0) < 1e-7 and opts.pack == 0 and opts.grid == 0 and opts.no_balance == 0
-    for field, value in (("pack", 3), ("pack", -1), ("grid", -2), ("debug_flags", 4), ("debug_flags", 8),
+    for field, value in (("pack", 3), ("pack", -1), ("grid", -2), ("debug_flags", 16), ("debug_flags", 8),
                          ("timeout_s", 1e9), ("tau", 65.0), ("tau", float("inf")), ("tau", float("nan")), ("exp_emu", 2),
                          ("exp_emu", -1), ("store_mode", 3), ("store_mode", -1), ("no_balance", 2),
                          ("no_balance", -1)):

@@ -51,6 +51,10 @@ def test_bounded_wait_reports_timeout_and_context_survives(fa, causal):
     assert detail[0] == 4 and detail[1] in STALLED_SITES, detail
     # reading the status cleared it
     assert fa.fa_device_status()[0] == fa.FA_OK
+    # the plain status call (code only) reports the same failure
+    fa.attention_forward(qd, kd, vd, causal=causal, options=opts)
+    assert fa.fa_device_status_code() == fa.FA_ERR_DEVICE_TIMEOUT
+    assert fa.fa_device_status_code() == fa.FA_OK
 
     # the context is still usable and a normal call is correct
     o, lse = fa.attention_forward(qd, kd, vd, causal=causal)

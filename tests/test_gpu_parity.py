@@ -2,7 +2,11 @@
 
 Tolerances for bf16 outputs of unit-normal inputs: max|O - O_ref| <= 2e-2,
 mean|O - O_ref| <= 2e-3, and |LSE - LSE_ref| <= 1e-3 (fp32 LSE).  Rows with no
-visible key must give O = 0 and LSE = -inf exactly.
+visible key must give O = 0 and LSE = -inf exactly.  For inputs that are not
+unit-normal (the wide-range workload: Q x 4, keys with a rising offset) the
+max bound is the one the arithmetic gives, 2^-7 max|V|: P is rounded to bf16
+(relative error up to 2^-8) for the P V product while the row sum stays fp32,
+so |dO| <= 2^-8 max|V|, and the bf16 rounding of O adds up to 2^-8 |O|.
 
 Small problems compare every output element; the benchmark configurations
 compare sampled rows (first, last and diagonal tiles plus random rows) in the
@@ -21,6 +25,14 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 MAX_TOL, MEAN_TOL, LSE_TOL = 2e-2, 2e-3, 1e-3
+
+
+def max_tol(w, v_bits):
+    """The max|dO| bound for workload w: the stated 2e-2 for unit-normal inputs,
+    else the arithmetic's 2^-7 max|V| (see the module docstring)."""
+    if w.q_mul == 1.0 and w.k_offset == 0.0:
+        return MAX_TOL
+    return 2.0 ** -7 * float(np.abs(synthetic.bf16_bits_to_f32(v_bits)).max())
 
 
 @pytest.fixture(scope="module")
@@ -45,7 +57,7 @@ def run_gpu(fa, w, q, k, v, options=None):
     return o, lse
 
 
-def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, what="", max_bound=MAX_TOL):
     """o_gpu [n, dv] float64, lse_gpu [n]; same for the oracle."""
     empty = ~np.isfinite(lse_ref)
     assert np.array_equal(~np.isfinite(lse_gpu), empty), f"{what}: empty-row pattern differs"
@@ -55,7 +67,7 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
     emax, emean = float(err.max()), float(err.mean())
     lerr = float(np.abs(lse_gpu[~empty] - lse_ref[~empty]).max()) if np.any(~empty) else 0.0
-    assert emax <= MAX_TOL, f"{what}: max|dO| {emax:.3e}"
+    assert emax <= max_bound, f"{what}: max|dO| {emax:.3e} (bound {max_bound:.3e})"
     assert emean <= MEAN_TOL, f"{what}: mean|dO| {emean:.3e}"
     assert lerr <= LSE_TOL, f"{what}: max|dLSE| {lerr:.3e}"
     return emax, emean, lerr
@@ -69,7 +81,7 @@ def full_check(fa, w, options=None):
     # LSE [B,Hq,Sq] -> row order (b, i, h)
     lg = lse.cpu().numpy().astype(np.float64).transpose(0, 2, 1).reshape(-1)
     lr = lse_ref.transpose(0, 2, 1).reshape(-1)
-    return compare(og, lg, o_ref.reshape(-1, w.d_v), lr, w.name)
+    return compare(og, lg, o_ref.reshape(-1, w.d_v), lr, w.name, max_tol(w, v))
 
 
 SMALL = [
@@ -228,7 +240,7 @@ def test_bench_config_sampled(fa, name):
     bi, ii, hi = (torch.from_numpy(x).cuda() for x in (b, i, h))
     og = o[bi, ii, hi].float().cpu().numpy().astype(np.float64)
     lg = lse[bi, hi, ii].cpu().numpy().astype(np.float64)
-    compare(og, lg, o_ref, lse_ref, name)
+    compare(og, lg, o_ref, lse_ref, name, max_tol(w, v))
     # properties that hold at any size: every output finite, every LSE finite
     # (no empty rows in these configurations), |O| bounded by max|V|
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
