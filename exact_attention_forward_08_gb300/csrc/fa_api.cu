@@ -58,7 +58,7 @@ struct DeviceState {
   void* noalloc_scratch = nullptr;  // g_fa_noalloc_scratch on this device
   bool kernel_ready[kNumKernels] = {};
   bool debug_ready[5 * 2 * 2 * 3] = {};  // (d_qk, d_v) pair x causal x (fixed, direct) x (trace, check, stagger)
-  bool bwd_ready[2 * 2 * 2] = {};   // (d 64 / 128) x (dK/dV, dQ) x (non-causal, causal)
+  bool bwd_ready[3 * 2 * 2] = {};   // ((64,64), (128,128), (192,128)) x (dK/dV, dQ) x (non-causal, causal)
   bool plan_ready = false;
 };
 
@@ -914,7 +914,8 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   if ((opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
   if (opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1 || opt.trace != nullptr || opt.stagger)
     return FA_ERR_UNSUPPORTED;
-  if (d_qk != d_v || (d_qk != 64 && d_qk != 128)) return FA_ERR_UNSUPPORTED;
+  const int pair = (d_qk == 64 && d_v == 64) ? 0 : ((d_qk == 128 && d_v == 128) ? 1 : ((d_qk == 192 && d_v == 128) ? 2 : -1));
+  if (pair < 0) return FA_ERR_UNSUPPORTED;
   if (batch == 0) return FA_OK;
   const int64_t big = int64_t(1) << 31;
   if (static_cast<int64_t>(seqlen_q) + seqlen_k + 4 * fa::kBM >= big) return FA_ERR_INVALID_ARG;
@@ -943,8 +944,9 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   // degenerate shapes: no query (dK = dV = 0) or no key (dQ = 0)
   if (!any_q || !any_k) {
     if (any_k) {
-      const size_t bytes = static_cast<size_t>(batch) * seqlen_k * heads_kv * d_qk * 2;
-      if (cudaMemsetAsync(dk, 0, bytes, stream) != cudaSuccess || cudaMemsetAsync(dv, 0, bytes, stream) != cudaSuccess)
+      const size_t rows = static_cast<size_t>(batch) * seqlen_k * heads_kv;
+      if (cudaMemsetAsync(dk, 0, rows * d_qk * 2, stream) != cudaSuccess ||
+          cudaMemsetAsync(dv, 0, rows * d_v * 2, stream) != cudaSuccess)
         return FA_ERR_CUDA;
     }
     if (any_q) {
@@ -956,8 +958,8 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
 
   fa::BwdEntry ent[2];
   for (int kind = 0; kind < 2; ++kind) {
-    if (!fa::bwd_entry(d_qk, kind, causal, &ent[kind])) return FA_ERR_UNSUPPORTED;
-    const int idx = ((d_qk == 128 ? 1 : 0) * 2 + kind) * 2 + causal;
+    if (!fa::bwd_entry(d_qk, d_v, kind, causal, &ent[kind])) return FA_ERR_UNSUPPORTED;
+    const int idx = (pair * 2 + kind) * 2 + causal;
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!st->bwd_ready[idx]) {
       if (ent[kind].smem > st->smem_optin) return FA_ERR_UNSUPPORTED;
@@ -971,7 +973,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   const int sq_pad = (seqlen_q + fa::kBM - 1) / fa::kBM * fa::kBM;
   float* l2 = static_cast<float*>(workspace);
   float* dvec = l2 + static_cast<int64_t>(batch) * heads_q * sq_pad;
-  if (fa::launch_bwd_prep(d_qk, o, dout, lse, l2, dvec, batch, heads_q, seqlen_q, sq_pad, st->sms * 16, stream) !=
+  if (fa::launch_bwd_prep(d_v, o, dout, lse, l2, dvec, batch, heads_q, seqlen_q, sq_pad, st->sms * 16, stream) !=
       cudaSuccess)
     return FA_ERR_CUDA;
 
@@ -988,10 +990,11 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     const void* t1 = kv ? dout : v;
     const int hr = kv ? heads_kv : heads_q, sr = kv ? seqlen_k : seqlen_q;
     const int ht = kv ? heads_q : heads_kv, stt = kv ? seqlen_q : seqlen_k;
-    // streamed tiles travel as 64-row halves (one per stage)
-    if (encode_kv(&p.tm_r0, r0, batch, sr, hr, d_qk) != FA_OK || encode_kv(&p.tm_r1, r1, batch, sr, hr, d_qk) != FA_OK ||
+    // streamed tiles travel as 64-row halves (one per stage); R0 / T0 (K, Q)
+    // have d_qk columns, R1 / T1 (V, dO) d_v
+    if (encode_kv(&p.tm_r0, r0, batch, sr, hr, d_qk) != FA_OK || encode_kv(&p.tm_r1, r1, batch, sr, hr, d_v) != FA_OK ||
         encode_kv(&p.tm_t0, t0, batch, stt, ht, d_qk, 64) != FA_OK ||
-        encode_kv(&p.tm_t1, t1, batch, stt, ht, d_qk, 64) != FA_OK)
+        encode_kv(&p.tm_t1, t1, batch, stt, ht, d_v, 64) != FA_OK)
       return FA_ERR_CUDA;
     p.l2 = l2;
     p.dvec = dvec;
@@ -1005,7 +1008,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     p.units = batch * hr;
     p.blocks = kv ? p.nk : p.mq;
     // causal sections: units whose streamed tiles fit in half the L2 together
-    const int64_t streamed = static_cast<int64_t>(stt) * d_qk * 2 * 2 * (kv ? ratio : 1);
+    const int64_t streamed = static_cast<int64_t>(stt) * (d_qk + d_v) * 2 * (kv ? ratio : 1);
     int64_t su = streamed > 0 ? l2_budget / streamed : 1;
     if (su < 1) su = 1;
     if (su > p.units) su = p.units;

@@ -24,6 +24,9 @@
 // per tile pair (S and dP recomputed) but needs neither the fp32 dQ
 // reductions across key blocks nor TMEM beyond 512 columns (S, dP, dK, dV).
 //
+// Head dims: d_qk = d_v in {64, 128}, and (d_qk, d_v) = (192, 128).  R0 / T0
+// (K, Q) have d_qk columns, R1 / T1 (V, dO) d_v columns.
+//
 // CTA: 320 threads, persistent (grid = SM count).  Each 128-row streamed
 // block is taken as two 64-row stages (the forward's two-stage overlap: one
 // stage's row warps work while the other stage's GEMMs run):
@@ -33,15 +36,24 @@
 //   warp 8     tcgen05.mma issue (one lane) and TMEM alloc / free.
 //   warp 9     TMA loads (one lane).
 // TMEM: S_0 [0,64), dP_0 [64,128), S_1 [128,192), dP_1 [192,256),
-// accumulator 0 [256, 256+D) (dV or dQ), accumulator 1 [384, 384+D) (dK).
+// accumulator 0 [256, 256+d) (dV or dQ), accumulator 1 [384, 384+d) (dK).
 // P^T (dK/dV) or dS (dQ) is written as packed bf16 pairs over the first 32
-// columns of S_s, dS^T over the first 32 of dP_s.
+// columns of S_s, dS^T over the first 32 of dP_s.  At (192, 128) the dK/dV
+// accumulators take 128 + 192 columns, so S_s and dP_s share 64 columns per
+// stage: S_s lands there, the row warps read it (s_read), dP_s is written
+// over it, and P^T / dS^T go to its first / last 32 columns; dV at [128, 256),
+// dK at [256, 448).  The dQ kernel at (192, 128) keeps the separate S and dP
+// columns with dQ at [256, 448) and reads Q and dO from SMEM (no room for the
+// TMEM copies).
 //
 // Hand-offs (all mbarriers, all waits bounded):
 //   res_full / res_empty     resident tiles of a task loaded / no longer read
 //   t_full[r] / t_empty[r]   ring slot r of streamed tiles (+ the LSE and D
 //                            vectors of the block for dK/dV)
-//   s_full[s]                S_s and dP_s of the current block in TMEM
+//   s_full[s]                S_s and dP_s of the current block in TMEM (shared
+//                            columns: S_s only)
+//   s_read[s] (count 128)    shared columns: S_s read by the row warps
+//   dp_full[s]               shared columns: dP_s in TMEM
 //   p_ready[s] (count 128)   P / dS of stage s written to TMEM
 //   acc_done                 the task's accumulators are final
 //   acc_free (count 256)     the epilogue of both stages has read them
@@ -80,22 +92,26 @@ struct BwdParams {
 // streamed tensors and is released as soon as that stage's GEMMs are done.
 // (With whole-block slots the ring only held two blocks at d = 128 and the
 // loader could not fetch far enough ahead to hide the L2 latency.)
-template <int D>
+template <int DQ, int DV>
 struct BwdLayout {
-  static_assert(D == 64 || D == 128, "backward head dims");
-  static constexpr int NC = D / 64;
-  static constexpr int kTile = NC * kChunkBytes;    // one resident 128-row tile
+  static_assert((DQ == DV && (DQ == 64 || DQ == 128)) || (DQ == 192 && DV == 128), "backward head dims");
+  static constexpr int NCQ = DQ / 64, NCV = DV / 64;
+  static constexpr int kTile0 = NCQ * kChunkBytes;  // resident R0 (K or Q): 128 rows x d_qk
+  static constexpr int kTile1 = NCV * kChunkBytes;  // resident R1 (V or dO): 128 rows x d_v
   static constexpr int kHalfChunk = 64 * 128;       // 64 rows x 128 B
-  static constexpr int kHalf = NC * kHalfChunk;     // one streamed 64-row half-tile
+  static constexpr int kHalf0 = NCQ * kHalfChunk;   // streamed T0 half-tile (Q or K)
+  static constexpr int kHalf1 = NCV * kHalfChunk;   // streamed T1 half-tile (dO or V)
   static constexpr int kVecH = 64 * 4;              // 64 fp32
-  static constexpr int kSlot = 2 * kHalf;           // T0 half, T1 half (1024-aligned)
+  static constexpr int kSlot = kHalf0 + kHalf1;     // T0 half, T1 half (1024-aligned)
   static constexpr int kMaxSmem = 232448;
-  static constexpr int NSLOT_fit = (kMaxSmem - 2 * kTile - 2048 - 1024) / (kSlot + 2 * kVecH);
+  static constexpr int NSLOT_fit = (kMaxSmem - kTile0 - kTile1 - 2048 - 1024) / (kSlot + 2 * kVecH);
   static constexpr int NSLOT = NSLOT_fit > 8 ? 8 : NSLOT_fit;
-  static_assert(NSLOT >= 4, "ring needs two blocks");
+  // three half-slots keep one block ahead of the GEMMs (the next half of a
+  // stage loads into the slot its own previous accumulating GEMMs release)
+  static_assert(NSLOT >= 3, "ring depth");
   static constexpr int oR0 = 0;
-  static constexpr int oR1 = kTile;
-  static constexpr int oRing = 2 * kTile;                   // slot r: T0 half, T1 half
+  static constexpr int oR1 = kTile0;
+  static constexpr int oRing = kTile0 + kTile1;             // slot r: T0 half, T1 half
   static constexpr int oVec = oRing + NSLOT * kSlot;        // slot r: L2 vector (64), D vector (64)
   static constexpr int oBar = oVec + NSLOT * 2 * kVecH;
   static constexpr int bResFull = 0;
@@ -108,7 +124,9 @@ struct BwdLayout {
   static constexpr int bAccFree = bSFull + 5;     // count 256
   static constexpr int bDrain = bSFull + 6;
   static constexpr int bAReady = bSFull + 7;     // dQ: Q and dO copied into TMEM (count 256)
-  static constexpr int kNumBars = bAReady + 1;
+  static constexpr int bSRead = bSFull + 8;      // [2] shared S / dP columns: S read (count 128)
+  static constexpr int bDpFull = bSFull + 10;    // [2] shared S / dP columns: dP in TMEM
+  static constexpr int kNumBars = bDpFull + 2;
   static constexpr int oMisc = oBar + kNumBars * 8;  // [0] TMEM base, [1] abort flag
   static constexpr int kBytes = oMisc + 16;
   static constexpr int kDynSmem = kBytes + 1024;
@@ -117,14 +135,38 @@ struct BwdLayout {
   static __device__ __forceinline__ uint32_t vec_off(int r) { return oVec + r * 2 * kVecH; }
 };
 
+// TMEM column plan of a kernel: S_s and dP_s share 64 columns (dK/dV with
+// d_qk + d_v > 256), or S_s at 128 s and dP_s at 128 s + 64; the accumulators
+// (dV then dK, or dQ); the dQ kernel's TMEM copies of Q and dO (when they fit).
+template <int DQ, int DV, int KIND>
+struct BwdCols {
+  static constexpr bool kShare = KIND == kBwdDkDv && DQ + DV > 256;
+  static constexpr bool kTmemA = KIND == kBwdDq && DQ + DV <= 256;
+  static constexpr uint32_t kAcc0 = kShare ? 128u : 256u;  // dV (dK/dV) or dQ
+  static constexpr uint32_t kAcc1 = kShare ? 256u : 384u;  // dK
+  static constexpr uint32_t kQCol = 384u, kOCol = 448u;    // dQ kernel, kTmemA only
+  static_assert(KIND != kBwdDkDv || kAcc1 + DQ <= 512, "dK accumulator");
+  static_assert(KIND != kBwdDq || kAcc0 + DQ <= (kTmemA ? kQCol : 512u), "dQ accumulator");
+  static __device__ __forceinline__ uint32_t s_col(int s) { return static_cast<uint32_t>((kShare ? 64 : 128) * s); }
+  static __device__ __forceinline__ uint32_t p_col(int s) {
+    return kShare ? static_cast<uint32_t>(64 * s) : static_cast<uint32_t>(128 * s + 64);
+  }
+  // where P^T (dK/dV) or dS (dQ) and dS^T (dK/dV) are written: the first 32
+  // columns of S_s / dP_s, or the two halves of the shared columns
+  static __device__ __forceinline__ uint32_t pt_col(int s) { return s_col(s); }
+  static __device__ __forceinline__ uint32_t dst_col(int s) { return kShare ? s_col(s) + 32u : p_col(s); }
+};
+
 enum : unsigned int {
   kSiteBwdRowS = 601,
   kSiteBwdRowAcc = 602,
+  kSiteBwdRowDp = 603,
   kSiteBwdMmaRes = 611,
   kSiteBwdMmaT = 612,
   kSiteBwdMmaP = 613,
   kSiteBwdMmaAcc = 614,
   kSiteBwdMmaDrain = 615,
+  kSiteBwdMmaSRead = 616,
   kSiteBwdLoadRes = 621,
   kSiteBwdLoadT = 622,
   kSiteBwdLoadDrain = 623,
@@ -280,14 +322,6 @@ __device__ __forceinline__ void issue_pv64(uint32_t d_tmem, uint32_t a_tmem, uin
                    accumulate ? 1u : 0u, leader);
 }
 
-// TMEM columns of stage s: S_s at 128 s, dP_s at 128 s + 64 (64 each);
-// accumulators at 256 (dV or dQ) and 384 (dK).  The dQ kernel keeps its
-// resident Q at 384 and dO at 448 (packed bf16 pairs) as the A operands of S
-// and dP, so those GEMMs read only the streamed half-tile from SMEM.
-constexpr uint32_t kBwdQCol = 384, kBwdOCol = 448;
-__device__ __forceinline__ uint32_t bwd_s_col(int s) { return static_cast<uint32_t>(128 * s); }
-__device__ __forceinline__ uint32_t bwd_p_col(int s) { return static_cast<uint32_t>(128 * s + 64); }
-
 // ---------------------------------------------------------------------------
 // row role (warpgroup s = stage s): thread = row = TMEM lane
 // ---------------------------------------------------------------------------
@@ -296,15 +330,17 @@ __device__ __forceinline__ uint32_t bwd_p_col(int s) { return static_cast<uint32
 // entries (0 elsewhere), dS = P (dP - D).  dK/dV: rows are keys, columns
 // queries (LSE and D per column, from the block's vectors in the ring slot);
 // dQ: rows are queries (LSE and D per row), columns keys.
-template <int D, int KIND, bool CAUSAL>
+template <int DQ, int DV, int KIND, bool CAUSAL>
 __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage, const uint32_t tmem,
                                              const uint32_t sbase, const uint8_t* smem, const WaitCtx& wc) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<DQ, DV>;
+  using C = BwdCols<DQ, DV, KIND>;
   const int t = threadIdx.x - 128 * stage;
   const uint32_t lane_off = static_cast<uint32_t>(t & ~31) << 16;
-  const uint32_t tS = tmem + lane_off + bwd_s_col(stage);  // S_s, then P^T (dK/dV) or dS (dQ) over its first 32 columns
-  const uint32_t tP = tmem + lane_off + bwd_p_col(stage);  // dP_s, then dS^T (dK/dV) over its first 32 columns
+  const uint32_t tS = tmem + lane_off + C::s_col(stage);  // S_s, then P^T (dK/dV) or dS (dQ) over its first 32 columns
+  const uint32_t tP = tmem + lane_off + C::p_col(stage);  // dP_s, then dS^T (dK/dV) over its first 32 columns
   const uint32_t bar0 = sbase + L::oBar;
+  uint32_t dp_phase = 0;  // shared S / dP columns
   const float sl2 = p.scale_log2;
   const int cb = 64 * stage;  // first column of this stage inside the streamed block
   uint32_t s_phase = 0, acc_phase = 0;
@@ -315,16 +351,16 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
   for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
     const BwdTask tk = bwd_task<KIND>(p, task);
     const int row = tk.blk * kBM + t;  // key (dK/dV) or query (dQ)
-    if (KIND == kBwdDq) {
+    if constexpr (C::kTmemA) {
       // stage s copies its resident tile (Q or dO, row t, 128-byte swizzled
       // in SMEM) into TMEM as packed bf16 pairs.  The previous task's
       // epilogue waited for all its MMAs, so these columns are free.
       if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bResFull, res_phase, wc, kSiteBwdRowS))) return;
       res_phase ^= 1u;
       const uint8_t* tile = smem + (stage == 0 ? L::oR0 : L::oR1);
-      const uint32_t tA = tmem + lane_off + (stage == 0 ? kBwdQCol : kBwdOCol);
+      const uint32_t tA = tmem + lane_off + (stage == 0 ? C::kQCol : C::kOCol);
 #pragma unroll
-      for (int c = 0; c < L::NC; ++c) {
+      for (int c = 0; c < L::NCQ; ++c) {
         const uint4* src = reinterpret_cast<const uint4*>(tile + c * kChunkBytes + t * 128);
         uint32_t w[32];
 #pragma unroll
@@ -373,29 +409,56 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
         const bool vis = row_ok && c >= cmin && c <= cmax;
         pr[c] = vis ? ex2_approx(__uint_as_float(r[c]) * sl2 - lse2) : 0.f;
       }
-      if (KIND == kBwdDkDv) {  // P^T for dV += P^T dO
-        uint32_t pk[32];
+      if constexpr (C::kShare) {
+        // S is in registers: dP_s may now be written over it
+        tc_fence_before();
+        mbar_arrive(bar0 + 8u * (L::bSRead + stage));
+        if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (L::bDpFull + stage), dp_phase, wc, kSiteBwdRowDp)))
+          return;
+        dp_phase ^= 1u;
+        tc_fence_after();
+        // dS^T = P^T (dP^T - D) from the whole of dP_s (loaded before either
+        // half of the columns is overwritten), then P^T and dS^T over them
+        uint32_t dp[64];
+        tmem_ld64_wait(tP, dp);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
-        tmem_st32(tS, pk);
-      }
-      // dS = P (dP - D), 32 columns at a time, onto columns 16q .. 16q+15 of
-      // dP (dK/dV) or S (dQ), all of them read already
-      const uint32_t tDst = KIND == kBwdDkDv ? tP : tS;
+        for (int h = 0; h < 2; ++h) {  // 16 packed columns of each at a time
+          uint32_t pk[16], dk[16];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t dp[32];
-        tmem_ld32_wait(tP + static_cast<uint32_t>(32 * q), dp);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c0 = 32 * q + 2 * i;
-          const float d0 = KIND == kBwdDkDv ? dvv[c0] : d_row;
-          const float d1 = KIND == kBwdDkDv ? dvv[c0 + 1] : d_row;
-          pk[i] = pack_bf16x2(pr[c0] * (__uint_as_float(dp[2 * i]) - d0),
-                              pr[c0 + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
+          for (int i = 0; i < 16; ++i) {
+            const int c0 = 32 * h + 2 * i;
+            pk[i] = pack_bf16x2(pr[c0], pr[c0 + 1]);
+            dk[i] = pack_bf16x2(pr[c0] * (__uint_as_float(dp[c0]) - dvv[c0]),
+                                pr[c0 + 1] * (__uint_as_float(dp[c0 + 1]) - dvv[c0 + 1]));
+          }
+          tmem_st16(tmem + lane_off + C::pt_col(stage) + static_cast<uint32_t>(16 * h), pk);
+          tmem_st16(tmem + lane_off + C::dst_col(stage) + static_cast<uint32_t>(16 * h), dk);
         }
-        tmem_st16(tDst + static_cast<uint32_t>(16 * q), pk);
+      } else {
+        if (KIND == kBwdDkDv) {  // P^T for dV += P^T dO
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+          tmem_st32(tS, pk);
+        }
+        // dS = P (dP - D), 32 columns at a time, onto columns 16q .. 16q+15 of
+        // dP (dK/dV) or S (dQ), all of them read already
+        const uint32_t tDst = KIND == kBwdDkDv ? tP : tS;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          uint32_t dp[32];
+          tmem_ld32_wait(tP + static_cast<uint32_t>(32 * q), dp);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c0 = 32 * q + 2 * i;
+            const float d0 = KIND == kBwdDkDv ? dvv[c0] : d_row;
+            const float d1 = KIND == kBwdDkDv ? dvv[c0 + 1] : d_row;
+            pk[i] = pack_bf16x2(pr[c0] * (__uint_as_float(dp[2 * i]) - d0),
+                                pr[c0 + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
+          }
+          tmem_st16(tDst + static_cast<uint32_t>(16 * q), pk);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -415,16 +478,16 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
     uint32_t tA;
     int c_lo, c_hi;
     if (KIND == kBwdDkDv) {
-      const int64_t off = ((static_cast<int64_t>(tk.b) * p.Sk + row) * p.Hkv + tk.h) * D;
-      dst = (stage == 0 ? p.out0 : p.out1) + off;  // dV, dK
+      const int64_t rr = (static_cast<int64_t>(tk.b) * p.Sk + row) * p.Hkv + tk.h;
+      dst = stage == 0 ? p.out0 + rr * DV : p.out1 + rr * DQ;  // dV, dK
       mult = stage == 0 ? 1.f : p.scale;
-      tA = tmem + lane_off + (stage == 0 ? 256u : 384u);
-      c_lo = 0, c_hi = D;
+      tA = tmem + lane_off + (stage == 0 ? C::kAcc0 : C::kAcc1);
+      c_lo = 0, c_hi = stage == 0 ? DV : DQ;
     } else {
-      dst = p.out0 + ((static_cast<int64_t>(tk.b) * p.Sq + row) * p.Hq + tk.h) * D;
+      dst = p.out0 + ((static_cast<int64_t>(tk.b) * p.Sq + row) * p.Hq + tk.h) * DQ;
       mult = p.scale;
-      tA = tmem + lane_off + 256u;
-      c_lo = stage * (D / 2), c_hi = c_lo + D / 2;
+      tA = tmem + lane_off + C::kAcc0;
+      c_lo = stage * (DQ / 2), c_hi = c_lo + DQ / 2;
     }
 #pragma unroll 1
     for (int c = c_lo; c < c_hi; c += 32) {
@@ -459,32 +522,44 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
 // Per streamed block j and stage s: the accumulating GEMMs of (j, s) as soon
 // as stage s has written P / dS, then S and dP of (j+1, s), so one stage's
 // row warps work while the other stage's GEMMs run.
-template <int D, int KIND>
+template <int DQ, int DV, int KIND>
 __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t tmem, const uint32_t sbase,
                                              const WaitCtx& wc) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<DQ, DV>;
+  using C = BwdCols<DQ, DV, KIND>;
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const uint32_t leader = (threadIdx.x & 31) == 0 ? 1u : 0u;
   auto wait = [&](uint32_t b, uint32_t parity, unsigned site) {
     return __all_sync(0xffffffffu, mbar_wait(b, parity, wc, site));
   };
-  uint32_t res_phase = 0, free_phase = 0, a_phase = 0, p_phase[2] = {0u, 0u};
+  uint32_t res_phase = 0, free_phase = 0, a_phase = 0, p_phase[2] = {0u, 0u}, sr_phase[2] = {0u, 0u};
   int slot_it = 0;  // streamed blocks consumed; block i's stage-s half sits in slot (2 i + s) % NSLOT
   const int num_tasks = p.units * p.blocks;
   const uint32_t r0 = sbase + L::oR0, r1 = sbase + L::oR1;
   auto half_slot = [&](int blk_it, int s) { return (2 * blk_it + s) % L::NSLOT; };
   auto half_parity = [&](int blk_it, int s) { return static_cast<uint32_t>((2 * blk_it + s) / L::NSLOT) & 1u; };
+  // S_s and dP_s of the half in `slot`; with shared columns only S_s here
+  // (dP_s follows once the row warps have read S_s: issue_dp)
   auto issue_sdp = [&](int s, int slot) {
-    const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf;
-    if (KIND == kBwdDkDv) {
-      issue_qk64<D>(tmem + bwd_s_col(s), r0, t0, leader);  // S_s  = R0 T0_s^T  (K Q_s^T)
-      issue_qk64<D>(tmem + bwd_p_col(s), r1, t1, leader);  // dP_s = R1 T1_s^T  (V dO_s^T)
+    const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf0;
+    if constexpr (C::kTmemA) {
+      issue_ts_qk64<DQ>(tmem + C::s_col(s), tmem + C::kQCol, t0, leader);  // S_s  = Q K_s^T
+      issue_ts_qk64<DV>(tmem + C::p_col(s), tmem + C::kOCol, t1, leader);  // dP_s = dO V_s^T
     } else {
-      issue_ts_qk64<D>(tmem + bwd_s_col(s), tmem + kBwdQCol, t0, leader);  // S_s  = Q K_s^T
-      issue_ts_qk64<D>(tmem + bwd_p_col(s), tmem + kBwdOCol, t1, leader);  // dP_s = dO V_s^T
+      issue_qk64<DQ>(tmem + C::s_col(s), r0, t0, leader);                    // S_s  = R0 T0_s^T
+      if constexpr (!C::kShare) issue_qk64<DV>(tmem + C::p_col(s), r1, t1, leader);  // dP_s = R1 T1_s^T
     }
     mma_commit(bar(L::bSFull + s), leader);
+  };
+  // shared columns: dP_s over S_s once the row warps have read it
+  auto issue_dp = [&](int s, int slot) -> bool {
+    if (!wait(bar(L::bSRead + s), sr_phase[s], kSiteBwdMmaSRead)) return false;
+    sr_phase[s] ^= 1u;
+    tc_fence_after();
+    issue_qk64<DV>(tmem + C::p_col(s), r1, sbase + L::slot_off(slot) + L::kHalf0, leader);  // dP_s = R1 T1_s^T
+    mma_commit(bar(L::bDpFull + s), leader);
+    return true;
   };
 
   for (int task = blockIdx.x, n = 0; task < num_tasks; task += gridDim.x, ++n) {
@@ -495,7 +570,7 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
       if (!wait(bar(L::bAccFree), free_phase, kSiteBwdMmaAcc)) goto out;
       free_phase ^= 1u;
     }
-    if (KIND == kBwdDq) {  // Q and dO of this task are in TMEM
+    if constexpr (C::kTmemA) {  // Q and dO of this task are in TMEM
       if (!wait(bar(L::bAReady), a_phase, kSiteBwdMmaRes)) goto out;
       a_phase ^= 1u;
     }
@@ -507,21 +582,26 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
         tc_fence_after();
         issue_sdp(s, half_slot(slot_it, s));
       }
+      if constexpr (C::kShare) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          if (!issue_dp(s, half_slot(slot_it, s))) goto out;
+      }
     }
     for (int it = 0; it < tk.nit; ++it, ++slot_it) {
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         const int slot = half_slot(slot_it, s);
-        const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf;
+        const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf0;
         if (!wait(bar(L::bPReady + s), p_phase[s], kSiteBwdMmaP)) goto out;
         p_phase[s] ^= 1u;
         tc_fence_after();
         const bool acc = it > 0 || s > 0;
         if (KIND == kBwdDkDv) {
-          issue_pv64<D>(tmem + 256u, tmem + bwd_s_col(s), t1, acc, leader);  // dV += P^T_s dO_s
-          issue_pv64<D>(tmem + 384u, tmem + bwd_p_col(s), t0, acc, leader);  // dK += dS^T_s Q_s
+          issue_pv64<DV>(tmem + C::kAcc0, tmem + C::pt_col(s), t1, acc, leader);   // dV += P^T_s dO_s
+          issue_pv64<DQ>(tmem + C::kAcc1, tmem + C::dst_col(s), t0, acc, leader);  // dK += dS^T_s Q_s
         } else {
-          issue_pv64<D>(tmem + 256u, tmem + bwd_s_col(s), t0, acc, leader);  // dQ += dS_s K_s
+          issue_pv64<DQ>(tmem + C::kAcc0, tmem + C::s_col(s), t0, acc, leader);    // dQ += dS_s K_s
         }
         mma_commit(bar(L::bTEmpty + slot), leader);  // this half is no longer read
         if (it + 1 < tk.nit) {
@@ -529,6 +609,13 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
           if (!wait(bar(L::bTFull + nslot), half_parity(slot_it + 1, s), kSiteBwdMmaT)) goto out;
           tc_fence_after();
           issue_sdp(s, nslot);
+        }
+      }
+      if constexpr (C::kShare) {  // dP of the next block, once each stage has read its S
+        if (it + 1 < tk.nit) {
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+            if (!issue_dp(s, half_slot(slot_it + 1, s))) goto out;
         }
       }
     }
@@ -543,9 +630,9 @@ out:
 // ---------------------------------------------------------------------------
 // TMA loads (warp 9, one lane)
 // ---------------------------------------------------------------------------
-template <int D, int KIND>
+template <int DQ, int DV, int KIND>
 __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t sbase, const WaitCtx& wc) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<DQ, DV>;
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t res_uses = 0;
@@ -559,11 +646,11 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
   for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
     const BwdTask tk = bwd_task<KIND>(p, task);
     if (res_uses > 0 && !mbar_wait(bar(L::bResEmpty), (res_uses - 1u) & 1u, wc, kSiteBwdLoadRes)) goto out;
-    mbar_arrive_expect_tx(bar(L::bResFull), 2u * L::kTile);
-    for (int c = 0; c < L::NC; ++c) {
+    mbar_arrive_expect_tx(bar(L::bResFull), static_cast<uint32_t>(L::kTile0 + L::kTile1));
+    for (int c = 0; c < L::NCQ; ++c)
       tma_load_4d(sbase + L::oR0 + c * kChunkBytes, &p.tm_r0, bar(L::bResFull), c * 64, tk.h, tk.blk * kBM, tk.b);
+    for (int c = 0; c < L::NCV; ++c)
       tma_load_4d(sbase + L::oR1 + c * kChunkBytes, &p.tm_r1, bar(L::bResFull), c * 64, tk.h, tk.blk * kBM, tk.b);
-    }
     ++res_uses;
     for (int it = 0; it < tk.nit; ++it) {
       const BwdIter bi = bwd_iter<KIND>(p, tk, it);
@@ -573,14 +660,13 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
             !mbar_wait(bar(L::bTEmpty + slot), static_cast<uint32_t>(half_it / L::NSLOT - 1) & 1u, wc,
                        kSiteBwdLoadT))
           goto out;
-        const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf;
+        const uint32_t t0 = sbase + L::slot_off(slot), t1 = t0 + L::kHalf0;
         const uint32_t fb = bar(L::bTFull + slot);
         const int row = bi.blk * kBM + 64 * s;
-        mbar_arrive_expect_tx(fb, 2u * L::kHalf + (KIND == kBwdDkDv ? 2u * L::kVecH : 0u));
-        for (int c = 0; c < L::NC; ++c) {
-          tma_load_4d(t0 + c * L::kHalfChunk, &p.tm_t0, fb, c * 64, bi.head, row, tk.b);
-          tma_load_4d(t1 + c * L::kHalfChunk, &p.tm_t1, fb, c * 64, bi.head, row, tk.b);
-        }
+        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(L::kHalf0 + L::kHalf1) +
+                                      (KIND == kBwdDkDv ? 2u * L::kVecH : 0u));
+        for (int c = 0; c < L::NCQ; ++c) tma_load_4d(t0 + c * L::kHalfChunk, &p.tm_t0, fb, c * 64, bi.head, row, tk.b);
+        for (int c = 0; c < L::NCV; ++c) tma_load_4d(t1 + c * L::kHalfChunk, &p.tm_t1, fb, c * 64, bi.head, row, tk.b);
         if (KIND == kBwdDkDv) {  // LSE and D of these 64 queries (whole padded blocks: always in range)
           const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + bi.head) * p.sq_pad + row;
           const uint32_t vdst = sbase + L::vec_off(slot);
@@ -601,9 +687,9 @@ out:
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int D, int KIND, bool CAUSAL>
+template <int DQ, int DV, int KIND, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
-  using L = BwdLayout<D>;
+  using L = BwdLayout<DQ, DV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -630,6 +716,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     mbar_init(b + 8 * L::bAccFree, 256);
     mbar_init(b + 8 * L::bDrain, 1);
     mbar_init(b + 8 * L::bAReady, 256);
+    for (int st = 0; st < 2; ++st) {
+      mbar_init(b + 8 * (L::bSRead + st), 128);
+      mbar_init(b + 8 * (L::bDpFull + st), 1);
+    }
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -644,12 +734,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (warp < 8) {
-    bwd_row_role<D, KIND, CAUSAL>(p, warp >> 2, tmem, sbase, smem, wc);
+    bwd_row_role<DQ, DV, KIND, CAUSAL>(p, warp >> 2, tmem, sbase, smem, wc);
   } else if (warp == 8) {
-    bwd_mma_role<D, KIND>(p, tmem, sbase, wc);
+    bwd_mma_role<DQ, DV, KIND>(p, tmem, sbase, wc);
     __syncwarp();
   } else if (warp == 9) {
-    if (lane == 0) bwd_load_role<D, KIND>(p, sbase, wc);
+    if (lane == 0) bwd_load_role<DQ, DV, KIND>(p, sbase, wc);
     __syncwarp();
   }
 

@@ -12,11 +12,11 @@ struct BwdEntry {
   cudaError_t (*launch)(const BwdParams& p, int grid, cudaStream_t stream);
 };
 
-// false when (d, kind, causal) is not built
-bool bwd_entry(int d, int kind, int causal, BwdEntry* out);
+// false when (d_qk, d_v, kind, causal) is not built
+bool bwd_entry(int dq, int dv, int kind, int causal, BwdEntry* out);
 
-// D = rowsum(dO * O) and LSE * log2(e) per row, padded to whole 128-row blocks
-cudaError_t launch_bwd_prep(int d, const void* o, const void* dout, const float* lse, float* l2, float* dvec, int B,
+// D = rowsum(dO * O) (over d_v) and LSE * log2(e) per row, padded to whole 128-row blocks
+cudaError_t launch_bwd_prep(int dv, const void* o, const void* dout, const float* lse, float* l2, float* dvec, int B,
                             int Hq, int Sq, int sq_pad, int max_blocks, cudaStream_t stream);
 
 }  // namespace fa

@@ -244,10 +244,11 @@ int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, in
  * dQ = scale dS K, dK = scale dS^T Q).  A shared key/value head (GQA/MQA)
  * receives the sum over its query heads.
  *
- * Layouts as fa_fwd: q, o, dout, dq [batch, seqlen_q, heads_q, d];
- * k, v, dk, dv [batch, seqlen_k, heads_kv, d]; lse [batch, heads_q, seqlen_q]
- * fp32 as fa_fwd writes it.  d_qk == d_v in {64, 128} (FA_ERR_UNSUPPORTED
- * otherwise).  dq, dk, dv are written whole (bf16).
+ * Layouts as fa_fwd: q, dq [batch, seqlen_q, heads_q, d_qk]; o, dout
+ * [batch, seqlen_q, heads_q, d_v]; k, dk [batch, seqlen_k, heads_kv, d_qk];
+ * v, dv [batch, seqlen_k, heads_kv, d_v]; lse [batch, heads_q, seqlen_q] fp32
+ * as fa_fwd writes it.  (d_qk, d_v) in {(64, 64), (128, 128), (192, 128)}
+ * (FA_ERR_UNSUPPORTED otherwise).  dq, dk, dv are written whole (bf16).
  *
  * workspace: device memory, 16-byte aligned, at least
  * fa_bwd_workspace_size(batch, heads_q, seqlen_q) bytes: D and lse * log2(e) per query row, padded to
@@ -258,7 +259,8 @@ int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, in
  * writes dK = dV = 0; seqlen_k == 0 writes dQ = 0.  fa_options: grid,
  * timeout_s and debug_flags (bit 0: the row warps never signal P ready, so a
  * bounded wait expires and fa_device_status reports FA_ERR_DEVICE_TIMEOUT)
- * apply; pack > 1, exp_emu and workspace do not (FA_ERR_UNSUPPORTED when set).
+ * apply; pack > 1, exp_emu, workspace, trace and stagger do not
+ * (FA_ERR_UNSUPPORTED when set).
  */
 size_t fa_bwd_workspace_size(int batch, int heads_q, int seqlen_q);
 
