@@ -394,14 +394,14 @@ struct Counts {
 
 // Check sites recorded with FA_ERR_DEVICE_CHECK
 enum : unsigned int {
-  kSiteCheckTask = 601,      // a decoded task outside the problem
-  kSiteCheckQCoord = 602,    // a Q tile coordinate outside the tensor
-  kSiteCheckKvCoord = 603,   // a K/V tile coordinate outside the tensor
-  kSiteCheckSmem = 604,      // the shared-memory layout past the launch's dynamic size
-  kSiteCheckTmem = 605,      // TMEM base not at lane 0 / column 0, or a lane quadrant off its warp
-  kSiteCheckOStore = 606,    // an output row or tile outside O
-  kSiteCheckLse = 607,       // an LSE index outside lse
-  kSiteCheckCounts = 610,    // + i: the i-th hand-off count comparison failed
+  kSiteCheckTask = 701,      // a decoded task outside the problem
+  kSiteCheckQCoord = 702,    // a Q tile coordinate outside the tensor
+  kSiteCheckKvCoord = 703,   // a K/V tile coordinate outside the tensor
+  kSiteCheckSmem = 704,      // the shared-memory layout past the launch's dynamic size
+  kSiteCheckTmem = 705,      // TMEM base not at lane 0 / column 0, or a lane quadrant off its warp
+  kSiteCheckOStore = 706,    // an output row or tile outside O
+  kSiteCheckLse = 707,       // an LSE index outside lse
+  kSiteCheckCounts = 710,    // + i: the i-th hand-off count comparison failed
 };
 
 __device__ __forceinline__ bool dbg_check(bool ok, const WaitCtx& wc, unsigned site) {

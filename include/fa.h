@@ -116,8 +116,8 @@ typedef struct fa_options {
                          memory extent and output index before use and, at exit, that each
                          hand-off between the roles was produced as often as it was
                          consumed.  A failed check skips the access, aborts the CTA and
-                         records FA_ERR_DEVICE_CHECK with its site (601-607 for the range
-                         checks, 610 + i for the hand-off counts) in the status word; the
+                         records FA_ERR_DEVICE_CHECK with its site (701-707 for the range
+                         checks, 710 + i for the hand-off counts) in the status word; the
                          output is then not valid.  The output of a clean run is identical
                          to the default kernel's.  Bit 3 (with bit 2 only): plant a fault
                          for the checks to catch: task 0 decodes to batch index = batch.
@@ -379,15 +379,19 @@ int fa_varlen_plan_host(const int* cu_seqlens_q, const int* cu_seqlens_k, int ba
 
 /*
  * Synchronise `stream`, then read and clear the current device's status
- * word.  *out receives FA_OK, FA_ERR_DEVICE_TIMEOUT or FA_ERR_INVALID_ARG (a
- * varlen call found bad cu_seqlens).  Returns FA_OK or FA_ERR_CUDA.
+ * word.  *out receives FA_OK, FA_ERR_DEVICE_TIMEOUT, FA_ERR_DEVICE_CHECK (a
+ * check of the checking build failed) or FA_ERR_INVALID_ARG (a varlen call
+ * found bad cu_seqlens).  Returns FA_OK or FA_ERR_CUDA.
  */
 int fa_device_status(fa_stream_t stream, int* out);
 
 /*
  * The same, with the recorded detail: detail (may be NULL) receives {code,
  * site, block or sequence index}, the site being the wait or check that
- * failed (role * 100 + barrier for a timed-out wait).
+ * failed: 101-404 a forward wait (role * 100 + barrier: 1 softmax,
+ * 2 correction, 3 MMA, 4 TMA), 501 bad cu_seqlens, 502 a varlen batch with
+ * more tasks than the workspace holds, 601-623 a backward wait,
+ * 701-707 a range check and 710 + i a hand-off count of the checking build.
  */
 int fa_device_status_detail(fa_stream_t stream, int* out, unsigned int detail[3]);
 

@@ -123,7 +123,7 @@ def test_checking_build_catches_planted_fault(fa, causal):
     fa.attention_forward(q, k, v, causal=causal, options=opts)
     code, detail = fa.fa_device_status()
     assert code == fa.FA_ERR_DEVICE_CHECK, (code, detail)
-    assert detail[0] == 5 and detail[1] == 601, detail
+    assert detail[0] == 5 and detail[1] == 701, detail
     assert fa.fa_device_status()[0] == fa.FA_OK
     # the context still computes correctly
     o, lse = fa.attention_forward(q, k, v, causal=causal)
