@@ -177,10 +177,14 @@ class ClockSampler:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; a stored ncu traffic figure is valid only for it."""
+    """Hash of the sources the forward kernels are built from (the backward's
+    and the debug instantiations' files excluded); a stored ncu figure is
+    valid only for it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_forward_08_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name.startswith(("fa_bwd", "fa_dbg_", "fa_var_")):
+            continue
         if name.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
