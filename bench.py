@@ -871,7 +871,8 @@ def trace_run(args) -> dict:
 
 def count_rescales(args) -> dict:
     """One forward launch of a fixed-length workload with the correction warps'
-    O-rescale counter on (fa_options.debug_flags bit 1)."""
+    O-rescale counter on (fa_options.debug_flags bit 1), in the checking build
+    (bit 2), whose arithmetic and rescale decisions are the default kernel's."""
     import numpy as np
     import torch
     import exact_attention_forward_08_gb300 as fa
@@ -882,8 +883,7 @@ def count_rescales(args) -> dict:
     to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
     q, k, v = (to_dev(a) for a in w.generate())
     opts = fa.default_options()
-    opts.debug_flags = fa.DEBUG_COUNT_RESCALE
-    opts.exp_emu = 1  # the counter is compiled into the FMA-exp2 kernel only (same rescale decisions)
+    opts.debug_flags = fa.DEBUG_COUNT_RESCALE | fa.DEBUG_CHECKS
     fa.fa_device_status()
     fa.attention_forward(q, k, v, causal=w.causal, scale=w.softmax_scale, options=opts)
     n = fa.fa_debug_rescale_count()

@@ -434,8 +434,9 @@ int validate_common(int heads_q, int heads_kv, int d_qk, int d_v, float scale, c
       (opt.trace_ctas < 1 || opt.trace_cap < 1 || (reinterpret_cast<uintptr_t>(opt.trace) & 7u) != 0))
     return FA_ERR_INVALID_ARG;
   if (opt.exp_emu != 0 && opt.exp_emu != 1) return FA_ERR_INVALID_ARG;
-  // the O-rescale counter is compiled into the FMA-exp2 kernels only
-  if ((opt.debug_flags & fa::kDebugCountRescale) != 0 && opt.exp_emu != 1) return FA_ERR_UNSUPPORTED;
+  // the O-rescale counter is compiled into the FMA-exp2 kernels and the checking build only
+  if ((opt.debug_flags & fa::kDebugCountRescale) != 0 && opt.exp_emu != 1 && !(opt.debug_flags & fa::kDebugChecks))
+    return FA_ERR_UNSUPPORTED;
   if (opt.store_mode < 0 || opt.store_mode > 2) return FA_ERR_INVALID_ARG;
   if (opt.no_balance != 0 && opt.no_balance != 1) return FA_ERR_INVALID_ARG;
   if (opt.stagger != 0 && opt.stagger != 1) return FA_ERR_INVALID_ARG;

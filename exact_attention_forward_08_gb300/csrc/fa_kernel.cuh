@@ -675,9 +675,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 // ---------------------------------------------------------------------------
 // correction + epilogue (WG2)
 // ---------------------------------------------------------------------------
-// COUNT: the FMA-exp2 ablation kernel also counts O rescales (debug_flags bit
-// 1); the rescale decisions do not depend on how the exponentials are taken,
-// and the default kernels carry no counting code.
+// COUNT: the FMA-exp2 ablation kernel and the checking build also count O
+// rescales (debug_flags bit 1); the rescale decisions do not depend on how the
+// exponentials are taken, and the default kernels carry no counting code.
 template <int DQ, int DV, bool CAUSAL, bool VARLEN, bool DYN, bool SPLIT, bool DIRECT, bool COUNT, int VAR>
 __device__ __forceinline__ void correction_role(const Params& p, const uint32_t tmem, const uint32_t sbase,
                                                 uint8_t* smem, float* mbox, const volatile int* ring,
@@ -1394,7 +1394,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                                                                       dbg_area, wc);
   } else if (warp < 12) {
     setmaxnreg_dec<104>();
-    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT, EMU, VAR>(p, tmem, sbase, smem, mbox, ring,
+    correction_role<DQ, DV, CAUSAL, VARLEN, DYN, SPLIT, DIRECT, EMU || (VAR & kVarCheck) != 0, VAR>(p, tmem, sbase, smem, mbox, ring,
                                                                            dbg_area, wc);
   } else {
     setmaxnreg_dec<56>();

@@ -106,9 +106,10 @@ typedef struct fa_options {
                          block after the first, the correction warps' rescales of O (the
                          TMEM round trip run when some row of the warp moved its reference
                          by more than tau); read with fa_debug_rescale_count().  Needs
-                         exp_emu = 1 (the counter lives in that ablation kernel only, so the
-                         default kernels carry no counting code; the rescale decisions do not
-                         depend on how the exponentials are computed), else
+                         exp_emu = 1 or bit 2 (the counter lives in the FMA-exp2 ablation
+                         kernel and in the checking build, whose arithmetic is the default
+                         kernel's, so the default kernels carry no counting code; the rescale
+                         decisions do not depend on how the exponentials are computed), else
                          FA_ERR_UNSUPPORTED.  The output is unchanged.
                          Bit 2 (fixed-length forward with static assignment, no exp_emu):
                          run the checking build of the kernel, which checks every decoded

@@ -14,6 +14,12 @@ and P arrivals per stage as the host plan gives K/V blocks to that CTA's
 tiles, in increasing clock order.
 
 Staggered-exponential ablation (fa_options.stagger): bit-identical output.
+
+O-rescale counter (debug bit 1) in the checking build, whose arithmetic is the
+default kernel's: on causal problems (the same task decomposition in every
+build) it counts exactly what the FMA-exp2 ablation kernel counts, since the
+rescale decisions depend only on the scores' row maxima, not on how the
+exponentials are taken; and it counts rescales on the wide-range input.
 """
 import zlib
 
@@ -231,3 +237,30 @@ def test_stagger_build_bitwise_equal(fa, case):
         code, detail = fa.fa_device_status()
         assert code == fa.FA_OK, detail
         assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1]), store_mode
+
+
+RESCALE_CASES = [c for c in SMALL if c[0] in ("causal384", "gqa4", "asym_offset", "many_tasks")]
+
+
+@pytest.mark.parametrize("case", RESCALE_CASES, ids=[c[0] for c in RESCALE_CASES])
+def test_rescale_counter_in_checking_build(fa, case):
+    w = workload(case)
+    q, k, v = (to_dev(a) for a in w.generate())
+    assert fa.fa_device_status()[0] == fa.FA_OK
+    counts = []
+    for flags, emu in ((fa.DEBUG_CHECKS | fa.DEBUG_COUNT_RESCALE, 0), (fa.DEBUG_COUNT_RESCALE, 1)):
+        opts = fa.default_options()
+        opts.debug_flags, opts.exp_emu = flags, emu
+        fa.fa_debug_rescale_count()  # clear
+        fa.attention_forward(q, k, v, causal=w.causal, scale=w.softmax_scale, options=opts)
+        counts.append(fa.fa_debug_rescale_count())
+        assert fa.fa_device_status()[0] == fa.FA_OK
+    assert counts[0] == counts[1], counts
+    if case[0] == "asym_offset":
+        assert counts[0] > 0
+    # without either build the counter is refused
+    opts = fa.default_options()
+    opts.debug_flags = fa.DEBUG_COUNT_RESCALE
+    with pytest.raises(fa.FaError) as e:
+        fa.attention_forward(q, k, v, causal=w.causal, scale=w.softmax_scale, options=opts)
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED
