@@ -73,6 +73,8 @@ def parse_args(argv=None):
                          "time of the trace build beside the default kernel's, instead of timing")
     ap.add_argument("--trace-ctas", type=int, default=8)
     ap.add_argument("--trace-cap", type=int, default=16384)
+    ap.add_argument("--trace-out", default=None,
+                    help="with --trace: also write the decoded per-CTA event lists (JSON) to this file")
     ap.add_argument("--count-rescales", action="store_true",
                     help="fixed-length forward: run the workload once with the O-rescale counter on and print the "
                          "count, the most the launch could count (warps x K/V blocks after a tile's first) and their "
@@ -863,6 +865,9 @@ def trace_run(args) -> dict:
     host = buf.cpu().numpy().view(np.uint64)
     ctas = tr.decode(host, args.trace_ctas, args.trace_cap)
     dropped = sum(max(0, n - args.trace_cap) for c in ctas for n in c["_counts"].values())
+    if args.trace_out:
+        with open(args.trace_out, "w") as f:
+            json.dump(ctas, f)
     return {"config": args.config, "workload": f"{w.name}: {w.notes}", "trace_ctas": args.trace_ctas,
             "records_dropped": dropped, "kernel_ms_default": round(base_ms, 4),
             "kernel_ms_trace_build": round(trace_ms, 4), "unit": "SM clock cycles",

@@ -696,6 +696,11 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   uint32_t od_count[2] = {0u, 0u};  // o_done phases consumed (one per task with blocks)
   uint32_t chunks = 0;              // epilogue chunks stored through the staging tile so far
   const int num_tasks = task_count<VARLEN>(p);
+  // short-task kernels with static assignment: the next task is decoded
+  // before the current task's epilogue (while the last P V run), so that the
+  // next task's first hand-off does not wait behind the decoding
+  constexpr bool kPre = DIRECT && !DYN;
+  Task nxt{};
   Tracer<(VAR & kVarTrace) != 0, 2> tr;
   tr.init(p, t == 0);
   Counts<CK> cnt;
@@ -704,10 +709,14 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
       goto out;
   }
 
+  if constexpr (kPre) {
+    const int t0 = read_task<DQ, DV, DYN>(0, num_tasks, bar0, ring, wc, kSiteCorrTask);
+    if (t0 >= 0) nxt = get_task<VARLEN, SPLIT, CAUSAL, DIRECT, !DYN>(p, t0);
+  }
   for (int kt = 0;; ++kt) {
     const int task = read_task<DQ, DV, DYN>(kt, num_tasks, bar0, ring, wc, kSiteCorrTask);
     if (task < 0) break;  // no task left, or an abort
-    Task tk = get_task<VARLEN, SPLIT, CAUSAL, DIRECT, !DYN>(p, task);
+    Task tk = kPre ? nxt : get_task<VARLEN, SPLIT, CAUSAL, DIRECT, !DYN>(p, task);
     if (!check_task<CK>(p, tk, task, wc)) break;
     tr.ev(p, kEvCoTask, static_cast<uint32_t>(task));
     float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
@@ -761,6 +770,10 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
     // task record is read again here rather than kept in registers across
     // the K/V loop (this role runs at 104 registers).
     if constexpr (VARLEN) tk = get_task<VARLEN, false, CAUSAL, false, false>(p, opaque_i32(task));
+    if constexpr (kPre) {
+      const int t1 = read_task<DQ, DV, DYN>(kt + 1, num_tasks, bar0, ring, wc, kSiteCorrTask);
+      if (t1 >= 0) nxt = get_task<VARLEN, SPLIT, CAUSAL, DIRECT, !DYN>(p, t1);
+    }
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       // key-split tail task: one output tile, both halves merged at s = 0
