@@ -68,9 +68,10 @@ def parse_args(argv=None):
     ap.add_argument("--splitkv", type=int, default=0,
                     help="split-KV ranges for fixed-length workloads (decode workloads always split; 0 = auto there)")
     ap.add_argument("--trace", action="store_true",
-                    help="fixed-length forward: run the workload once with the kernel's event log (trace build) on "
-                         "the first --trace-ctas CTAs and print the interval summary (cycles), with the mean launch "
-                         "time of the trace build beside the default kernel's, instead of timing")
+                    help="fixed-length forward (or, with --pass bwd, backward at head dims 128): run the workload "
+                         "once with the kernel's event log (trace build) on the first --trace-ctas CTAs and print the "
+                         "interval summary (cycles), with the mean time of the trace build beside the default "
+                         "kernel's, instead of timing")
     ap.add_argument("--trace-ctas", type=int, default=8)
     ap.add_argument("--trace-cap", type=int, default=16384)
     ap.add_argument("--trace-out", default=None,
@@ -874,6 +875,59 @@ def trace_run(args) -> dict:
             "summary": tr.summarize(ctas)}
 
 
+def trace_run_bwd(args) -> dict:
+    """One backward call (dK/dV and dQ kernels) of a fixed-length (128, 128)
+    workload with the event log on, and the interval summary of each kernel."""
+    import numpy as np
+    import torch
+    import exact_attention_forward_08_gb300 as fa
+    import synthetic
+    from exact_attention_forward_08_gb300 import trace as tr
+    w = get_workload(args.config)
+    if is_varlen(w) or is_decode(args.config):
+        raise SystemExit("--trace takes a fixed-length --config")
+    fa.load_library()
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    q, k, v = (to_dev(a) for a in w.generate())
+    g = to_dev(synthetic.normal_bf16(w.shapes["o"], w.seed, 7))
+    o, lse = fa.attention_forward(q, k, v, causal=w.causal, scale=w.softmax_scale)
+    words = tr.trace_words(args.trace_ctas, args.trace_cap)
+    buf = torch.zeros(2 * words, dtype=torch.int64, device="cuda")
+    topts = fa.default_options()
+    topts.trace = buf.data_ptr()
+    topts.trace_ctas = args.trace_ctas
+    topts.trace_cap = args.trace_cap
+
+    def mean_ms(opts, n=5):
+        for _ in range(2):
+            fa.attention_backward(q, k, v, o, lse, g, causal=w.causal, scale=w.softmax_scale, options=opts)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fa.attention_backward(q, k, v, o, lse, g, causal=w.causal, scale=w.softmax_scale, options=opts)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    base_ms = mean_ms(None)
+    trace_ms = mean_ms(topts)
+    buf.zero_()
+    fa.attention_backward(q, k, v, o, lse, g, causal=w.causal, scale=w.softmax_scale, options=topts)
+    torch.cuda.synchronize()
+    code, detail = fa.fa_device_status()
+    if code != 0:
+        raise SystemExit(f"device status {code} {detail}")
+    host = buf.cpu().numpy().view(np.uint64)
+    out = {"config": args.config, "pass": "bwd", "workload": f"{w.name}: {w.notes}", "trace_ctas": args.trace_ctas,
+           "call_ms_default": round(base_ms, 4), "call_ms_trace_build": round(trace_ms, 4),
+           "unit": "SM clock cycles"}
+    for kind, name in ((0, "dkdv"), (1, "dq")):
+        ctas = tr.decode(host[kind * words:(kind + 1) * words], args.trace_ctas, args.trace_cap)
+        out[f"{name}_records_dropped"] = sum(max(0, n - args.trace_cap) for c in ctas for n in c["_counts"].values())
+        out[f"{name}_summary"] = tr.summarize_bwd(ctas)
+    return out
+
+
 def count_rescales(args) -> dict:
     """One forward launch of a fixed-length workload with the correction warps'
     O-rescale counter on (fa_options.debug_flags bit 1), in the checking build
@@ -913,7 +967,7 @@ def main(argv=None):
         print(json.dumps(count_rescales(args)), flush=True)
         return 0
     if args.trace:
-        print(json.dumps(trace_run(args)), flush=True)
+        print(json.dumps(trace_run_bwd(args) if args.pass_ == "bwd" else trace_run(args)), flush=True)
         return 0
     if args.impl == "reference":
         runner = run_reference

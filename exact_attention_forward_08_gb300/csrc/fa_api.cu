@@ -59,6 +59,7 @@ struct DeviceState {
   bool kernel_ready[kNumKernels] = {};
   bool debug_ready[5 * 2 * 2 * 3] = {};  // (d_qk, d_v) pair x causal x (fixed, direct) x (trace, check, stagger)
   bool bwd_ready[3 * 2 * 2] = {};   // ((64,64), (128,128), (192,128)) x (dK/dV, dQ) x (non-causal, causal)
+  bool bwd_trace_ready[2 * 2] = {};  // the event-log build, (128,128): (dK/dV, dQ) x (non-causal, causal)
   bool plan_ready = false;
 };
 
@@ -913,10 +914,13 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
   if (opt.grid < 0 || !std::isfinite(opt.timeout_s) || opt.timeout_s > 3600.0) return FA_ERR_INVALID_ARG;
   if ((opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
-  if (opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1 || opt.trace != nullptr || opt.stagger)
-    return FA_ERR_UNSUPPORTED;
+  if (opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1 || opt.stagger) return FA_ERR_UNSUPPORTED;
+  const bool trace = opt.trace != nullptr;
+  if (trace && (opt.trace_ctas < 1 || opt.trace_cap < 1 || (reinterpret_cast<uintptr_t>(opt.trace) & 7u) != 0))
+    return FA_ERR_INVALID_ARG;
   const int pair = (d_qk == 64 && d_v == 64) ? 0 : ((d_qk == 128 && d_v == 128) ? 1 : ((d_qk == 192 && d_v == 128) ? 2 : -1));
   if (pair < 0) return FA_ERR_UNSUPPORTED;
+  if (trace && pair != 1) return FA_ERR_UNSUPPORTED;  // the event-log build is (128, 128) only
   if (batch == 0) return FA_OK;
   const int64_t big = int64_t(1) << 31;
   if (static_cast<int64_t>(seqlen_q) + seqlen_k + 4 * fa::kBM >= big) return FA_ERR_INVALID_ARG;
@@ -939,7 +943,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   if (rc != FA_OK) return rc;
   auto dev_ok = [&](const void* ptr) { return ptr == nullptr || is_device_ptr(ptr, dev); };
   if (!dev_ok(q) || !dev_ok(k) || !dev_ok(v) || !dev_ok(o) || !dev_ok(lse) || !dev_ok(dout) || !dev_ok(dq) ||
-      !dev_ok(dk) || !dev_ok(dv) || !dev_ok(workspace))
+      !dev_ok(dk) || !dev_ok(dv) || !dev_ok(workspace) || !dev_ok(opt.trace))
     return FA_ERR_INVALID_ARG;
 
   // degenerate shapes: no query (dK = dV = 0) or no key (dQ = 0)
@@ -959,15 +963,17 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
 
   fa::BwdEntry ent[2];
   for (int kind = 0; kind < 2; ++kind) {
-    if (!fa::bwd_entry(d_qk, d_v, kind, causal, &ent[kind])) return FA_ERR_UNSUPPORTED;
-    const int idx = (pair * 2 + kind) * 2 + causal;
+    const bool found = trace ? fa::bwd_trace_entry(d_qk, d_v, kind, causal, &ent[kind])
+                             : fa::bwd_entry(d_qk, d_v, kind, causal, &ent[kind]);
+    if (!found) return FA_ERR_UNSUPPORTED;
+    bool& ready = trace ? st->bwd_trace_ready[kind * 2 + causal] : st->bwd_ready[(pair * 2 + kind) * 2 + causal];
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!st->bwd_ready[idx]) {
+    if (!ready) {
       if (ent[kind].smem > st->smem_optin) return FA_ERR_UNSUPPORTED;
       if (cudaFuncSetAttribute(ent[kind].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ent[kind].smem) !=
           cudaSuccess)
         return FA_ERR_CUDA;
-      st->bwd_ready[idx] = true;
+      ready = true;
     }
   }
 
@@ -1018,6 +1024,11 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
     p.timeout_ns = static_cast<unsigned long long>(opt.timeout_s * 1e9);
     p.debug_flags = opt.debug_flags;
+    if (trace) {  // the dK/dV kernel's log first, then the dQ kernel's
+      p.trace = opt.trace + static_cast<int64_t>(kind) * opt.trace_ctas * fa::kTraceTracks * (opt.trace_cap + 1);
+      p.trace_ctas = opt.trace_ctas;
+      p.trace_cap = opt.trace_cap;
+    }
     const int64_t tasks = static_cast<int64_t>(p.units) * p.blocks;
     if (tasks >= big) return FA_ERR_INVALID_ARG;
     int64_t grid = opt.grid > 0 ? opt.grid : st->sms;

@@ -4,18 +4,6 @@
 
 namespace fa {
 
-template <int DQ, int DV, int KIND, bool CAUSAL>
-static cudaError_t launch_bwd(const BwdParams& p, int grid, cudaStream_t stream) {
-  fa_bwd_kernel<DQ, DV, KIND, CAUSAL><<<grid, kBwdThreads, BwdLayout<DQ, DV>::kDynSmem, stream>>>(p);
-  return cudaGetLastError();
-}
-
-template <int DQ, int DV, int KIND, bool CAUSAL>
-static BwdEntry make_bwd_entry() {
-  return BwdEntry{reinterpret_cast<const void*>(&fa_bwd_kernel<DQ, DV, KIND, CAUSAL>),
-                  BwdLayout<DQ, DV>::kDynSmem, &launch_bwd<DQ, DV, KIND, CAUSAL>};
-}
-
 template <int DQ, int DV>
 static BwdEntry pick_bwd(int kind, int causal) {
   if (kind == kBwdDkDv)

@@ -85,6 +85,9 @@ struct BwdParams {
   float scale, scale_log2;
   unsigned long long timeout_ns;
   int debug_flags;           // kDebugSkipPArrive: the row warps never signal p_ready (failure-path test)
+  uint64_t* trace;           // VAR & kVarTrace: [trace_ctas][kTraceTracks][1 + trace_cap] words
+  int trace_ctas;            // CTAs 0 .. trace_ctas-1 record
+  int trace_cap;             // records kept per track
 };
 
 // Streamed tiles travel as half-tiles: rows 64s .. 64s+63 of a 128-row block
@@ -330,7 +333,7 @@ __device__ __forceinline__ void issue_pv64(uint32_t d_tmem, uint32_t a_tmem, uin
 // entries (0 elsewhere), dS = P (dP - D).  dK/dV: rows are keys, columns
 // queries (LSE and D per column, from the block's vectors in the ring slot);
 // dQ: rows are queries (LSE and D per row), columns keys.
-template <int DQ, int DV, int KIND, bool CAUSAL>
+template <int DQ, int DV, int KIND, bool CAUSAL, int VAR>
 __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage, const uint32_t tmem,
                                              const uint32_t sbase, const uint8_t* smem, const WaitCtx& wc) {
   using L = BwdLayout<DQ, DV>;
@@ -348,9 +351,12 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
   const int num_tasks = p.units * p.blocks;
 
   uint32_t res_phase = 0;
+  Tracer<(VAR & kVarTrace) != 0, -1> tr;  // track = stage
+  tr.init(p, t == 0, stage);
   for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
     const BwdTask tk = bwd_task<KIND>(p, task);
     const int row = tk.blk * kBM + t;  // key (dK/dV) or query (dQ)
+    tr.ev(p, kEvBrTask, static_cast<uint32_t>(task));
     if constexpr (C::kTmemA) {
       // stage s copies its resident tile (Q or dO, row t, 128-byte swizzled
       // in SMEM) into TMEM as packed bf16 pairs.  The previous task's
@@ -383,9 +389,14 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
     for (int it = 0; it < tk.nit; ++it, ++slot_it) {
       const BwdIter bi = bwd_iter<KIND>(p, tk, it);
       const int slot = (2 * slot_it + stage) % L::NSLOT;  // this stage's half of block it
-      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (L::bSFull + stage), s_phase, wc, kSiteBwdRowS))) return;
+      tr.ev(p, kEvBrWait, static_cast<uint32_t>(it));
+      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (L::bSFull + stage), s_phase, wc, kSiteBwdRowS))) {
+        tr.finish(p);
+        return;
+      }
       s_phase ^= 1u;
       tc_fence_after();
+      tr.ev(p, kEvBrS, static_cast<uint32_t>(it));
 
       // visible columns c (0 .. 63 of this stage) in [cmin, cmax]
       int cmin = 0, cmax = 63;
@@ -463,15 +474,20 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
       tmem_wait_st();
       tc_fence_before();
       if (!(p.debug_flags & kDebugSkipPArrive)) mbar_arrive(bar0 + 8u * (L::bPReady + stage));
+      tr.ev(p, kEvBrP, static_cast<uint32_t>(it));
     }
 
     // epilogue: dK/dV: stage 0 writes dV, stage 1 dK (scaled); dQ: stage s
     // writes columns [s D/2, (s+1) D/2) (scaled)
     if (tk.nit > 0) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bAccDone, acc_phase, wc, kSiteBwdRowAcc))) return;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * L::bAccDone, acc_phase, wc, kSiteBwdRowAcc))) {
+        tr.finish(p);
+        return;
+      }
       acc_phase ^= 1u;
       tc_fence_after();
     }
+    tr.ev(p, kEvBrAcc, static_cast<uint32_t>(task));
     const bool store = KIND == kBwdDkDv ? row < p.Sk : row < p.Sq;
     uint16_t* dst;
     float mult;
@@ -513,7 +529,9 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
     }
     tc_fence_before();
     mbar_arrive(bar0 + 8u * L::bAccFree);
+    tr.ev(p, kEvBrEpi, static_cast<uint32_t>(task));
   }
+  tr.finish(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -522,7 +540,7 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
 // Per streamed block j and stage s: the accumulating GEMMs of (j, s) as soon
 // as stage s has written P / dS, then S and dP of (j+1, s), so one stage's
 // row warps work while the other stage's GEMMs run.
-template <int DQ, int DV, int KIND>
+template <int DQ, int DV, int KIND, int VAR>
 __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t tmem, const uint32_t sbase,
                                              const WaitCtx& wc) {
   using L = BwdLayout<DQ, DV>;
@@ -562,10 +580,13 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
     return true;
   };
 
+  Tracer<(VAR & kVarTrace) != 0, 3> tr;
+  tr.init(p, leader != 0);
   for (int task = blockIdx.x, n = 0; task < num_tasks; task += gridDim.x, ++n) {
     const BwdTask tk = bwd_task<KIND>(p, task);
     if (!wait(bar(L::bResFull), res_phase, kSiteBwdMmaRes)) goto out;
     res_phase ^= 1u;
+    tr.ev(p, kEvBmTask, static_cast<uint32_t>(task));
     if (n > 0) {  // the previous task's epilogue has read the accumulators
       if (!wait(bar(L::bAccFree), free_phase, kSiteBwdMmaAcc)) goto out;
       free_phase ^= 1u;
@@ -580,7 +601,9 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
       for (int s = 0; s < 2; ++s) {
         if (!wait(bar(L::bTFull + half_slot(slot_it, s)), half_parity(slot_it, s), kSiteBwdMmaT)) goto out;
         tc_fence_after();
+        tr.ev(p, kEvBmT, static_cast<uint32_t>(s << 16));
         issue_sdp(s, half_slot(slot_it, s));
+        tr.ev(p, kEvBmSdp, static_cast<uint32_t>(s << 16));
       }
       if constexpr (C::kShare) {
 #pragma unroll
@@ -596,6 +619,7 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
         if (!wait(bar(L::bPReady + s), p_phase[s], kSiteBwdMmaP)) goto out;
         p_phase[s] ^= 1u;
         tc_fence_after();
+        tr.ev(p, kEvBmP, static_cast<uint32_t>(s << 16 | it));
         const bool acc = it > 0 || s > 0;
         if (KIND == kBwdDkDv) {
           issue_pv64<DV>(tmem + C::kAcc0, tmem + C::pt_col(s), t1, acc, leader);   // dV += P^T_s dO_s
@@ -604,11 +628,14 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
           issue_pv64<DQ>(tmem + C::kAcc0, tmem + C::s_col(s), t0, acc, leader);    // dQ += dS_s K_s
         }
         mma_commit(bar(L::bTEmpty + slot), leader);  // this half is no longer read
+        tr.ev(p, kEvBmAcc, static_cast<uint32_t>(s << 16 | it));
         if (it + 1 < tk.nit) {
           const int nslot = half_slot(slot_it + 1, s);
           if (!wait(bar(L::bTFull + nslot), half_parity(slot_it + 1, s), kSiteBwdMmaT)) goto out;
           tc_fence_after();
+          tr.ev(p, kEvBmT, static_cast<uint32_t>(s << 16 | (it + 1)));
           issue_sdp(s, nslot);
+          tr.ev(p, kEvBmSdp, static_cast<uint32_t>(s << 16 | (it + 1)));
         }
       }
       if constexpr (C::kShare) {  // dP of the next block, once each stage has read its S
@@ -625,12 +652,13 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
 out:
   mma_commit(bar(L::bDrain), leader);
   mbar_drain_wait(bar(L::bDrain), 0u, wc, kSiteBwdMmaDrain);
+  tr.finish(p);
 }
 
 // ---------------------------------------------------------------------------
 // TMA loads (warp 9, one lane)
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, int KIND>
+template <int DQ, int DV, int KIND, int VAR>
 __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t sbase, const WaitCtx& wc) {
   using L = BwdLayout<DQ, DV>;
   const uint32_t bar0 = sbase + L::oBar;
@@ -643,8 +671,11 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
   tma_prefetch_desc(&p.tm_t0);
   tma_prefetch_desc(&p.tm_t1);
 
+  Tracer<(VAR & kVarTrace) != 0, 4> tr;
+  tr.init(p, true);
   for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
     const BwdTask tk = bwd_task<KIND>(p, task);
+    tr.ev(p, kEvBlTask, static_cast<uint32_t>(task));
     if (res_uses > 0 && !mbar_wait(bar(L::bResEmpty), (res_uses - 1u) & 1u, wc, kSiteBwdLoadRes)) goto out;
     mbar_arrive_expect_tx(bar(L::bResFull), static_cast<uint32_t>(L::kTile0 + L::kTile1));
     for (int c = 0; c < L::NCQ; ++c)
@@ -673,6 +704,7 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
           bulk_load(vdst, p.l2 + vi, L::kVecH, fb);
           bulk_load(vdst + L::kVecH, p.dvec + vi, L::kVecH, fb);
         }
+        tr.ev(p, kEvBlT, static_cast<uint32_t>(half_it));
       }
     }
   }
@@ -682,12 +714,14 @@ out:
     const uint32_t uses = static_cast<uint32_t>((half_it - i + L::NSLOT - 1) / L::NSLOT);
     mbar_drain_wait(bar(L::bTFull + i), (uses - 1u) & 1u, wc, kSiteBwdLoadDrain);
   }
+  tr.finish(p);
 }
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int DQ, int DV, int KIND, bool CAUSAL>
+// VAR: 0, or kVarTrace for the event-log build
+template <int DQ, int DV, int KIND, bool CAUSAL, int VAR = 0>
 __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdLayout<DQ, DV>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -734,12 +768,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
 
   if (warp < 8) {
-    bwd_row_role<DQ, DV, KIND, CAUSAL>(p, warp >> 2, tmem, sbase, smem, wc);
+    bwd_row_role<DQ, DV, KIND, CAUSAL, VAR>(p, warp >> 2, tmem, sbase, smem, wc);
   } else if (warp == 8) {
-    bwd_mma_role<DQ, DV, KIND>(p, tmem, sbase, wc);
+    bwd_mma_role<DQ, DV, KIND, VAR>(p, tmem, sbase, wc);
     __syncwarp();
   } else if (warp == 9) {
-    if (lane == 0) bwd_load_role<DQ, DV, KIND>(p, sbase, wc);
+    if (lane == 0) bwd_load_role<DQ, DV, KIND, VAR>(p, sbase, wc);
     __syncwarp();
   }
 

@@ -311,9 +311,10 @@ __device__ __forceinline__ void mbar_drain_wait(uint32_t bar, uint32_t parity, c
 // debug instantiations: the event log and the checks
 // ---------------------------------------------------------------------------
 // Event log: track = role (softmax stage 0, softmax stage 1, correction, MMA,
-// TMA); a record is one 64-bit word {code (bits 56-63), argument (bits
-// 32-55), clock64 low 32 bits}.  Word 0 of a track holds its record count
-// (records past trace_cap are counted, not kept).
+// TMA; in the backward: row warps of stage 0 and 1, unused, MMA, TMA); a
+// record is one 64-bit word {code (bits 56-63), argument (bits 32-55),
+// clock64 low 32 bits}.  Word 0 of a track holds its record count (records
+// past trace_cap are counted, not kept).
 constexpr int kTraceTracks = 5;
 enum : uint32_t {
   // softmax (argument: block j; task: task index)
@@ -324,28 +325,38 @@ enum : uint32_t {
   kEvMmTask = 32, kEvMmKv = 33, kEvMmQ = 34, kEvMmP = 35, kEvMmPV = 36, kEvMmQK = 37,
   // TMA (argument: stage or ring tile)
   kEvLdTask = 48, kEvLdQ = 49, kEvLdKvWait = 50, kEvLdKv = 51,
+  // backward, row warps of stage s (tracks 0 / 1; argument: streamed block of the task, or task)
+  kEvBrTask = 64, kEvBrWait = 65, kEvBrS = 66, kEvBrP = 67, kEvBrAcc = 68, kEvBrEpi = 69,
+  // backward, MMA warp (track 3; argument: stage << 16 | block, or task)
+  kEvBmTask = 80, kEvBmP = 81, kEvBmAcc = 82, kEvBmT = 83, kEvBmSdp = 84,
+  // backward, TMA thread (track 4; argument: half-tile index, or task)
+  kEvBlTask = 96, kEvBlT = 97,
 };
 
 // Keeps two registers per recording role (the record count and the on
 // flag; a third for the track when TRACK < 0, i.e. chosen at run time): the
 // track's address is recomputed from the kernel parameters, which live in
-// parameter space, at each record.
+// parameter space, at each record.  PARAMS is the forward's Params or the
+// backward's BwdParams (both carry trace, trace_ctas and trace_cap).
 template <bool ON, int TRACK>
 struct Tracer {
   uint32_t n = 0;
   bool on = false;
   int track = TRACK;
-  __device__ __forceinline__ void init(const Params& p, bool recorder, int trk = TRACK) {
+  template <class PARAMS>
+  __device__ __forceinline__ void init(const PARAMS& p, bool recorder, int trk = TRACK) {
     if constexpr (ON) {
       on = recorder && p.trace != nullptr && static_cast<int>(blockIdx.x) < p.trace_ctas;
       if constexpr (TRACK < 0) track = trk;
     }
   }
-  __device__ __forceinline__ uint64_t* base(const Params& p) const {
+  template <class PARAMS>
+  __device__ __forceinline__ uint64_t* base(const PARAMS& p) const {
     const int tr = TRACK < 0 ? track : TRACK;
     return p.trace + (static_cast<int64_t>(blockIdx.x) * kTraceTracks + tr) * (p.trace_cap + 1);
   }
-  __device__ __forceinline__ void ev(const Params& p, uint32_t code, uint32_t arg) {
+  template <class PARAMS>
+  __device__ __forceinline__ void ev(const PARAMS& p, uint32_t code, uint32_t arg) {
     if constexpr (ON) {
       if (on) {
         if (n < static_cast<uint32_t>(p.trace_cap))
@@ -355,7 +366,8 @@ struct Tracer {
       }
     }
   }
-  __device__ __forceinline__ void finish(const Params& p) {
+  template <class PARAMS>
+  __device__ __forceinline__ void finish(const PARAMS& p) {
     if constexpr (ON) {
       if (on) base(p)[0] = n;
     }

@@ -15,6 +15,12 @@ MMA warp's latency to see P and its issue times; the
 latency from a Q K^T issue to the softmax seeing S; the period of a stage's
 blocks; and, per task boundary, the gap between one task's last P V and the
 next task's first.  Times are in SM clock cycles.
+
+``summarize_bwd`` does the same for the backward kernels' log (one kernel's
+half of the buffer): per 64-row stage and streamed block, the row warps'
+wait for S and dP and their work to P (and dS) stored, the MMA warp's issue
+of the accumulating GEMMs and of the next S and dP, its waits, and the
+hand-offs between them.
 """
 from __future__ import annotations
 
@@ -26,6 +32,10 @@ EVENTS = {
     16: "co_task", 17: "co_corr", 18: "co_rescaled", 19: "co_arrive", 20: "co_odone", 21: "co_epi",
     32: "mm_task", 33: "mm_kv", 34: "mm_q", 35: "mm_p", 36: "mm_pv", 37: "mm_qk",
     48: "ld_task", 49: "ld_q", 50: "ld_kvwait", 51: "ld_kv",
+    # backward (tracks softmax0 / softmax1 = row warps of stage 0 / 1, mma, tma)
+    64: "br_task", 65: "br_wait", 66: "br_s", 67: "br_p", 68: "br_acc", 69: "br_epi",
+    80: "bm_task", 81: "bm_p", 82: "bm_acc", 83: "bm_t", 84: "bm_sdp",
+    96: "bl_task", 97: "bl_t",
 }
 CODES = {v: k for k, v in EVENTS.items()}
 
@@ -178,6 +188,90 @@ def summarize(ctas) -> dict:
         for t, it in ld:
             if it in kv:
                 add("tma.tile_issue_to_mma_ready", kv[it] - t)
+        span = [t for name in TRACKS for t, _, _ in cta[name]]
+        if span:
+            add("cta.span", max(span) - min(span))
+    return {k: _stats(v) for k, v in sorted(acc.items())}
+
+
+def summarize_bwd(ctas) -> dict:
+    """Interval statistics of the backward event log over every decoded CTA
+    (cycles).  Row events carry the streamed block `it` of the task, MMA
+    events stage << 16 | it."""
+    acc = {}
+
+    def add(key, v):
+        acc.setdefault(key, []).append(v)
+
+    for cta in ctas:
+        br_s = {0: [], 1: []}
+        br_p = {0: [], 1: []}
+        for s in (0, 1):
+            cur = {}
+            for t, ev, arg in cta[f"softmax{s}"]:
+                if ev == "br_wait":
+                    cur = {"wait": t, "it": arg}
+                elif ev == "br_s":
+                    cur["s"] = t
+                    br_s[s].append((t, arg))
+                elif ev == "br_p":
+                    br_p[s].append((t, arg))
+                    if "wait" in cur and "s" in cur:
+                        tag = "first" if cur["it"] == 0 else "steady"
+                        add(f"row.{tag}.wait_for_S", cur["s"] - cur["wait"])
+                        add(f"row.{tag}.work_S_to_P", t - cur["s"])
+                elif ev == "br_acc":
+                    cur = {"acc": t}
+                elif ev == "br_epi" and "acc" in cur:
+                    add("row.epilogue", t - cur["acc"])
+            for (t0, i0), (t1, i1) in zip(br_p[s], br_p[s][1:]):
+                if i1 == i0 + 1:
+                    add("stage.block_period", t1 - t0)
+        bm_p = {0: [], 1: []}
+        bm_sdp = {0: [], 1: []}
+        last = None
+        last_acc = None
+        task_last_acc, task_first_acc = [], []
+        first_in_task = True
+        for t, ev, arg in cta["mma"]:
+            s = _stage_of(arg)
+            if ev == "bm_task":
+                if last_acc is not None:
+                    task_last_acc.append(last_acc)
+                first_in_task = True
+                last = t
+            elif ev == "bm_p":
+                bm_p[s].append((t, _block_of(arg)))
+                if last is not None:
+                    add("mma.wait_for_P", t - last)
+                last = t
+            elif ev == "bm_acc":
+                if last is not None:
+                    add("mma.issue_acc", t - last)
+                if first_in_task:
+                    task_first_acc.append(t)
+                    first_in_task = False
+                last = last_acc = t
+            elif ev == "bm_t":
+                if last is not None:
+                    add("mma.wait_T", t - last)
+                last = t
+            elif ev == "bm_sdp":
+                bm_sdp[s].append((t, _block_of(arg)))
+                if last is not None:
+                    add("mma.issue_S_dP", t - last)
+                last = t
+        for s in (0, 1):
+            for (tr_, _), (tm, _) in zip(br_p[s], bm_p[s]):
+                add("handoff.row_P_to_mma_P", tm - tr_)
+            for (tq, _), (ts, _) in zip(bm_sdp[s], br_s[s]):
+                add("handoff.S_dP_issue_to_row_S", ts - tq)
+        for a, b in zip(task_last_acc, task_first_acc[1:]):
+            add("task.last_acc_to_next_first_acc", b - a)
+        issued = [t for t, ev, _ in cta["tma"] if ev == "bl_t"]
+        ready = [t for t, ev, _ in cta["mma"] if ev == "bm_t"]
+        for a, b in zip(issued, ready):
+            add("tma.half_tile_issue_to_mma_ready", b - a)
         span = [t for name in TRACKS for t, _, _ in cta[name]]
         if span:
             add("cta.span", max(span) - min(span))

@@ -164,7 +164,10 @@ typedef struct fa_options {
                          32 bits}, stamped by lane 0 of the role's first warp at each step
                          of the hand-off protocol: the waits and arrivals of each role (codes
                          in csrc/fa_kernel.cuh).  A separate kernel build; the output is
-                         identical to the default kernel's. */
+                         identical to the default kernel's.  fa_bwd_ex takes it too (head
+                         dims (128, 128)): twice the words, the dK/dV kernel's log first,
+                         then the dQ kernel's, each with the tracks row warps of stage 0,
+                         row warps of stage 1, (unused), MMA, TMA. */
   int trace_ctas;     /* CTAs that record (>= 1 when trace is set) */
   int trace_cap;      /* records kept per track (>= 1 when trace is set) */
   int stagger;        /* 1: an ablation build in which the two softmax warpgroups take turns
@@ -260,8 +263,9 @@ int fa_splitkv_num_splits(int batch, int heads_q, int heads_kv, int seqlen_q, in
  * writes dK = dV = 0; seqlen_k == 0 writes dQ = 0.  fa_options: grid,
  * timeout_s and debug_flags (bit 0: the row warps never signal P ready, so a
  * bounded wait expires and fa_device_status reports FA_ERR_DEVICE_TIMEOUT)
- * apply; pack > 1, exp_emu, workspace, trace and stagger do not
- * (FA_ERR_UNSUPPORTED when set).
+ * apply, and trace (head dims (128, 128): the event-log build of both
+ * kernels, see fa_options.trace); pack > 1, exp_emu, workspace and stagger
+ * do not (FA_ERR_UNSUPPORTED when set).
  */
 size_t fa_bwd_workspace_size(int batch, int heads_q, int seqlen_q);
 

@@ -235,3 +235,56 @@ def test_backward_paired_order_bitwise(fa, case):
         for a, b in zip(grads(0, grid), plain):
             assert torch.equal(a, b), (name, grid)
     check(w, (q, k, v, g), plain, name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_event_log_build(fa, causal):
+    """The event-log build of both backward kernels (fa_options.trace, head
+    dims 128): gradients bit-identical to the default build; with every CTA
+    recording, each stage's row warps log one S wait and one P arrival per
+    streamed block, as many as the MMA warp logs P waits, which is the task
+    count times the blocks each task streams (non-causal: B Hq mq nk in both
+    kernels)."""
+    from exact_attention_forward_08_gb300 import trace as tr
+    B, Hq, Hkv, S = 2, 4, 2, 640
+    w = synthetic.Workload("b_trace", B, Hq, Hkv, S, S, 128, 128, causal, seed=77)
+    q, k, v = w.generate()
+    g = synthetic.normal_bf16(w.shapes["o"], 78, 7)
+    qd, kd, vd, gd = (to_dev(a) for a in (q, k, v, g))
+    o, lse = fa.attention_forward(qd, kd, vd, causal=causal, scale=w.softmax_scale)
+    ref = fa.attention_backward(qd, kd, vd, o, lse, gd, causal=causal, scale=w.softmax_scale)
+    grid, cap = 3, 4096
+    words = tr.trace_words(grid, cap)
+    buf = torch.zeros(2 * words, dtype=torch.int64, device="cuda")
+    opts = fa.default_options()
+    opts.grid = grid
+    opts.trace, opts.trace_ctas, opts.trace_cap = buf.data_ptr(), grid, cap
+    got = fa.attention_backward(qd, kd, vd, o, lse, gd, causal=causal, scale=w.softmax_scale, options=opts)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status()[0] == fa.FA_OK
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    host = buf.cpu().numpy().view(np.uint64)
+    mq = nk = (S + 127) // 128
+    for kind in (0, 1):
+        ctas = tr.decode(host[kind * words:(kind + 1) * words], grid, cap)
+        for s in (0, 1):
+            p_row = sum(1 for c in ctas for _, ev, _ in c[f"softmax{s}"] if ev == "br_p")
+            s_row = sum(1 for c in ctas for _, ev, _ in c[f"softmax{s}"] if ev == "br_s")
+            p_mma = sum(1 for c in ctas for _, ev, arg in c["mma"] if ev == "bm_p" and arg >> 16 == s)
+            assert p_row == s_row == p_mma, (kind, s, p_row, s_row, p_mma)
+            if not causal:
+                assert p_row == B * Hq * mq * nk, (kind, s, p_row)
+        for c in ctas:
+            for name in ("softmax0", "softmax1", "mma", "tma"):
+                times = [t for t, _, _ in c[name]]
+                assert times == sorted(times), name
+        summ = tr.summarize_bwd(ctas)
+        assert summ["row.steady.work_S_to_P"]["n"] > 0 and summ["mma.issue_acc"]["n"] > 0
+    # head dims other than 128 are not built with the log
+    w64 = synthetic.Workload("b_trace64", 1, 2, 2, 128, 128, 64, 64, False, seed=3)
+    q6, k6, v6 = (to_dev(a) for a in w64.generate())
+    o6, l6 = fa.attention_forward(q6, k6, v6)
+    with pytest.raises(fa.FaError) as e:
+        fa.attention_backward(q6, k6, v6, o6, l6, o6, options=opts)
+    assert e.value.code == fa.FA_ERR_UNSUPPORTED

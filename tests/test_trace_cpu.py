@@ -85,3 +85,43 @@ def test_abi_rejects_bad_trace_options_before_cuda():
     assert fa.fa_fwd_ex(fake, fake, fake, fake, fake, 1, 2, 2, 128, 128, 128, 128, 0, 0.0, o, None) == \
         fa.FA_ERR_INVALID_ARG
     assert fa.fa_status_string(5) == "FA_ERR_DEVICE_CHECK"
+
+
+def test_backward_intervals():
+    """Two streamed blocks of one task on stage 0 of the backward log."""
+    row = [("br_task", 0, 0)]
+    mma = [("bm_task", 0, 5), ("bm_t", 0, 10), ("bm_sdp", 0, 400)]
+    tma = [("bl_task", 0, 0), ("bl_t", 0, 2), ("bl_t", 1, 3), ("bl_t", 2, 1000)]
+    for it, base in ((0, 100), (1, 3100)):
+        row += [("br_wait", it, base), ("br_s", it, base + 600), ("br_p", it, base + 1900)]
+        mma += [("bm_p", it, base + 2000), ("bm_acc", it, base + 2600)]
+        if it == 0:
+            mma += [("bm_t", 1, base + 2700), ("bm_sdp", 1, base + 3300)]
+    row += [("br_acc", 0, 7000), ("br_epi", 0, 8200)]
+    dec = tr.decode(buffer({"softmax0": row, "mma": mma, "tma": tma}), 1, 64)
+    s = tr.summarize_bwd(dec)
+    assert s["row.first.wait_for_S"]["median"] == 600 and s["row.steady.work_S_to_P"]["median"] == 1300
+    assert s["stage.block_period"]["median"] == 3000
+    assert s["handoff.row_P_to_mma_P"]["median"] == 100
+    assert s["mma.issue_acc"]["median"] == 600
+    assert sorted([s["mma.issue_S_dP"]["p10"], s["mma.issue_S_dP"]["p90"]]) == [390, 600]
+    assert s["row.epilogue"]["median"] == 1200
+    # S / dP issued at 400 and 3400, seen by the row warps at 700 and 3700
+    assert s["handoff.S_dP_issue_to_row_S"]["median"] == 300 and s["handoff.S_dP_issue_to_row_S"]["n"] == 2
+    # half-tiles: issued at 2, 3; the MMA found them ready at 10 and 2800
+    assert s["tma.half_tile_issue_to_mma_ready"]["n"] == 2
+
+
+def test_abi_rejects_bad_backward_trace_options_before_cuda():
+    import exact_attention_forward_08_gb300 as fa
+    from exact_attention_forward_08_gb300 import _build
+    _build.build()
+    fa.load_library()
+    fake = 0x10000
+    args = (fake,) * 9 + (1, 2, 2, 128, 128)
+    o = fa.default_options()
+    o.trace, o.trace_ctas, o.trace_cap = fake, 0, 10
+    assert fa.fa_bwd(*args, 128, 128, 0, 0.0, fake, 1 << 20, None, o) == fa.FA_ERR_INVALID_ARG
+    o.trace_ctas = 1
+    # the event-log build is made for head dims 128 only
+    assert fa.fa_bwd(*args, 64, 64, 0, 0.0, fake, 1 << 20, None, o) == fa.FA_ERR_UNSUPPORTED
