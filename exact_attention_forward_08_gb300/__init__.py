@@ -25,6 +25,7 @@ from . import _build
 __all__ = ["fa_fwd", "fa_fwd_ex", "fa_fwd_varlen", "fa_fwd_varlen_ex", "fa_varlen_workspace_size",
            "fa_varlen_plan_host", "fa_fwd_splitkv", "fa_splitkv_workspace_size", "fa_splitkv_num_splits",
            "attention_forward_splitkv", "fa_bwd", "fa_bwd_workspace_size", "attention_backward",
+           "fa_bwd_varlen", "fa_bwd_varlen_workspace_size", "attention_backward_varlen",
            "fa_fwd_varlen_noalloc", "fa_noalloc_scratch_bytes", "fa_device_status", "fa_device_status_code", "fa_status_string", "fa_selftest_exp2", "fa_make_plan",
            "fa_plan_task", "fa_plan_set_grid", "fa_plan_block_masked", "fa_plan_first_masked_block", "fa_version", "FaOptions", "FaPlan",
            "FaTask", "FaVarlenTask", "attention_forward", "attention_forward_varlen", "FaError", "load_library",
@@ -138,6 +139,13 @@ def load_library(path: str | None = None):
     bw = [_P] * 9 + [_I] * 8 + [ctypes.c_float, _P, ctypes.c_size_t]
     lib.fa_bwd.argtypes = bw + [_P]
     lib.fa_bwd.restype = _I
+    bvl = [_P] * 11 + [_I, ctypes.c_int64, ctypes.c_int64] + [_I] * 5 + [ctypes.c_float, _P, ctypes.c_size_t]
+    lib.fa_bwd_varlen.argtypes = bvl + [_P]
+    lib.fa_bwd_varlen.restype = _I
+    lib.fa_bwd_varlen_ex.argtypes = bvl + [ctypes.POINTER(FaOptions), _P]
+    lib.fa_bwd_varlen_ex.restype = _I
+    lib.fa_bwd_varlen_workspace_size.argtypes = [_I, _I, _I, ctypes.c_int64, ctypes.c_int64]
+    lib.fa_bwd_varlen_workspace_size.restype = ctypes.c_size_t
     lib.fa_bwd_ex.argtypes = bw + [ctypes.POINTER(FaOptions), _P]
     lib.fa_bwd_ex.restype = _I
     lib.fa_bwd_workspace_size.argtypes = [_I, _I, _I]
@@ -506,3 +514,59 @@ def flops(batch, heads_q, seqlen_q, seqlen_k, d_qk, d_v, causal) -> float:
 
 def default_scale(d_qk: int) -> float:
     return 1.0 / math.sqrt(d_qk)
+
+
+def fa_bwd_varlen_workspace_size(batch: int, heads_q: int, heads_kv: int, total_q: int, total_k: int) -> int:
+    return load_library().fa_bwd_varlen_workspace_size(batch, heads_q, heads_kv, total_q, total_k)
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, batch, total_q, total_k, heads_q, heads_kv, d_qk,
+                  d_v, causal, scale, workspace, workspace_bytes, stream, opts=None) -> int:
+    """``fa_bwd_varlen_ex`` of include/fa.h (``opts`` None: defaults); pointers as integers."""
+    return load_library().fa_bwd_varlen_ex(q, k, v, o, lse, dout, dq, dk, dv, cu_q, cu_k, batch, total_q, total_k,
+                                           heads_q, heads_kv, d_qk, d_v, int(causal), float(scale), workspace,
+                                           workspace_bytes, ctypes.byref(opts) if opts is not None else None,
+                                           stream)
+
+
+def attention_backward_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, causal: bool = False,
+                              scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None,
+                              options: FaOptions | None = None):
+    """(dQ, dK, dV) of a variable-length batch laid out as
+    ``attention_forward_varlen``'s: q [total_q,Hq,dqk], k [total_k,Hkv,dqk],
+    v [total_k,Hkv,dv], its outputs o [total_q,Hq,dv] and lse [Hq,total_q],
+    dout like o; cu_seqlens int32 CUDA tensors [B+1].  Allocates the gradients
+    and the workspace when not given."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 3-D bf16 CUDA tensor")
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise FaError(FA_ERR_INVALID_ARG, "lse must be a contiguous fp32 CUDA tensor")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.dim() != 1:
+            raise FaError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 1-D int32 CUDA tensor")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 1:
+        raise FaError(FA_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must both hold batch + 1 offsets")
+    batch = cu_seqlens_q.numel() - 1
+    total_q, Hq, dqk = q.shape
+    total_k, Hkv, _ = k.shape
+    dvh = v.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_varlen_workspace_size(batch, Hq, Hkv, total_q, total_k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sptr = stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+    s = 0.0 if scale is None else float(scale)
+    rc = fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                       batch, total_q, total_k, Hq, Hkv, dqk, dvh, causal, s, workspace.data_ptr(),
+                       workspace.numel() * workspace.element_size(), sptr, options)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_varlen")
+    return dq, dk, dv

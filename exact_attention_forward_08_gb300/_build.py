@@ -20,7 +20,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libfa_gb300.so")
 
 SOURCES = ["fa_api.cu", "fa_inst_d64.cu", "fa_inst_d128.cu", "fa_inst_d192.cu", "fa_bwd.cu", "fa_dbg_trace.cu",
-           "fa_dbg_check_a.cu", "fa_dbg_check_b.cu", "fa_var_stagger.cu", "fa_bwd_trace.cu"]
+           "fa_dbg_check_a.cu", "fa_dbg_check_b.cu", "fa_var_stagger.cu", "fa_bwd_trace.cu",
+           "fa_bwd_varlen.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -60,6 +60,7 @@ struct DeviceState {
   bool debug_ready[5 * 2 * 2 * 3] = {};  // (d_qk, d_v) pair x causal x (fixed, direct) x (trace, check, stagger)
   bool bwd_ready[3 * 2 * 2] = {};   // ((64,64), (128,128), (192,128)) x (dK/dV, dQ) x (non-causal, causal)
   bool bwd_trace_ready[2 * 2] = {};  // the event-log build, (128,128): (dK/dV, dQ) x (non-causal, causal)
+  bool bwd_varlen_ready[3 * 2 * 2] = {};  // the variable-length build, as bwd_ready
   bool plan_ready = false;
 };
 
@@ -1009,6 +1010,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
     p.out1 = static_cast<uint16_t*>(kv ? dk : nullptr);
     p.status = st->status;
     p.B = batch, p.Hq = heads_q, p.Hkv = heads_kv, p.Sq = seqlen_q, p.Sk = seqlen_k, p.sq_pad = sq_pad;
+    p.vec_hstride = sq_pad;
     p.ratio = ratio, p.causal = causal;
     p.mq = (seqlen_q + fa::kBM - 1) / fa::kBM;
     p.nk = (seqlen_k + fa::kBN - 1) / fa::kBN;
@@ -1051,6 +1053,179 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            int causal, float scale, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   return fa_bwd_ex(q, k, v, o, lse, dout, dq, dk, dv, batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal,
                    scale, workspace, workspace_bytes, nullptr, stream);
+}
+
+// ---------------------------------------------------------------------------
+// backward of a variable-length batch
+// ---------------------------------------------------------------------------
+namespace {
+
+// Workspace of fa_bwd_varlen: a 256-byte header (the two task counts), the
+// dK/dV and dQ task records at their upper bounds, then the l2 and dvec
+// vectors [Hq, pad_stride] (each sequence's rows padded to 128).
+struct BwdVarlenLayout {
+  int64_t kv_cap = 0, q_cap = 0, pad_stride = 0;
+  size_t off_kv = 0, off_q = 0, off_l2 = 0, off_dvec = 0, bytes = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+bool bwd_varlen_layout(int batch, int heads_q, int heads_kv, int64_t total_q, int64_t total_k, BwdVarlenLayout* L) {
+  if (batch < 0 || heads_q < 1 || heads_kv < 1 || total_q < 0 || total_k < 0) return false;
+  const int64_t big = int64_t(1) << 31;
+  if (total_q >= big || total_k >= big) return false;
+  const int64_t qb = (total_q + fa::kBM - 1) / fa::kBM + batch, kb = (total_k + fa::kBN - 1) / fa::kBN + batch;
+  L->kv_cap = heads_kv * kb;
+  L->q_cap = heads_q * qb;
+  L->pad_stride = fa::kBM * qb;
+  if (L->kv_cap >= big || L->q_cap >= big || L->pad_stride * heads_q >= big) return false;
+  const size_t rec = sizeof(fa::VarlenTask);
+  L->off_kv = 256;
+  L->off_q = L->off_kv + static_cast<size_t>(L->kv_cap) * rec;
+  L->off_l2 = align256(L->off_q + static_cast<size_t>(L->q_cap) * rec);
+  const size_t vec = static_cast<size_t>(heads_q) * L->pad_stride * sizeof(float);
+  L->off_dvec = align256(L->off_l2 + vec);
+  L->bytes = L->off_dvec + vec;
+  return true;
+}
+
+}  // namespace
+
+size_t fa_bwd_varlen_workspace_size(int batch, int heads_q, int heads_kv, int64_t total_q, int64_t total_k) {
+  BwdVarlenLayout L;
+  return bwd_varlen_layout(batch, heads_q, heads_kv, total_q, total_k, &L) ? L.bytes : 0;
+}
+
+int fa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                     int64_t total_q, int64_t total_k, int heads_q, int heads_kv, int d_qk, int d_v, int causal,
+                     float scale, void* workspace, size_t workspace_bytes, const fa_options* opts,
+                     fa_stream_t stream_) {
+  fa_options opt;
+  fa_options_default(&opt);
+  if (opts) opt = *opts;
+  if (opt.timeout_s <= 0.0) opt.timeout_s = 1.0;
+  causal = causal ? 1 : 0;
+  if (batch < 0 || batch > fa::kVarlenPlanMaxBatch || heads_q < 1 || heads_kv < 1 || heads_q % heads_kv)
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+  if (opt.grid < 0 || !std::isfinite(opt.timeout_s) || opt.timeout_s > 3600.0) return FA_ERR_INVALID_ARG;
+  if ((opt.debug_flags & ~fa::kDebugSkipPArrive) != 0) return FA_ERR_INVALID_ARG;
+  if (opt.exp_emu != 0 || opt.workspace != nullptr || opt.pack > 1 || opt.stagger || opt.trace != nullptr)
+    return FA_ERR_UNSUPPORTED;
+  const int pair = (d_qk == 64 && d_v == 64) ? 0 : ((d_qk == 128 && d_v == 128) ? 1 : ((d_qk == 192 && d_v == 128) ? 2 : -1));
+  if (pair < 0) return FA_ERR_UNSUPPORTED;
+  BwdVarlenLayout L;
+  if (!bwd_varlen_layout(batch, heads_q, heads_kv, total_q, total_k, &L)) return FA_ERR_INVALID_ARG;
+  if (batch == 0) return FA_OK;
+  const bool any_q = total_q > 0, any_k = total_k > 0;
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return FA_ERR_INVALID_ARG;
+  if ((any_q && (q == nullptr || o == nullptr || lse == nullptr || dout == nullptr || dq == nullptr)) ||
+      (any_k && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)))
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 || (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) != 0)
+    return FA_ERR_INVALID_ARG;
+  if (any_q && any_k && (workspace == nullptr || workspace_bytes < L.bytes)) return FA_ERR_INVALID_ARG;
+  if (scale == 0.f) scale = 1.0f / std::sqrt(static_cast<float>(d_qk));
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceState* st = nullptr;
+  int rc = init_device(dev, &st);
+  if (rc != FA_OK) return rc;
+  auto dev_ok = [&](const void* ptr) { return ptr == nullptr || is_device_ptr(ptr, dev); };
+  if (!dev_ok(q) || !dev_ok(k) || !dev_ok(v) || !dev_ok(o) || !dev_ok(lse) || !dev_ok(dout) || !dev_ok(dq) ||
+      !dev_ok(dk) || !dev_ok(dv) || !dev_ok(workspace) || !dev_ok(cu_seqlens_q) || !dev_ok(cu_seqlens_k))
+    return FA_ERR_INVALID_ARG;
+
+  // no query anywhere: dK = dV = 0; no key anywhere: dQ = 0 (whole tensors)
+  if (!any_q || !any_k) {
+    if (any_k) {
+      const size_t rows = static_cast<size_t>(total_k) * heads_kv;
+      if (cudaMemsetAsync(dk, 0, rows * d_qk * 2, stream) != cudaSuccess ||
+          cudaMemsetAsync(dv, 0, rows * d_v * 2, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    }
+    if (any_q && cudaMemsetAsync(dq, 0, static_cast<size_t>(total_q) * heads_q * d_qk * 2, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
+
+  fa::BwdEntry ent[2];
+  for (int kind = 0; kind < 2; ++kind) {
+    if (!fa::bwd_varlen_entry(d_qk, d_v, kind, causal, &ent[kind])) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    bool& ready = st->bwd_varlen_ready[(pair * 2 + kind) * 2 + causal];
+    if (!ready) {
+      if (ent[kind].smem > st->smem_optin) return FA_ERR_UNSUPPORTED;
+      if (cudaFuncSetAttribute(ent[kind].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ent[kind].smem) !=
+          cudaSuccess)
+        return FA_ERR_CUDA;
+      ready = true;
+    }
+  }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* counts = reinterpret_cast<int*>(ws);
+  fa::VarlenTask* kv_tasks = reinterpret_cast<fa::VarlenTask*>(ws + L.off_kv);
+  fa::VarlenTask* q_tasks = reinterpret_cast<fa::VarlenTask*>(ws + L.off_q);
+  float* l2 = reinterpret_cast<float*>(ws + L.off_l2);
+  float* dvec = reinterpret_cast<float*>(ws + L.off_dvec);
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);  // the planner's first call sets its shared-memory attribute
+    if (fa::launch_bwd_varlen_plan(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, heads_q, heads_kv, kv_tasks,
+                                   q_tasks, counts, st->status, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  const int pad_stride = static_cast<int>(L.pad_stride);
+  if (fa::launch_bwd_prep_varlen(d_v, o, dout, lse, l2, dvec, q_tasks, counts + 1, heads_q, total_q, pad_stride,
+                                 st->sms * 16, stream) != cudaSuccess)
+    return FA_ERR_CUDA;
+
+  const int tq = static_cast<int>(total_q), tk = static_cast<int>(total_k);
+  for (int kind = 0; kind < 2; ++kind) {
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const bool kv = kind == fa::kBwdDkDv;
+    const void* r0 = kv ? k : q;
+    const void* r1 = kv ? v : dout;
+    const void* t0 = kv ? q : k;
+    const void* t1 = kv ? dout : v;
+    const int hr = kv ? heads_kv : heads_q, sr = kv ? tk : tq;
+    const int ht = kv ? heads_q : heads_kv, stt = kv ? tq : tk;
+    if (encode_kv(&p.tm_r0, r0, 1, sr, hr, d_qk) != FA_OK || encode_kv(&p.tm_r1, r1, 1, sr, hr, d_v) != FA_OK ||
+        encode_kv(&p.tm_t0, t0, 1, stt, ht, d_qk, 64) != FA_OK || encode_kv(&p.tm_t1, t1, 1, stt, ht, d_v, 64) != FA_OK)
+      return FA_ERR_CUDA;
+    p.l2 = l2;
+    p.dvec = dvec;
+    p.out0 = static_cast<uint16_t*>(kv ? dv : dq);
+    p.out1 = static_cast<uint16_t*>(kv ? dk : nullptr);
+    p.status = st->status;
+    p.B = 1, p.Hq = heads_q, p.Hkv = heads_kv;
+    p.ratio = heads_q / heads_kv, p.causal = causal;
+    p.section_units = 1;
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    p.timeout_ns = static_cast<unsigned long long>(opt.timeout_s * 1e9);
+    p.debug_flags = opt.debug_flags;
+    p.vec_hstride = pad_stride;
+    p.vtasks = kv ? kv_tasks : q_tasks;
+    p.vcount = counts + kind;
+    const int grid = opt.grid > 0 ? opt.grid : st->sms;
+    if (ent[kind].launch(p, grid, stream) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  int64_t total_q, int64_t total_k, int heads_q, int heads_kv, int d_qk, int d_v, int causal,
+                  float scale, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa_bwd_varlen_ex(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                          heads_q, heads_kv, d_qk, d_v, causal, scale, workspace, workspace_bytes, nullptr, stream);
 }
 
 int fa_device_status(fa_stream_t stream, int* out) { return fa_device_status_detail(stream, out, nullptr); }

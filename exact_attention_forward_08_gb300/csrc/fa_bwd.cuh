@@ -68,8 +68,9 @@ constexpr int kBwdThreads = 320;
 struct BwdParams {
   CUtensorMap tm_r0, tm_r1;  // resident tiles: (K, V) for dK/dV, (Q, dO) for dQ; 4-D (d, H, S, B)
   CUtensorMap tm_t0, tm_t1;  // streamed tiles: (Q, dO) for dK/dV, (K, V) for dQ
-  const float* l2;           // [B, Hq, sq_pad]: LSE * log2(e), +inf on padded / empty rows
-  const float* dvec;         // [B, Hq, sq_pad]: D = rowsum(dO * O), 0 on padded rows
+  const float* l2;           // [B, Hq, sq_pad]: LSE * log2(e), +inf on padded / empty rows (varlen:
+                             // [Hq, vec_hstride], each sequence's padded rows at its offset)
+  const float* dvec;         // the same layout: D = rowsum(dO * O), 0 on padded rows
   uint16_t* out0;            // dV (dK/dV) or dQ, bf16 bits
   uint16_t* out1;            // dK (dK/dV)
   unsigned int* status;
@@ -88,7 +89,15 @@ struct BwdParams {
   uint64_t* trace;           // VAR & kVarTrace: [trace_ctas][kTraceTracks][1 + trace_cap] words
   int trace_ctas;            // CTAs 0 .. trace_ctas-1 record
   int trace_cap;             // records kept per track
+  int vec_hstride;           // l2 / dvec elements between query heads (fixed-length: sq_pad)
+  // variable-length batches (VAR & kBwdVarlen): this kernel's task records,
+  // written on the device by the planning kernel, and their count
+  const VarlenTask* vtasks;
+  const int* vcount;
 };
+
+// VAR bit of the variable-length build (the event log is bit kVarTrace)
+constexpr int kBwdVarlen = 8;
 
 // Streamed tiles travel as half-tiles: rows 64s .. 64s+63 of a 128-row block
 // are what stage s reads, so each ring slot holds one stage's half of both
@@ -177,13 +186,40 @@ enum : unsigned int {
 
 // One task of either direction.
 struct BwdTask {
-  int b, h;      // batch; K/V head (dK/dV) or query head (dQ)
+  int b, h;      // batch (sequence); K/V head (dK/dV) or query head (dQ)
   int blk;       // 128-row block of the resident tiles
   int it0;       // dK/dV: first query block; dQ: 0
   int nit;       // streamed blocks (dK/dV: ratio query heads x (mq - it0) blocks)
+  // variable-length batches only (the fixed-length kernels read the
+  // problem's values from the parameters instead: BwdSeq)
+  int sq, sk;    // the sequence's query and key counts
+  int res_r0, str_r0;  // first row of the sequence in the resident / streamed TMA views
+  int qbase, kbase;    // row of the sequence's first query / key in q, dq / k, dk, dv
+  int vbase;           // l2 / dvec index of the sequence's row 0 of query head 0
 };
 
-// Task t.  Units are (b, head) pairs; tasks of a unit cover its 128-row
+// The sequence a task belongs to: the task record's values (VARLEN) or the
+// fixed-length problem's.
+template <bool VARLEN>
+struct BwdSeq {
+  const BwdParams& p;
+  const BwdTask& k;
+  __device__ __forceinline__ int sq() const { return VARLEN ? k.sq : p.Sq; }
+  __device__ __forceinline__ int sk() const { return VARLEN ? k.sk : p.Sk; }
+  __device__ __forceinline__ int mq() const { return VARLEN ? (k.sq + kBM - 1) / kBM : p.mq; }
+  __device__ __forceinline__ int nk() const { return VARLEN ? (k.sk + kBN - 1) / kBN : p.nk; }
+  __device__ __forceinline__ int bc() const { return VARLEN ? 0 : k.b; }                  // TMA batch coordinate
+  __device__ __forceinline__ int res_r0() const { return VARLEN ? k.res_r0 : 0; }      // TMA row offsets
+  __device__ __forceinline__ int str_r0() const { return VARLEN ? k.str_r0 : 0; }
+  __device__ __forceinline__ int64_t qbase() const { return VARLEN ? k.qbase : static_cast<int64_t>(k.b) * p.Sq; }
+  __device__ __forceinline__ int64_t kbase() const { return VARLEN ? k.kbase : static_cast<int64_t>(k.b) * p.Sk; }
+  __device__ __forceinline__ int64_t vbase() const {
+    return VARLEN ? k.vbase : static_cast<int64_t>(k.b) * p.Hq * p.vec_hstride;
+  }
+};
+
+// Fixed-length task t: its batch, head and block, and the problem-wide
+// fields.  Units are (b, head) pairs; tasks of a unit cover its 128-row
 // blocks.  Non-causal: unit by unit.  Causal: sections of `section_units`
 // units whose streamed tiles fit in L2 together, heaviest block first inside
 // a section (for dK/dV the first key blocks, which every later query sees;
@@ -192,8 +228,7 @@ struct BwdTask {
 // the task of heaviness rank q and its complement blocks - 1 - q, whose
 // streamed blocks sum to a constant, run on one CTA in consecutive waves.
 template <int KIND>
-__device__ __forceinline__ BwdTask bwd_task(const BwdParams& p, int t) {
-  BwdTask k;
+__device__ __forceinline__ void bwd_task_fixed(const BwdParams& p, int t, BwdTask& k) {
   const int M = p.blocks;
   int unit, q;
   if (!p.causal) {
@@ -236,29 +271,59 @@ __device__ __forceinline__ BwdTask bwd_task(const BwdParams& p, int t) {
   const int H = KIND == kBwdDkDv ? p.Hkv : p.Hq;
   k.b = unit / H;
   k.h = unit - k.b * H;
+  // key block, heaviest (lowest) first; or query block, heaviest (highest) first under the mask
+  k.blk = KIND == kBwdDkDv ? q : (p.causal ? M - 1 - q : q);
+}
+
+// Task t, and the streamed blocks it visits.  Variable-length batches: the
+// planning kernel's record t (sequences longest first).  Fixed length: see
+// bwd_task_fixed.
+template <int KIND, bool VARLEN>
+__device__ __forceinline__ BwdTask bwd_task(const BwdParams& p, int t) {
+  BwdTask k;
+  if constexpr (VARLEN) {
+    // record: sequence, head, block, padded row offset; q_row0, sq, k_row0, sk
+    const int4* r = reinterpret_cast<const int4*>(p.vtasks + t);
+    const int4 a = r[0], c = r[1];
+    k.b = a.x, k.h = a.y, k.blk = a.z;
+    k.vbase = a.w;
+    k.qbase = c.x, k.sq = c.y, k.kbase = c.z, k.sk = c.w;
+    k.res_r0 = KIND == kBwdDkDv ? c.z : c.x;
+    k.str_r0 = KIND == kBwdDkDv ? c.x : c.z;
+  } else {
+    bwd_task_fixed<KIND>(p, t, k);
+  }
+  const BwdSeq<VARLEN> sq{p, k};
   if (KIND == kBwdDkDv) {
-    k.blk = q;  // key block, heaviest (lowest) first
     int first_q = 0;
     if (p.causal) {  // the first query that sees key blk * 128: q >= k - (Sk - Sq)
-      const int qmin = k.blk * kBN - (p.Sk - p.Sq);
+      const int qmin = k.blk * kBN - (sq.sk() - sq.sq());
       first_q = qmin > 0 ? qmin / kBM : 0;
     }
     k.it0 = first_q;
-    k.nit = first_q < p.mq ? p.ratio * (p.mq - first_q) : 0;
+    k.nit = first_q < sq.mq() ? p.ratio * (sq.mq() - first_q) : 0;
   } else {
-    k.blk = p.causal ? M - 1 - q : q;  // query block, heaviest (highest) first under the mask
     k.it0 = 0;
-    int n = p.nk;
+    int n = sq.nk();
     if (p.causal) {
       int last = (k.blk + 1) * kBM;
-      if (last > p.Sq) last = p.Sq;
-      const int64_t max_key = static_cast<int64_t>(last - 1) + p.Sk - p.Sq;
+      if (last > sq.sq()) last = sq.sq();
+      const int64_t max_key = static_cast<int64_t>(last - 1) + sq.sk() - sq.sq();
       n = max_key < 0 ? 0 : static_cast<int>(max_key / kBN + 1);
-      if (n > p.nk) n = p.nk;
+      if (n > sq.nk()) n = sq.nk();
     }
-    k.nit = k.blk * kBM < p.Sq ? n : 0;
+    k.nit = k.blk * kBM < sq.sq() ? n : 0;
   }
   return k;
+}
+
+
+// Tasks of this kernel: the fixed-length grid of units x blocks, or the
+// planning kernel's count.
+template <bool VARLEN>
+__device__ __forceinline__ int bwd_task_count(const BwdParams& p) {
+  if constexpr (VARLEN) return *p.vcount;
+  else return p.units * p.blocks;
 }
 
 // Streamed block `it` of a task: for dK/dV the query head and query block,
@@ -268,11 +333,11 @@ struct BwdIter {
   int blk;   // their 128-row block
 };
 
-template <int KIND>
+template <int KIND, bool VARLEN>
 __device__ __forceinline__ BwdIter bwd_iter(const BwdParams& p, const BwdTask& k, int it) {
   BwdIter r;
   if (KIND == kBwdDkDv) {
-    const int nq = p.mq - k.it0;
+    const int nq = BwdSeq<VARLEN>{p, k}.mq() - k.it0;
     const int hh = it / nq;
     r.head = k.h * p.ratio + hh;
     r.blk = k.it0 + (it - hh * nq);
@@ -336,6 +401,7 @@ __device__ __forceinline__ void issue_pv64(uint32_t d_tmem, uint32_t a_tmem, uin
 template <int DQ, int DV, int KIND, bool CAUSAL, int VAR>
 __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage, const uint32_t tmem,
                                              const uint32_t sbase, const uint8_t* smem, const WaitCtx& wc) {
+  constexpr bool VARLEN = (VAR & kBwdVarlen) != 0;
   using L = BwdLayout<DQ, DV>;
   using C = BwdCols<DQ, DV, KIND>;
   const int t = threadIdx.x - 128 * stage;
@@ -348,13 +414,14 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
   const int cb = 64 * stage;  // first column of this stage inside the streamed block
   uint32_t s_phase = 0, acc_phase = 0;
   int slot_it = 0;
-  const int num_tasks = p.units * p.blocks;
+  const int num_tasks = bwd_task_count<VARLEN>(p);
 
   uint32_t res_phase = 0;
   Tracer<(VAR & kVarTrace) != 0, -1> tr;  // track = stage
   tr.init(p, t == 0, stage);
   for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
-    const BwdTask tk = bwd_task<KIND>(p, task);
+    const BwdTask tk = bwd_task<KIND, VARLEN>(p, task);
+    const BwdSeq<VARLEN> sq{p, tk};
     const int row = tk.blk * kBM + t;  // key (dK/dV) or query (dQ)
     tr.ev(p, kEvBrTask, static_cast<uint32_t>(task));
     if constexpr (C::kTmemA) {
@@ -382,12 +449,12 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
     }
     float l2_row = 0.f, d_row = 0.f;
     if (KIND == kBwdDq) {  // row < sq_pad: the block lies inside the padded rows
-      const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + tk.h) * p.sq_pad + row;
+      const int64_t vi = sq.vbase() + static_cast<int64_t>(tk.h) * p.vec_hstride + row;
       l2_row = p.l2[vi];
       d_row = p.dvec[vi];
     }
     for (int it = 0; it < tk.nit; ++it, ++slot_it) {
-      const BwdIter bi = bwd_iter<KIND>(p, tk, it);
+      const BwdIter bi = bwd_iter<KIND, VARLEN>(p, tk, it);
       const int slot = (2 * slot_it + stage) % L::NSLOT;  // this stage's half of block it
       tr.ev(p, kEvBrWait, static_cast<uint32_t>(it));
       if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (L::bSFull + stage), s_phase, wc, kSiteBwdRowS))) {
@@ -402,11 +469,11 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
       int cmin = 0, cmax = 63;
       bool row_ok = true;
       if (KIND == kBwdDkDv) {
-        row_ok = row < p.Sk;
-        if (CAUSAL) cmin = row - (p.Sk - p.Sq) - bi.blk * kBM - cb;  // query q sees key k iff q >= k - (Sk - Sq)
+        row_ok = row < sq.sk();
+        if (CAUSAL) cmin = row - (sq.sk() - sq.sq()) - bi.blk * kBM - cb;  // query q sees key k iff q >= k - (Sk - Sq)
       } else {
-        cmax = min(63, p.Sk - 1 - bi.blk * kBN - cb);  // keys < Sk
-        if (CAUSAL) cmax = min(cmax, row + (p.Sk - p.Sq) - bi.blk * kBN - cb);
+        cmax = min(63, sq.sk() - 1 - bi.blk * kBN - cb);  // keys < Sk
+        if (CAUSAL) cmax = min(cmax, row + (sq.sk() - sq.sq()) - bi.blk * kBN - cb);
       }
       const float* l2v = reinterpret_cast<const float*>(smem + L::vec_off(slot));
       const float* dvv = l2v + 64;
@@ -488,19 +555,19 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
       tc_fence_after();
     }
     tr.ev(p, kEvBrAcc, static_cast<uint32_t>(task));
-    const bool store = KIND == kBwdDkDv ? row < p.Sk : row < p.Sq;
+    const bool store = KIND == kBwdDkDv ? row < sq.sk() : row < sq.sq();
     uint16_t* dst;
     float mult;
     uint32_t tA;
     int c_lo, c_hi;
     if (KIND == kBwdDkDv) {
-      const int64_t rr = (static_cast<int64_t>(tk.b) * p.Sk + row) * p.Hkv + tk.h;
+      const int64_t rr = (sq.kbase() + row) * p.Hkv + tk.h;
       dst = stage == 0 ? p.out0 + rr * DV : p.out1 + rr * DQ;  // dV, dK
       mult = stage == 0 ? 1.f : p.scale;
       tA = tmem + lane_off + (stage == 0 ? C::kAcc0 : C::kAcc1);
       c_lo = 0, c_hi = stage == 0 ? DV : DQ;
     } else {
-      dst = p.out0 + ((static_cast<int64_t>(tk.b) * p.Sq + row) * p.Hq + tk.h) * DQ;
+      dst = p.out0 + ((sq.qbase() + row) * p.Hq + tk.h) * DQ;
       mult = p.scale;
       tA = tmem + lane_off + C::kAcc0;
       c_lo = stage * (DQ / 2), c_hi = c_lo + DQ / 2;
@@ -543,6 +610,7 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
 template <int DQ, int DV, int KIND, int VAR>
 __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t tmem, const uint32_t sbase,
                                              const WaitCtx& wc) {
+  constexpr bool VARLEN = (VAR & kBwdVarlen) != 0;
   using L = BwdLayout<DQ, DV>;
   using C = BwdCols<DQ, DV, KIND>;
   const uint32_t bar0 = sbase + L::oBar;
@@ -553,7 +621,7 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
   };
   uint32_t res_phase = 0, free_phase = 0, a_phase = 0, p_phase[2] = {0u, 0u}, sr_phase[2] = {0u, 0u};
   int slot_it = 0;  // streamed blocks consumed; block i's stage-s half sits in slot (2 i + s) % NSLOT
-  const int num_tasks = p.units * p.blocks;
+  const int num_tasks = bwd_task_count<VARLEN>(p);
   const uint32_t r0 = sbase + L::oR0, r1 = sbase + L::oR1;
   auto half_slot = [&](int blk_it, int s) { return (2 * blk_it + s) % L::NSLOT; };
   auto half_parity = [&](int blk_it, int s) { return static_cast<uint32_t>((2 * blk_it + s) / L::NSLOT) & 1u; };
@@ -583,7 +651,7 @@ __device__ __forceinline__ void bwd_mma_role(const BwdParams& p, const uint32_t 
   Tracer<(VAR & kVarTrace) != 0, 3> tr;
   tr.init(p, leader != 0);
   for (int task = blockIdx.x, n = 0; task < num_tasks; task += gridDim.x, ++n) {
-    const BwdTask tk = bwd_task<KIND>(p, task);
+    const BwdTask tk = bwd_task<KIND, VARLEN>(p, task);
     if (!wait(bar(L::bResFull), res_phase, kSiteBwdMmaRes)) goto out;
     res_phase ^= 1u;
     tr.ev(p, kEvBmTask, static_cast<uint32_t>(task));
@@ -660,12 +728,13 @@ out:
 // ---------------------------------------------------------------------------
 template <int DQ, int DV, int KIND, int VAR>
 __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t sbase, const WaitCtx& wc) {
+  constexpr bool VARLEN = (VAR & kBwdVarlen) != 0;
   using L = BwdLayout<DQ, DV>;
   const uint32_t bar0 = sbase + L::oBar;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t res_uses = 0;
   int half_it = 0;  // streamed half-tiles issued
-  const int num_tasks = p.units * p.blocks;
+  const int num_tasks = bwd_task_count<VARLEN>(p);
   tma_prefetch_desc(&p.tm_r0);
   tma_prefetch_desc(&p.tm_r1);
   tma_prefetch_desc(&p.tm_t0);
@@ -674,17 +743,20 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
   Tracer<(VAR & kVarTrace) != 0, 4> tr;
   tr.init(p, true);
   for (int task = blockIdx.x; task < num_tasks; task += gridDim.x) {
-    const BwdTask tk = bwd_task<KIND>(p, task);
+    const BwdTask tk = bwd_task<KIND, VARLEN>(p, task);
+    const BwdSeq<VARLEN> sq{p, tk};
     tr.ev(p, kEvBlTask, static_cast<uint32_t>(task));
     if (res_uses > 0 && !mbar_wait(bar(L::bResEmpty), (res_uses - 1u) & 1u, wc, kSiteBwdLoadRes)) goto out;
     mbar_arrive_expect_tx(bar(L::bResFull), static_cast<uint32_t>(L::kTile0 + L::kTile1));
     for (int c = 0; c < L::NCQ; ++c)
-      tma_load_4d(sbase + L::oR0 + c * kChunkBytes, &p.tm_r0, bar(L::bResFull), c * 64, tk.h, tk.blk * kBM, tk.b);
+      tma_load_4d(sbase + L::oR0 + c * kChunkBytes, &p.tm_r0, bar(L::bResFull), c * 64, tk.h,
+                  sq.res_r0() + tk.blk * kBM, sq.bc());
     for (int c = 0; c < L::NCV; ++c)
-      tma_load_4d(sbase + L::oR1 + c * kChunkBytes, &p.tm_r1, bar(L::bResFull), c * 64, tk.h, tk.blk * kBM, tk.b);
+      tma_load_4d(sbase + L::oR1 + c * kChunkBytes, &p.tm_r1, bar(L::bResFull), c * 64, tk.h,
+                  sq.res_r0() + tk.blk * kBM, sq.bc());
     ++res_uses;
     for (int it = 0; it < tk.nit; ++it) {
-      const BwdIter bi = bwd_iter<KIND>(p, tk, it);
+      const BwdIter bi = bwd_iter<KIND, VARLEN>(p, tk, it);
       for (int s = 0; s < 2; ++s, ++half_it) {  // stage s's half: rows 64s .. 64s+63 of the block
         const int slot = half_it % L::NSLOT;
         if (half_it >= L::NSLOT &&
@@ -696,10 +768,12 @@ __device__ __forceinline__ void bwd_load_role(const BwdParams& p, const uint32_t
         const int row = bi.blk * kBM + 64 * s;
         mbar_arrive_expect_tx(fb, static_cast<uint32_t>(L::kHalf0 + L::kHalf1) +
                                       (KIND == kBwdDkDv ? 2u * L::kVecH : 0u));
-        for (int c = 0; c < L::NCQ; ++c) tma_load_4d(t0 + c * L::kHalfChunk, &p.tm_t0, fb, c * 64, bi.head, row, tk.b);
-        for (int c = 0; c < L::NCV; ++c) tma_load_4d(t1 + c * L::kHalfChunk, &p.tm_t1, fb, c * 64, bi.head, row, tk.b);
+        for (int c = 0; c < L::NCQ; ++c)
+          tma_load_4d(t0 + c * L::kHalfChunk, &p.tm_t0, fb, c * 64, bi.head, sq.str_r0() + row, sq.bc());
+        for (int c = 0; c < L::NCV; ++c)
+          tma_load_4d(t1 + c * L::kHalfChunk, &p.tm_t1, fb, c * 64, bi.head, sq.str_r0() + row, sq.bc());
         if (KIND == kBwdDkDv) {  // LSE and D of these 64 queries (whole padded blocks: always in range)
-          const int64_t vi = (static_cast<int64_t>(tk.b) * p.Hq + bi.head) * p.sq_pad + row;
+          const int64_t vi = sq.vbase() + static_cast<int64_t>(bi.head) * p.vec_hstride + row;
           const uint32_t vdst = sbase + L::vec_off(slot);
           bulk_load(vdst, p.l2 + vi, L::kVecH, fb);
           bulk_load(vdst + L::kVecH, p.dvec + vi, L::kVecH, fb);
@@ -789,13 +863,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 // prep: D = rowsum(dO * O) and LSE * log2(e) per (b, query head, row), rows
 // padded to whole 128-row blocks; one warp per row
 // ---------------------------------------------------------------------------
+// D of one row (elements at `off` of o and dout, D_V of them), summed over
+// the warp: every lane returns the total
+template <int D>
+__device__ __forceinline__ float prep_row_dot(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                              int64_t off, bool valid) {
+  constexpr int kPer = D / 32;  // 2 or 4 bf16 per lane
+  const int lane = threadIdx.x & 31;
+  float acc = 0.f;
+  if (valid) {
+    off += lane * kPer;
+    uint32_t ow[kPer / 2], gw[kPer / 2];
+    if constexpr (kPer == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+      const uint2 g = *reinterpret_cast<const uint2*>(dout + off);
+      ow[0] = a.x, ow[1] = a.y, gw[0] = g.x, gw[1] = g.y;
+    } else {
+      ow[0] = *reinterpret_cast<const uint32_t*>(o + off);
+      gw[0] = *reinterpret_cast<const uint32_t*>(dout + off);
+    }
+#pragma unroll
+    for (int w = 0; w < kPer / 2; ++w) {
+      acc += __uint_as_float(ow[w] << 16) * __uint_as_float(gw[w] << 16);
+      acc += __uint_as_float(ow[w] & 0xffff0000u) * __uint_as_float(gw[w] & 0xffff0000u);
+    }
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  return acc;
+}
+
+// the row's base-2 LSE: +inf for padded rows and rows with no visible key (P = 0)
+__device__ __forceinline__ float prep_row_l2(const float* __restrict__ lse, int64_t i, bool valid) {
+  float v = INFINITY;
+  if (valid) {
+    const float l = lse[i];
+    if (l != -INFINITY) v = l * 1.4426950408889634f;
+  }
+  return v;
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __restrict__ o,
                                                           const uint16_t* __restrict__ dout,
                                                           const float* __restrict__ lse, float* __restrict__ l2,
                                                           float* __restrict__ dvec, int B, int Hq, int Sq,
                                                           int sq_pad) {
-  constexpr int kPer = D / 32;  // 2 or 4 bf16 per lane
   const int lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(B) * Hq * sq_pad;
   const int64_t step = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -804,37 +917,44 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
     const int i = static_cast<int>(r - bh * sq_pad);
     const int64_t b = bh / Hq;
     const int h = static_cast<int>(bh - b * Hq);
-    float acc = 0.f;
-    if (i < Sq) {
-      const int64_t off = ((b * Sq + i) * Hq + h) * D + lane * kPer;
-      uint32_t ow[kPer / 2], gw[kPer / 2];
-      if constexpr (kPer == 4) {
-        const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-        const uint2 g = *reinterpret_cast<const uint2*>(dout + off);
-        ow[0] = a.x, ow[1] = a.y, gw[0] = g.x, gw[1] = g.y;
-      } else {
-        ow[0] = *reinterpret_cast<const uint32_t*>(o + off);
-        gw[0] = *reinterpret_cast<const uint32_t*>(dout + off);
-      }
-#pragma unroll
-      for (int w = 0; w < kPer / 2; ++w) {
-        acc += __uint_as_float(ow[w] << 16) * __uint_as_float(gw[w] << 16);
-        acc += __uint_as_float(ow[w] & 0xffff0000u) * __uint_as_float(gw[w] & 0xffff0000u);
-      }
-    }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    const bool valid = i < Sq;
+    const float acc = prep_row_dot<D>(o, dout, ((b * Sq + i) * Hq + h) * D, valid);
     if (lane == 0) {
-      float v = INFINITY;  // padded rows, and rows with no visible key, get P = 0
-      if (i < Sq) {
-        const float l = lse[bh * Sq + i];
-        if (l != -INFINITY) v = l * 1.4426950408889634f;
-      }
-      l2[r] = v;
-      dvec[r] = i < Sq ? acc : 0.f;
+      l2[r] = prep_row_l2(lse, bh * Sq + i, valid);
+      dvec[r] = valid ? acc : 0.f;
     }
   }
 }
 
+// The same for a variable-length batch, one warp per row of each dQ task
+// record (sequence b, query head h, 128-row block; the sequence's padded row
+// offset, first row and length): rows at h * vec_hstride + offset + row, LSE
+// from [Hq, total_q].
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_varlen_kernel(const uint16_t* __restrict__ o,
+                                                                 const uint16_t* __restrict__ dout,
+                                                                 const float* __restrict__ lse,
+                                                                 float* __restrict__ l2, float* __restrict__ dvec,
+                                                                 const VarlenTask* __restrict__ tasks,
+                                                                 const int* __restrict__ count, int Hq,
+                                                                 int64_t total_q, int vec_hstride) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = static_cast<int64_t>(*count) * kBM;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += step) {
+    const int4* rec = reinterpret_cast<const int4*>(tasks + (r / kBM));
+    const int4 a = rec[0], c = rec[1];  // b, h, block, offset; q_row0, sq, k_row0, sk
+    const int h = a.y;
+    const int i = a.z * kBM + static_cast<int>(r % kBM);  // row inside the sequence
+    const bool valid = i < c.y;
+    const int64_t q = static_cast<int64_t>(c.x) + i;  // row in the packed tensors
+    const float acc = prep_row_dot<D>(o, dout, (q * Hq + h) * D, valid);
+    if (lane == 0) {
+      const int64_t idx = static_cast<int64_t>(h) * vec_hstride + a.w + i;
+      l2[idx] = prep_row_l2(lse, h * total_q + q, valid);
+      dvec[idx] = valid ? acc : 0.f;
+    }
+  }
+}
 
 }  // namespace fa

@@ -280,6 +280,44 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               const fa_options* opts, fa_stream_t stream);
 
 /*
+ * Backward of a variable-length batch: dQ, dK, dV of fa_fwd_varlen's output
+ * ("Infra: Flash Attention", section "Why backward recomputes", applied to
+ * each sequence as its own problem).  Layouts as fa_fwd_varlen's: q, dq
+ * [total_q, heads_q, d_qk]; k, dk [total_k, heads_kv, d_qk]; v, dv
+ * [total_k, heads_kv, d_v]; o, dout [total_q, heads_q, d_v] bf16; lse
+ * [heads_q, total_q] fp32 (the forward's); cu_seqlens_q / cu_seqlens_k int32
+ * [batch + 1] in device memory (sequence b: query rows cu_seqlens_q[b] ..
+ * cu_seqlens_q[b+1]-1, key rows likewise; causal is bottom-right inside each
+ * sequence).  Head dims (64, 64), (128, 128), (192, 128); batch <= 8192.
+ * Rows outside every sequence are neither read nor written, except that
+ * total_q == 0 zeroes the whole of dk and dv and total_k == 0 the whole of
+ * dq.  A sequence without queries gets dK = dV = 0, one without keys dQ = 0.
+ *
+ * workspace: device memory of fa_bwd_varlen_workspace_size(batch, heads_q,
+ * heads_kv, total_q, total_k) bytes, 16-byte aligned (the planned task lists
+ * and D, LSE * log2(e) per padded query row); calls that may overlap need
+ * different workspaces.  Stream-ordered launches: a planning kernel (one
+ * CTA: checks cu_seqlens, orders the sequences longest first and writes the
+ * task records), the row preparation, the dK/dV kernel and the dQ kernel;
+ * deterministic.  Bad cu_seqlens: nothing is computed and fa_device_status
+ * reports FA_ERR_INVALID_ARG with site 501 and the sequence index.
+ * fa_options: grid, timeout_s and debug_flags bit 0 apply; pack > 1,
+ * exp_emu, workspace, trace and stagger are FA_ERR_UNSUPPORTED.
+ */
+size_t fa_bwd_varlen_workspace_size(int batch, int heads_q, int heads_kv, int64_t total_q, int64_t total_k);
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                  int64_t total_q, int64_t total_k, int heads_q, int heads_kv, int d_qk, int d_v, int causal,
+                  float scale, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+int fa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                     int64_t total_q, int64_t total_k, int heads_q, int heads_kv, int d_qk, int d_v, int causal,
+                     float scale, void* workspace, size_t workspace_bytes, const fa_options* opts,
+                     fa_stream_t stream);
+
+/*
  * Test hook for the emulated exponential: for i < n, y_fma[i] = 2^x[i] by the
  * FMA-pipe polynomial used with exp_emu = 1, y_mufu[i] = the hardware ex2
  * (ex2.approx.ftz).  Device pointers, fp32; stream-ordered.

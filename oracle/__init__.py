@@ -151,6 +151,34 @@ def attn_bwd(q, k, v, dout, causal: bool = False, scale: float | None = None, th
     return dq, dk, dvv
 
 
+def attn_bwd_varlen(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, causal: bool = False, scale: float | None = None,
+                    threads: int | None = None, lib=None):
+    """Reference attention backward of a variable-length batch laid out as
+    ``attn_fwd_varlen``'s (dout like its O): ``attn_bwd`` on every sequence as
+    a batch of one.  Returns (dQ [total_q,Hq,dqk], dK [total_k,Hkv,dqk],
+    dV [total_k,Hkv,dv]) as float64; a sequence without queries has
+    dK = dV = 0, one without keys dQ = 0; rows outside every sequence are NaN."""
+    cu_q = [int(x) for x in cu_seqlens_q]
+    cu_k = [int(x) for x in cu_seqlens_k]
+    total_q, Hq, dqk = q.shape
+    total_k, Hkv, _ = k.shape
+    dvh = v.shape[2]
+    dq = np.full((total_q, Hq, dqk), np.nan)
+    dk = np.full((total_k, Hkv, dqk), np.nan)
+    dv = np.full((total_k, Hkv, dvh), np.nan)
+    for b in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        if q1 == q0 or k1 == k0:  # nothing flows: the gradients of whatever rows exist are 0
+            dq[q0:q1] = 0.0
+            dk[k0:k1] = 0.0
+            dv[k0:k1] = 0.0
+            continue
+        g = attn_bwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], dout[None, q0:q1], causal, scale,
+                     threads=threads, lib=lib)
+        dq[q0:q1], dk[k0:k1], dv[k0:k1] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv
+
+
 def row_ids(b, i, h, Sq: int, Hq: int) -> np.ndarray:
     """Linear row ids r = (b*Sq + i)*Hq + h."""
     return (np.asarray(b, dtype=np.int64) * Sq + np.asarray(i, dtype=np.int64)) * Hq + np.asarray(h, dtype=np.int64)

@@ -112,6 +112,85 @@ def test_oracle_varlen_rows_outside_sequences():
     assert np.allclose(o[2:4], 1.0) and np.allclose(lse[0, 2:4], np.log(2.0))
 
 
+def packed_bruteforce_bwd(q, k, v, dout, cu_q, cu_k, causal, scale):
+    """The backward of packed_bruteforce through the same explicit mask, from
+    the softmax's own derivative written over the packed rows (P from the
+    forward's LSE; D = rowsum(dO o O); dS = P (dP - D); dQ = scale dS K,
+    dK = scale dS^T Q, dV = P^T dO, with the K/V gradients of a GQA group
+    summed over its query heads).  Plain float64 numpy."""
+    total_q, Hq, _ = q.shape
+    total_k, Hkv, _ = k.shape
+    o, lse = packed_bruteforce(q, k, v, cu_q, cu_k, causal, scale)
+    seq_q = np.full(total_q, -1)
+    seq_k = np.full(total_k, -1)
+    for b in range(len(cu_q) - 1):
+        seq_q[cu_q[b]:cu_q[b + 1]] = b
+        seq_k[cu_k[b]:cu_k[b + 1]] = b
+    t = np.arange(total_q)[:, None]
+    u = np.arange(total_k)[None, :]
+    mask = (seq_q[:, None] == seq_k[None, :]) & (seq_q[:, None] >= 0)
+    if causal:
+        bq = np.maximum(seq_q, 0)
+        q0 = np.asarray(cu_q)[bq][:, None]
+        sq = (np.asarray(cu_q)[bq + 1] - np.asarray(cu_q)[bq])[:, None]
+        k0 = np.asarray(cu_k)[bq][:, None]
+        sk = (np.asarray(cu_k)[bq + 1] - np.asarray(cu_k)[bq])[:, None]
+        mask &= (u - k0) <= (t - q0) + sk - sq
+    ratio = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for h in range(Hq):
+        kh = k[:, h // ratio, :]
+        vh = v[:, h // ratio, :]
+        s = scale * (q[:, h, :] @ kh.T)
+        lrow = lse[h][:, None]
+        p = np.where(mask & np.isfinite(lrow), np.exp(s - np.where(np.isfinite(lrow), lrow, 0.0)), 0.0)
+        g = dout[:, h, :]
+        dp = g @ vh.T
+        dd = (g * o[:, h, :]).sum(axis=1, keepdims=True)
+        ds = p * (dp - dd)
+        dq[:, h, :] = scale * (ds @ kh)
+        dk[:, h // ratio, :] += scale * (ds.T @ q[:, h, :])
+        dv[:, h // ratio, :] += p.T @ g
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_oracle_varlen_backward_equals_packed_bruteforce(case):
+    seq_q, seq_k, Hq, Hkv, causal = case
+    cu_q = np.concatenate([[0], np.cumsum(seq_q)]).astype(int)
+    cu_k = np.concatenate([[0], np.cumsum(seq_k)]).astype(int)
+    rng = np.random.default_rng(sum(seq_q) * 31 + Hq)
+    d, dvh = 8, 6
+    q = rng.standard_normal((cu_q[-1], Hq, d))
+    k = rng.standard_normal((cu_k[-1], Hkv, d))
+    v = rng.standard_normal((cu_k[-1], Hkv, dvh))
+    g = rng.standard_normal((cu_q[-1], Hq, dvh))
+    scale = 0.4
+    got = oracle.attn_bwd_varlen(q, k, v, g, cu_q, cu_k, causal=causal, scale=scale, threads=2)
+    want = packed_bruteforce_bwd(q, k, v, g, cu_q, cu_k, causal, scale)
+    for a, b in zip(got, want):
+        assert np.allclose(a, b, rtol=1e-10, atol=1e-12)
+
+
+def test_oracle_varlen_backward_equal_lengths_is_the_batched_problem():
+    B, S, Hq, Hkv, d = 3, 11, 4, 2, 8
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((B, S, Hq, d))
+    k = rng.standard_normal((B, S + 2, Hkv, d))
+    v = rng.standard_normal((B, S + 2, Hkv, d))
+    g = rng.standard_normal((B, S, Hq, d))
+    for causal in (False, True):
+        ref = oracle.attn_bwd(q, k, v, g, causal=causal, threads=2)
+        cu_q = np.arange(B + 1) * S
+        cu_k = np.arange(B + 1) * (S + 2)
+        got = oracle.attn_bwd_varlen(q.reshape(B * S, Hq, d), k.reshape(-1, Hkv, d), v.reshape(-1, Hkv, d),
+                                     g.reshape(B * S, Hq, d), cu_q, cu_k, causal=causal, threads=2)
+        for a, b in zip(got, ref):
+            assert np.array_equal(a.reshape(b.shape), b)
+
+
 def test_varlen_workloads_recipe():
     for w in synthetic.varlen_workloads().values():
         assert w.total_q == 32768 and w.total_k == 32768
