@@ -622,6 +622,31 @@ def bwd_cpu_sample(w, q, k, v, g, seconds: float):
     return flops / dt / 1e12, text, dt, min(threads, w.batch * w.heads_kv)
 
 
+def bwd_cpu_sample_varlen(w, q, k, v, g, seconds: float):
+    """The backward oracle on whole sequences of the batch, shortest first,
+    until about `seconds` have passed.  Returns (TFLOP/s, sample text, s, cores)."""
+    import oracle
+    threads = oracle.default_threads()
+    order = sorted(range(w.batch), key=lambda b: w.seqlens_q[b] * w.seqlens_k[b])
+    cu_q, cu_k = w.cu_seqlens_q, w.cu_seqlens_k
+    done, flops, t0 = 0, 0.0, time.perf_counter()
+    for b in order:
+        q0, q1, k0, k1 = int(cu_q[b]), int(cu_q[b + 1]), int(cu_k[b]), int(cu_k[b + 1])
+        if q1 == q0 or k1 == k0:
+            continue
+        oracle.attn_bwd(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], g[None, q0:q1], causal=w.causal,
+                        scale=w.softmax_scale, threads=threads)
+        f = 2.5 * 2.0 * w.heads_q * (q1 - q0) * (k1 - k0) * (w.d_qk + w.d_v)
+        flops += f / 2 if w.causal else f
+        done += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    text = (f"{done} of {w.batch} sequences of {w.name}, shortest first (fp64 C oracle backward, {threads} threads, "
+            f"{dt:.1f} s)")
+    return flops / dt / 1e12, text, dt, threads
+
+
 def run_ours_bwd(args):
     import dataclasses
 
@@ -637,18 +662,25 @@ def run_ours_bwd(args):
     dist_init("nccl" if world > 1 else "gloo")
     fa.load_library()
     w0 = get_workload(args.config)
-    if is_varlen(w0):
-        raise SystemExit("--pass bwd takes fixed-length workloads")
+    if is_decode(args.config):
+        raise SystemExit("--pass bwd takes fixed-length or variable-length workloads")
+    varlen = is_varlen(w0)
     w = dataclasses.replace(w0, seed=rank_batch_seed(w0.seed, rank))
     qb, kb, vb = w.generate()
     gb = synthetic.normal_bf16(w.shapes["o"], w.seed, 7)
     to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
     qh, kh, vh, gh = (to_t(a).pin_memory() for a in (qb, kb, vb, gb))
     qd, kd, vd, gd = (t.to(dev) for t in (qh, kh, vh, gh))
-    o, lse = fa.attention_forward(qd, kd, vd, causal=w.causal, scale=w.softmax_scale)
+    if varlen:
+        cq = torch.tensor(w.cu_seqlens_q, dtype=torch.int32, device=dev)
+        ck = torch.tensor(w.cu_seqlens_k, dtype=torch.int32, device=dev)
+        o, lse = fa.attention_forward_varlen(qd, kd, vd, cq, ck, causal=w.causal, scale=w.softmax_scale)
+        ws_bytes = fa.fa_bwd_varlen_workspace_size(w.batch, w.heads_q, w.heads_kv, w.total_q, w.total_k)
+    else:
+        o, lse = fa.attention_forward(qd, kd, vd, causal=w.causal, scale=w.softmax_scale)
+        ws_bytes = fa.fa_bwd_workspace_size(w.batch, w.heads_q, w.seqlen_q)
     oh, lh = o.cpu().pin_memory(), lse.cpu().pin_memory()
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws_bytes = fa.fa_bwd_workspace_size(w.batch, w.heads_q, w.seqlen_q)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     sp = torch.cuda.current_stream(dev).cuda_stream
     scale = w.softmax_scale
@@ -660,10 +692,16 @@ def run_ours_bwd(args):
 
     def launch(ins, outs, stream):
         q_, k_, v_, o_, l_, g_ = ins
-        rc = fa.fa_bwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), l_.data_ptr(), g_.data_ptr(),
-                       outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), w.batch, w.heads_q, w.heads_kv,
-                       w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, stream,
-                       bopts)
+        if varlen:
+            rc = fa.fa_bwd_varlen(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), l_.data_ptr(),
+                                  g_.data_ptr(), outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
+                                  cq.data_ptr(), ck.data_ptr(), w.batch, w.total_q, w.total_k, w.heads_q, w.heads_kv,
+                                  w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes, stream)
+        else:
+            rc = fa.fa_bwd(q_.data_ptr(), k_.data_ptr(), v_.data_ptr(), o_.data_ptr(), l_.data_ptr(), g_.data_ptr(),
+                           outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), w.batch, w.heads_q, w.heads_kv,
+                           w.seqlen_q, w.seqlen_k, w.d_qk, w.d_v, int(w.causal), scale, ws.data_ptr(), ws_bytes,
+                           stream, bopts)
         if rc != 0:
             raise fa.FaError(rc, "fa_bwd")
 
@@ -712,10 +750,13 @@ def run_ours_bwd(args):
     d2h = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
     peak, peak_src = load_peak()
     achieved = flops / (ms_step * 1e-3) / 1e12
-    blocks_even = -(-w.seqlen_q // 128) % 2 == 0 and -(-w.seqlen_k // 128) % 2 == 0
-    cfg = config_of(w, world, flops, False, 1,
-                    "plain order (ablation)" if args.no_balance else
-                    ("heavy and light blocks paired on one CTA" if w.causal and blocks_even else "plain order"))
+    if varlen:
+        order = "sequences longest first (planning kernel), static round-robin"
+    else:
+        blocks_even = -(-w.seqlen_q // 128) % 2 == 0 and -(-w.seqlen_k // 128) % 2 == 0
+        order = ("plain order (ablation)" if args.no_balance else
+                 ("heavy and light blocks paired on one CTA" if w.causal and blocks_even else "plain order"))
+    cfg = config_of(w, world, flops, False, 1, order)
     cfg["pass"] = "backward (dQ, dK, dV; flops = 2.5x forward, 5 GEMMs; the kernels run 7)"
     result = {
         "metric": METRIC_BWD, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -723,7 +764,8 @@ def run_ours_bwd(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
-        "gpu_launches": args.steps * 3,  # row preparation, dK/dV kernel, dQ kernel
+        # row preparation, dK/dV kernel, dQ kernel (and the planning kernel for varlen)
+        "gpu_launches": args.steps * (4 if varlen else 3),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": f"{peak_src} (bf16 dense, burst)", "algorithmic_flops": flops,
@@ -732,7 +774,8 @@ def run_ours_bwd(args):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v_, text, dt, cores = bwd_cpu_sample(w, qb, kb, vb, gb, args.cpu_seconds)
+        v_, text, dt, cores = (bwd_cpu_sample_varlen if varlen else bwd_cpu_sample)(w, qb, kb, vb, gb,
+                                                                                  args.cpu_seconds)
         result["cpu_baseline"] = {"value": v_, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": text,
                                   "seconds": round(dt, 2)}
     elif rank == 0:
@@ -790,15 +833,15 @@ def run_reference(args):
 
 def run_reference_bwd(args, w, q, k, v):
     """The backward oracle, each step on the first rows of every (batch, head)
-    (bwd_cpu_sample), sized so the whole run stays near two minutes."""
+    (bwd_cpu_sample; whole sequences for a variable-length batch), sized so
+    the whole run stays near two minutes."""
     import synthetic
-    if is_varlen(w):
-        raise SystemExit("--pass bwd takes fixed-length workloads")
+    sample = bwd_cpu_sample_varlen if is_varlen(w) else bwd_cpu_sample
     g = synthetic.normal_bf16(w.shapes["o"], w.seed, 7)
     per_step = min(10.0, 120.0 / (args.steps + args.warmup))
     for _ in range(args.warmup):
-        bwd_cpu_sample(w, q, k, v, g, per_step)
-    runs = [bwd_cpu_sample(w, q, k, v, g, per_step) for _ in range(args.steps)]
+        sample(w, q, k, v, g, per_step)
+    runs = [sample(w, q, k, v, g, per_step) for _ in range(args.steps)]
     value = sum(r[0] for r in runs) / len(runs)
     cfg = config_of(w, 1, 2.5 * w.flops(), False)
     cfg["pass"] = "backward (flops = 2.5x forward)"
