@@ -1176,8 +1176,8 @@ int fa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o,
   float* dvec = reinterpret_cast<float*>(ws + L.off_dvec);
   {
     std::lock_guard<std::mutex> lock(g_mutex);  // the planner's first call sets its shared-memory attribute
-    if (fa::launch_bwd_varlen_plan(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, heads_q, heads_kv, kv_tasks,
-                                   q_tasks, counts, st->status, stream) != cudaSuccess)
+    if (fa::launch_bwd_varlen_plan(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, heads_q, heads_kv, causal,
+                                   kv_tasks, q_tasks, counts, st->status, stream) != cudaSuccess)
       return FA_ERR_CUDA;
   }
   const int pad_stride = static_cast<int>(L.pad_stride);

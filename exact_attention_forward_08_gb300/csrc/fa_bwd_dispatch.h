@@ -41,7 +41,7 @@ constexpr int kVarlenPlanMaxBatch = 8192;
 // FA_ERR_INVALID_ARG with site 501 and the sequence in the status word.  The
 // first call sets the kernel's shared-memory attribute (callers serialise it).
 cudaError_t launch_bwd_varlen_plan(const int* cu_q, const int* cu_k, int batch, int64_t total_q, int64_t total_k,
-                                   int Hq, int Hkv, VarlenTask* kv_tasks, VarlenTask* q_tasks, int* counts,
+                                   int Hq, int Hkv, int causal, VarlenTask* kv_tasks, VarlenTask* q_tasks, int* counts,
                                    unsigned int* status, cudaStream_t stream);
 
 // D and LSE * log2(e) for a variable-length batch, per row of each dQ task

@@ -54,7 +54,7 @@ cudaError_t launch_bwd_prep_varlen(int dv, const void* o, const void* dout, cons
 // side in 128-row blocks (longest first, ties by index: the longest-first
 // order of the forward's planner), and writes, in that order, the dK/dV
 // tasks (sequence, K/V head, key block) and the dQ tasks (sequence, query
-// head, query block) of every sequence, each record with the sequence's
+// head, query block) of every sequence, block by block, heaviest first, each record with the sequence's
 // padded row offset in the l2 / dvec vectors (sequences in batch order,
 // 128-row blocks), first rows and lengths.
 // ---------------------------------------------------------------------------
@@ -110,7 +110,7 @@ __device__ long long plan_exclusive_scan(int n, F f, int* out, long long* warp_s
 }
 
 __global__ void __launch_bounds__(kBwdPlanThreads) bwd_varlen_plan_kernel(
-    const int* cu_q, const int* cu_k, int batch, int64_t total_q, int64_t total_k, int Hq, int Hkv,
+    const int* cu_q, const int* cu_k, int batch, int64_t total_q, int64_t total_k, int Hq, int Hkv, int causal,
     VarlenTask* kv_tasks, VarlenTask* q_tasks, int* counts, unsigned int* status) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int bad_index;
@@ -197,10 +197,14 @@ __global__ void __launch_bounds__(kBwdPlanThreads) bwd_varlen_plan_kernel(
       const int b = varlen_sort_index(vals[pos]);
       const int sq = sq_of(b), sk = sk_of(b);
       const int nblk = kind == 0 ? (sk + kBN - 1) / kBN : (sq + kBM - 1) / kBM;
+      // block-major inside a sequence, heaviest block first (under the
+      // mask: the first key blocks for dK/dV, the last query blocks for dQ),
+      // so that round-robin over the list deals each CTA a similar load
+      const int H = kind == 0 ? Hkv : Hq;
       const int i = t - start[pos];
-      const int h = i / nblk;
+      const int j = i / H;
       VarlenTask r;
-      r.b = b, r.g = h, r.mb = i - h * nblk, r.reserved = pad_off[b];
+      r.b = b, r.g = i - j * H, r.mb = (kind == 1 && causal) ? nblk - 1 - j : j, r.reserved = pad_off[b];
       r.q_row0 = cu_q[b], r.sq = sq, r.k_row0 = cu_k[b], r.sk = sk;
       out[t] = r;
     }
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(kBwdPlanThreads) bwd_varlen_plan_kernel(
 }
 
 cudaError_t launch_bwd_varlen_plan(const int* cu_q, const int* cu_k, int batch, int64_t total_q, int64_t total_k,
-                                   int Hq, int Hkv, VarlenTask* kv_tasks, VarlenTask* q_tasks, int* counts,
+                                   int Hq, int Hkv, int causal, VarlenTask* kv_tasks, VarlenTask* q_tasks, int* counts,
                                    unsigned int* status, cudaStream_t stream) {
   static bool attr_set = false;  // set once; the caller holds the library's device lock
   const size_t smem = bwd_varlen_plan_smem_bytes(batch);
@@ -223,7 +227,7 @@ cudaError_t launch_bwd_varlen_plan(const int* cu_q, const int* cu_k, int batch, 
     attr_set = true;
   }
   bwd_varlen_plan_kernel<<<1, kBwdPlanThreads, smem, stream>>>(cu_q, cu_k, batch, total_q, total_k, Hq, Hkv,
-                                                               kv_tasks, q_tasks, counts, status);
+                                                               causal, kv_tasks, q_tasks, counts, status);
   return cudaGetLastError();
 }
 
