@@ -179,14 +179,18 @@ class ClockSampler:
                                    default=None)}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(which: str = "fwd") -> str:
     """Hash of the sources the forward kernels are built from (the backward's
-    and the debug instantiations' files excluded); a stored ncu figure is
-    valid only for it."""
+    and the debug instantiations' files excluded), or with which="bwd" of the
+    backward kernels' sources (fa_bwd* and the headers they include); a
+    stored ncu figure is valid only for it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_forward_08_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith(("fa_bwd", "fa_dbg_", "fa_var_")):
+        if which == "bwd":
+            if not (name.startswith("fa_bwd") or name in ("ptx.cuh", "fa_kernel.cuh", "fa_schedule.h")):
+                continue
+        elif name.startswith(("fa_bwd", "fa_dbg_", "fa_var_")):
             continue
         if name.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(csrc, name), "rb") as f:

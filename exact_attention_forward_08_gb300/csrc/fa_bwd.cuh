@@ -475,17 +475,25 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
         cmax = min(63, sq.sk() - 1 - bi.blk * kBN - cb);  // keys < Sk
         if (CAUSAL) cmax = min(cmax, row + (sq.sk() - sq.sq()) - bi.blk * kBN - cb);
       }
-      const float* l2v = reinterpret_cast<const float*>(smem + L::vec_off(slot));
-      const float* dvv = l2v + 64;
+      // the block's LSE and D per column (dK/dV), read four at a time (every
+      // lane reads the same 16 bytes: one shared-memory wavefront per four
+      // columns, which the tensor cores' operand reads share)
+      const float4* l2v = reinterpret_cast<const float4*>(smem + L::vec_off(slot));
+      const float4* dvv = l2v + 16;
 
       uint32_t r[64];
       tmem_ld64_wait(tS, r);
       float pr[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float lse2 = KIND == kBwdDkDv ? l2v[c] : l2_row;
-        const bool vis = row_ok && c >= cmin && c <= cmax;
-        pr[c] = vis ? ex2_approx(__uint_as_float(r[c]) * sl2 - lse2) : 0.f;
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = KIND == kBwdDkDv ? l2v[c4] : make_float4(l2_row, l2_row, l2_row, l2_row);
+        const float lse2[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 4 * c4 + j;
+          const bool vis = row_ok && c >= cmin && c <= cmax;
+          pr[c] = vis ? ex2_approx(__uint_as_float(r[c]) * sl2 - lse2[j]) : 0.f;
+        }
       }
       if constexpr (C::kShare) {
         // S is in registers: dP_s may now be written over it
@@ -505,9 +513,10 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c0 = 32 * h + 2 * i;
+            const float4 d4 = dvv[c0 / 4];
+            const float d0 = (i & 1) ? d4.z : d4.x, d1 = (i & 1) ? d4.w : d4.y;
             pk[i] = pack_bf16x2(pr[c0], pr[c0 + 1]);
-            dk[i] = pack_bf16x2(pr[c0] * (__uint_as_float(dp[c0]) - dvv[c0]),
-                                pr[c0 + 1] * (__uint_as_float(dp[c0 + 1]) - dvv[c0 + 1]));
+            dk[i] = pack_bf16x2(pr[c0] * (__uint_as_float(dp[c0]) - d0), pr[c0 + 1] * (__uint_as_float(dp[c0 + 1]) - d1));
           }
           tmem_st16(tmem + lane_off + C::pt_col(stage) + static_cast<uint32_t>(16 * h), pk);
           tmem_st16(tmem + lane_off + C::dst_col(stage) + static_cast<uint32_t>(16 * h), dk);
@@ -530,8 +539,12 @@ __device__ __forceinline__ void bwd_row_role(const BwdParams& p, const int stage
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c0 = 32 * q + 2 * i;
-            const float d0 = KIND == kBwdDkDv ? dvv[c0] : d_row;
-            const float d1 = KIND == kBwdDkDv ? dvv[c0 + 1] : d_row;
+            float d0 = d_row, d1 = d_row;
+            if (KIND == kBwdDkDv) {
+              const float4 d4 = dvv[c0 / 4];
+              d0 = (i & 1) ? d4.z : d4.x;
+              d1 = (i & 1) ? d4.w : d4.y;
+            }
             pk[i] = pack_bf16x2(pr[c0] * (__uint_as_float(dp[2 * i]) - d0),
                                 pr[c0 + 1] * (__uint_as_float(dp[2 * i + 1]) - d1));
           }
