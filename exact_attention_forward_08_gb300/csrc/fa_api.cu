@@ -61,6 +61,7 @@ struct DeviceState {
   bool bwd_ready[3 * 2 * 2] = {};   // ((64,64), (128,128), (192,128)) x (dK/dV, dQ) x (non-causal, causal)
   bool bwd_trace_ready[2 * 2] = {};  // the event-log build, (128,128): (dK/dV, dQ) x (non-causal, causal)
   bool bwd_varlen_ready[3 * 2 * 2] = {};  // the variable-length build, as bwd_ready
+  bool bwd_plan_ready = false;            // the backward's varlen planning kernel
   bool plan_ready = false;
 };
 
@@ -1177,7 +1178,7 @@ int fa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o,
   {
     std::lock_guard<std::mutex> lock(g_mutex);  // the planner's first call sets its shared-memory attribute
     if (fa::launch_bwd_varlen_plan(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, heads_q, heads_kv, causal,
-                                   kv_tasks, q_tasks, counts, st->status, stream) != cudaSuccess)
+                                   kv_tasks, q_tasks, counts, st->status, &st->bwd_plan_ready, stream) != cudaSuccess)
       return FA_ERR_CUDA;
   }
   const int pad_stride = static_cast<int>(L.pad_stride);

@@ -38,11 +38,12 @@ constexpr int kVarlenPlanMaxBatch = 8192;
 
 // the backward's planning kernel for a variable-length batch: counts[0] dK/dV
 // tasks, counts[1] dQ tasks, their records; bad cu_seqlens: both counts 0 and
-// FA_ERR_INVALID_ARG with site 501 and the sequence in the status word.  The
-// first call sets the kernel's shared-memory attribute (callers serialise it).
+// FA_ERR_INVALID_ARG with site 501 and the sequence in the status word.  While
+// *attr_ready is false (once per device; callers serialise it) the kernel's
+// shared-memory attribute is set first.
 cudaError_t launch_bwd_varlen_plan(const int* cu_q, const int* cu_k, int batch, int64_t total_q, int64_t total_k,
                                    int Hq, int Hkv, int causal, VarlenTask* kv_tasks, VarlenTask* q_tasks, int* counts,
-                                   unsigned int* status, cudaStream_t stream);
+                                   unsigned int* status, bool* attr_ready, cudaStream_t stream);
 
 // D and LSE * log2(e) for a variable-length batch, per row of each dQ task
 // record (count on the device), at h * vec_hstride + the sequence's padded offset + row

@@ -217,14 +217,13 @@ __global__ void __launch_bounds__(kBwdPlanThreads) bwd_varlen_plan_kernel(
 
 cudaError_t launch_bwd_varlen_plan(const int* cu_q, const int* cu_k, int batch, int64_t total_q, int64_t total_k,
                                    int Hq, int Hkv, int causal, VarlenTask* kv_tasks, VarlenTask* q_tasks, int* counts,
-                                   unsigned int* status, cudaStream_t stream) {
-  static bool attr_set = false;  // set once; the caller holds the library's device lock
+                                   unsigned int* status, bool* attr_ready, cudaStream_t stream) {
   const size_t smem = bwd_varlen_plan_smem_bytes(batch);
-  if (!attr_set) {
+  if (!*attr_ready) {  // once per device (the caller holds the library's lock)
     const cudaError_t e = cudaFuncSetAttribute(bwd_varlen_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(bwd_varlen_plan_smem_bytes(kVarlenPlanMaxBatch)));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    *attr_ready = true;
   }
   bwd_varlen_plan_kernel<<<1, kBwdPlanThreads, smem, stream>>>(cu_q, cu_k, batch, total_q, total_k, Hq, Hkv,
                                                                causal, kv_tasks, q_tasks, counts, status);
