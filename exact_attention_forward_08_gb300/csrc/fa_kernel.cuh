@@ -660,21 +660,21 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
         }
       }
       tmem_wait_st();
-      float sa0, sa1;
-      f2_unpack(f2_add(sum_a, sum_b), sa0, sa1);
-      row_sum = row_sum * acc + (sa0 + sa1);
-
-      if (j == n - 1) {  // final statistics for the epilogue
-        mb_sum[t] = row_sum;
-        mb_ref[t] = ref;
-        mbar_arrive(bar_fin);
-      }
+      // P is in TMEM: signal the MMA warp first, then the row sum
       tc_fence_before();
       if (!skip_p) {
         mbar_arrive(bar_p);
         cnt.inc(kCntSmP + stage);
       }
       tr.ev(p, kEvSmP, static_cast<uint32_t>(j));
+      float sa0, sa1;
+      f2_unpack(f2_add(sum_a, sum_b), sa0, sa1);
+      row_sum = row_sum * acc + (sa0 + sa1);
+      if (j == n - 1) {  // final statistics for the epilogue
+        mb_sum[t] = row_sum;
+        mb_ref[t] = ref;
+        mbar_arrive(bar_fin);
+      }
     }
   }
   tr.finish(p);
