@@ -35,12 +35,22 @@
 // Hand-offs per stage s and K/V block j (mbarrier names follow the pages'
 // "Softmax, correction and barrier hand-off" section):
 //   s_full[s]    MMA commit after S_s = Q_s K_j^T            -> softmax
-//   corr_full[s] softmax posted acc_scale (right after the row
-//                max, before the exponentials)               -> correction
-//   fin_full[s]  last block only: row_sum and the reference
-//                posted for the epilogue                     -> correction
+//   corr_full[s] blocks after a task's first: softmax posted
+//                acc_scale (right after the row max, before
+//                the exponentials)                           -> correction
+//   fin_full[s][t & 1]  last block of task t only: row_sum and the
+//                reference posted for the epilogue, in one of
+//                two slots by task parity                    -> correction
 //   p_full[s]    count 256: 128 softmax threads (P written) +
-//                128 correction threads (O rescaled or not)  -> PV MMA
+//                128 correction threads (O rescaled or not;
+//                for a task's first block: O free, an arrival
+//                made as soon as the previous task's epilogue
+//                has read O_s out of TMEM)                   -> PV MMA
+// The two fin_full slots let the correction warps signal a stage's last block
+// without first reading its final statistics (the slot a task writes was read
+// two tasks earlier, before the P V that the writer's S depends on); the
+// early O-free arrival lets a task's first P V start behind one epilogue, not
+// behind both stages' epilogues and the next task's first row maximum.
 //   o_done[s]    MMA commit after the stage's last P V of a
 //                task                                        -> epilogue
 //   task_full[r] / task_empty[r]  (DYN only) the TMA thread takes the next
@@ -147,7 +157,10 @@ struct Layout {
   static constexpr int kQBytes = NQC * kChunkBytes;
   static constexpr int kSlotBytes = NQC * kChunkBytes;  // a ring slot holds one K tile or one V tile
   static constexpr int kStageOBytes = kChunkBytes;
-  static constexpr int kMboxBytes = 2 * 3 * 128 * 4;   // [stage][acc_scale,row_sum,ref][row]
+  // [stage][acc_scale, (row_sum, ref) x task parity][row]: the final statistics
+  // alternate between two slots so that a stage's last-block P V need not wait
+  // for them to be read
+  static constexpr int kMboxBytes = 2 * 5 * 128 * 4;
   static constexpr int kMaxSmem = 232448;              // 227 KB per CTA (opt-in)
   static constexpr int kFixed = 2 * kQBytes + kStageOBytes + kMboxBytes + 1024 + 1024;
   static constexpr int NS_fit = (kMaxSmem - kFixed) / kSlotBytes;
@@ -169,12 +182,13 @@ struct Layout {
   static constexpr int bPFull = bSFull + 2;
   static constexpr int bODone = bPFull + 2;
   static constexpr int bCorrFull = bODone + 2;
-  static constexpr int bFinFull = bCorrFull + 2;  // final row_sum / reference posted (count 128)
-  static constexpr int bStagger = bFinFull + 2;   // [2] (VAR & kVarStagger) stage s finished its exps (count 128)
+  static constexpr int bFinFull = bCorrFull + 2;  // [stage][task parity] final row_sum / reference posted (count 128)
+  static constexpr int bStagger = bFinFull + 4;   // [2] (VAR & kVarStagger) stage s finished its exps (count 128)
   static constexpr int bEpiFull = bStagger + 2;   // WG2: staging tile written (count 128)
   static constexpr int bStageFree = bEpiFull + 1; // WG2: TMA store finished reading staging (count 1)
   static constexpr int bDrain = bStageFree + 1;   // MMA drain at exit
-  static constexpr int bTaskFull = bDrain + 1;               // [kTaskRing] (DYN) count 1
+  static constexpr int bSink = bDrain + 1;      // arrivals nobody waits for (count 256)
+  static constexpr int bTaskFull = bSink + 1;                // [kTaskRing] (DYN) count 1
   static constexpr int bTaskEmpty = bTaskFull + kTaskRing;   // [kTaskRing] (DYN) count kTaskReaders
   static constexpr int kNumBars = bTaskEmpty + kTaskRing;
 
@@ -494,16 +508,18 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
   const uint32_t tS = tmem + (static_cast<uint32_t>(t & ~31) << 16) + static_cast<uint32_t>(stage * 128);
   const uint32_t bar_s = sbase + L::oBar + 8 * (L::bSFull + stage);
   const uint32_t bar_corr = sbase + L::oBar + 8 * (L::bCorrFull + stage);
+  const uint32_t bar_sink = sbase + L::oBar + 8 * L::bSink;
   const uint32_t bar_p = sbase + L::oBar + 8 * (L::bPFull + stage);
-  const uint32_t bar_fin = sbase + L::oBar + 8 * (L::bFinFull + stage);
+  const uint32_t bar_fin = sbase + L::oBar + 8 * (L::bFinFull + 2 * stage);  // [task parity]
   constexpr bool STAG = (VAR & kVarStagger) != 0;
   uint32_t stag_k = 0;  // staggered blocks of this stage so far (STAG)
-  float* mb_acc = mbox + (stage * 3 + 0) * 128;
-  float* mb_sum = mbox + (stage * 3 + 1) * 128;
-  float* mb_ref = mbox + (stage * 3 + 2) * 128;
+  float* mb_acc = mbox + (stage * 5 + 0) * 128;
+  float* mb_fin = mbox + (stage * 5 + 1) * 128;  // [task parity][row_sum, ref][row]
   const float sl2 = p.scale_log2;
   const float neg_tau = -p.tau;
   const bool skip_p = (p.debug_flags & kDebugSkipPArrive) != 0;
+  // bit 0: phase of the S barrier; bit 1: parity of the tasks with blocks of
+  // this stage so far (the slot of the final statistics).  One register.
   uint32_t phase = 0;
   const int num_tasks = task_count<VARLEN>(p);
   Tracer<(VAR & kVarTrace) != 0, -1> tr;  // track = stage
@@ -542,7 +558,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
 
     for (int j = 0; j < n; ++j) {
       tr.ev(p, kEvSmWait, static_cast<uint32_t>(j));
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_s, phase, wc, kSiteSoftmaxS));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_s, phase & 1u, wc, kSiteSoftmaxS));
       if (!ok) {
         tr.finish(p);
         return;
@@ -595,9 +611,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
       ref = (row_max == -INFINITY) ? 0.f : row_max * sl2;
 
       // post acc_scale now: the correction warps rescale O (when needed) while
-      // the exponentials below run, off the path to the PV MMA
+      // the exponentials below run, off the path to the PV MMA.  A first block
+      // is not posted (its acc_scale is 1 and its P V writes O afresh; the
+      // correction warps read the slot from the second block on): its arrival
+      // goes to a barrier nobody waits for, chosen without a branch.
       mb_acc[t] = acc;
-      mbar_arrive(bar_corr);
+      mbar_arrive(j > 0 ? bar_corr : bar_sink);
 
       // p = 2^(s * scale_log2 - ref): one packed FMA per pair, then ex2; the
       // row sum is accumulated in packed pairs of fp32.  P goes to TMEM as
@@ -670,10 +689,12 @@ __device__ __forceinline__ void softmax_role(const Params& p, const int stage, c
       float sa0, sa1;
       f2_unpack(f2_add(sum_a, sum_b), sa0, sa1);
       row_sum = row_sum * acc + (sa0 + sa1);
-      if (j == n - 1) {  // final statistics for the epilogue
-        mb_sum[t] = row_sum;
-        mb_ref[t] = ref;
-        mbar_arrive(bar_fin);
+      if (j == n - 1) {  // final statistics for the epilogue, in this task's slot
+        const uint32_t par = (phase >> 1) & 1u;
+        mb_fin[(2 * par) * 128 + t] = row_sum;
+        mb_fin[(2 * par + 1) * 128 + t] = ref;
+        mbar_arrive(bar_fin + 8 * par);
+        phase ^= 2u;
       }
     }
   }
@@ -704,7 +725,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   uint8_t* staging = smem + L::oStage;
   const uint32_t staging_s = sbase + L::oStage;
   uint32_t corr_phase[2] = {0u, 0u};
-  uint32_t fin_phase[2] = {0u, 0u};
+  uint32_t fin_k[2] = {0u, 0u};     // final statistics read (one per task with blocks; slot = parity)
   uint32_t od_count[2] = {0u, 0u};  // o_done phases consumed (one per task with blocks)
   uint32_t chunks = 0;              // epilogue chunks stored through the staging tile so far
   const int num_tasks = task_count<VARLEN>(p);
@@ -716,11 +737,34 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
   Tracer<(VAR & kVarTrace) != 0, 2> tr;
   tr.init(p, t == 0);
   Counts<CK> cnt;
+  // The P-ready barrier of a stage's first block in a task also says that O is
+  // free: these warps arrive on it as soon as the previous task's epilogue has
+  // read the stage's O out of TMEM (here: before the first task), not when the
+  // block comes up, so that the next task's first P V need not wait behind the
+  // other stage's epilogue.
+  auto o_free = [&](int s) {
+    tc_fence_before();
+    mbar_arrive(bar0 + 8 * (L::bPFull + s));
+    tr.ev(p, kEvCoArrive, static_cast<uint32_t>(s << 16));
+  };
+  // the final row sum and reference of stage s in the current task (the
+  // softmax alternates between two slots by task parity)
+  auto read_fin = [&](int s, float& sum, float& ref) -> bool {
+    const uint32_t par = fin_k[s] & 1u;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bFinFull + 2 * s + static_cast<int>(par)),
+                                           (fin_k[s] >> 1) & 1u, wc, kSiteCorrFin)))
+      return false;
+    ++fin_k[s];
+    sum = mbox[(s * 5 + 1 + 2 * static_cast<int>(par)) * 128 + t];
+    ref = mbox[(s * 5 + 2 + 2 * static_cast<int>(par)) * 128 + t];
+    return true;
+  };
   if constexpr (CK) {  // this warp's TMEM lane quadrant is (warp % 4)
     if (!__all_sync(0xffffffffu, dbg_check((t & ~31) == 32 * ((threadIdx.x >> 5) & 3), wc, kSiteCheckTmem)))
       goto out;
   }
-
+  o_free(0);
+  o_free(1);
   if constexpr (kPre) {
     const int t0 = read_task<DQ, DV, DYN>(0, num_tasks, bar0, ring, wc, kSiteCorrTask);
     if (t0 >= 0) nxt = get_task<VARLEN, SPLIT, CAUSAL, DIRECT, !DYN>(p, t0);
@@ -733,21 +777,30 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
     tr.ev(p, kEvCoTask, static_cast<uint32_t>(task));
     float fin_sum[2] = {0.f, 0.f}, fin_ref[2] = {0.f, 0.f};
 
-    for (int j = 0; j < tk.nmax; ++j) {
+    // first blocks: nothing to rescale, and their P-ready arrival was made
+    // when O became free
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (tk.n[s] > 0) {
+        cnt.inc(kCntCoCorr + s);
+        cnt.inc(kCntCoP + s);
+      }
+    }
+    for (int j = 1; j < tk.nmax; ++j) {
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (j >= tk.n[s]) continue;
-        bool ok = __all_sync(0xffffffffu,
-                             mbar_wait(bar0 + 8 * (L::bCorrFull + s), corr_phase[s], wc, kSiteCorrCorr));
+        const bool ok = __all_sync(0xffffffffu,
+                                   mbar_wait(bar0 + 8 * (L::bCorrFull + s), corr_phase[s], wc, kSiteCorrCorr));
         if (!ok) goto out;
         corr_phase[s] ^= 1u;
         cnt.inc(kCntCoCorr + s);
         tr.ev(p, kEvCoCorr, static_cast<uint32_t>(s << 16 | j));
-        const float acc = mbox[(s * 3 + 0) * 128 + t];
+        const float acc = mbox[(s * 5 + 0) * 128 + t];
         // warp-uniform skip of the O round trip when no row moved its
         // reference.  The softmax posted acc_scale after S_j was ready, and S_j
         // ready implies that P V_{j-1} completed, so O is final here.
-        if (j > 0 && __any_sync(0xffffffffu, acc != 1.f)) {
+        if (__any_sync(0xffffffffu, acc != 1.f)) {
           if constexpr (COUNT) {
             if ((p.debug_flags & kDebugCountRescale) && (t & 31) == 0) atomicAdd(p.status + 3, 1u);
           }
@@ -763,13 +816,6 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
           }
           tmem_wait_st();
           tr.ev(p, kEvCoRescaled, static_cast<uint32_t>(s << 16 | j));
-        }
-        if (j == tk.n[s] - 1) {  // last block: the final row sum and reference
-          ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bFinFull + s), fin_phase[s], wc, kSiteCorrFin));
-          if (!ok) goto out;
-          fin_phase[s] ^= 1u;
-          fin_sum[s] = mbox[(s * 3 + 1) * 128 + t];
-          fin_ref[s] = mbox[(s * 3 + 2) * 128 + t];
         }
         tc_fence_before();
         mbar_arrive(bar0 + 8 * (L::bPFull + s));
@@ -802,6 +848,8 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
       const int row_pos = DIRECT ? fdiv(t, pr.fd_pack) : t / pr.pack;
       const int pos = pos0 + row_pos;
       const int head = tk.g * pr.pack + (t - row_pos * pr.pack);
+      if (has && !read_fin(s, fin_sum[s], fin_ref[s])) goto out;
+      if (merge && !read_fin(1, fin_sum[1], fin_ref[1])) goto out;
       if (has) {  // o_done completes once per task: after the stage's last P V
         const bool ok =
             __all_sync(0xffffffffu, mbar_wait(bar0 + 8 * (L::bODone + s), od_count[s] & 1u, wc, kSiteCorrODone));
@@ -861,6 +909,7 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
                                            __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
           }
         }
+        if (has) o_free(s);
         if (store) p.lpart[((static_cast<int64_t>(tk.split) * pr.B + tk.b) * pr.Hq + head) * pr.Sq + pos] = lse;
         continue;
       }
@@ -929,6 +978,10 @@ __device__ __forceinline__ void correction_role(const Params& p, const uint32_t 
 #pragma unroll
             for (int q = 0; q < 4; ++q) row[(half * 4 + q) ^ (t & 7)] = v[q];  // 128-byte swizzle of the TMA box
           }
+        }
+        if (c == L::NVC - 1) {  // the stage's O has been read out of TMEM
+          if (has) o_free(s);
+          if (merge) o_free(1);
         }
         if (direct) continue;
         fence_proxy_async_smem();
@@ -1232,15 +1285,15 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
     if (!check_task<CK>(p, tk, task, wc)) break;
     tr.ev(p, kEvLdTask, static_cast<uint32_t>(task));
     if (tk.nmax == 0) continue;
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      if (tk.n[s] == 0) continue;
-      if (q_uses[s] > 0 && !mbar_wait(bar(L::bQEmpty + s), (q_uses[s] - 1u) & 1u, wc, kSiteLoadQ)) goto out;
+    // Q tile of stage s (none when the stage has no block)
+    auto load_q = [&](int s) -> bool {
+      if (tk.n[s] == 0) return true;
+      if (q_uses[s] > 0 && !mbar_wait(bar(L::bQEmpty + s), (q_uses[s] - 1u) & 1u, wc, kSiteLoadQ)) return false;
       if constexpr (CK) {  // the Q tile starts inside q
         const int row = tk.q_row0 + tk.pos0[s];
         if (!dbg_check(row >= 0 && row < pr.Sq && tk.g >= 0 && tk.g < pr.groups && tk.bc >= 0 && tk.bc < pr.B, wc,
                        kSiteCheckQCoord))
-          goto out;
+          return false;
       }
       const uint32_t qb = bar(L::bQFull + s);
       mbar_arrive_expect_tx(qb, L::NQC * kChunkBytes);
@@ -1249,7 +1302,33 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
         tma_load_5d(dst + c * kChunkBytes, &p.tm_q, qb, c * 64, 0, tk.g, tk.q_row0 + tk.pos0[s], tk.bc);
       ++q_uses[s];
       tr.ev(p, kEvLdQ, static_cast<uint32_t>(s));
-    }
+      return true;
+    };
+    // K_j (which = 0) or V_j (1) into the next ring slot
+    auto load_kv = [&](int which, int j) -> bool {
+      const uint32_t slot = kv_it % L::NS;
+      tr.ev(p, kEvLdKvWait, kv_it);
+      if (kv_it >= static_cast<uint32_t>(L::NS) &&
+          !mbar_wait(bar(L::bKvEmpty + static_cast<int>(slot)), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
+        return false;
+      if constexpr (CK) {  // the K/V tile starts inside k / v
+        const int row = tk.k_row0 + j * kBN;
+        if (!dbg_check(row >= 0 && row < pr.Sk && tk.kvh >= 0 && tk.kvh < pr.Hkv && tk.bc >= 0 && tk.bc < pr.B, wc,
+                       kSiteCheckKvCoord))
+          return false;
+      }
+      const uint32_t fb = bar(L::bKvFull + static_cast<int>(slot));
+      const uint32_t dst = sbase + L::oRing + slot * L::kSlotBytes;
+      const int nch = which == 0 ? L::NQC : L::NVC;
+      mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nch * kChunkBytes));
+      for (int c = 0; c < nch; ++c)
+        tma_load_4d(dst + c * kChunkBytes, which == 0 ? static_cast<const void*>(&p.tm_k) : &p.tm_v, fb, c * 64,
+                    tk.kvh, tk.k_row0 + j * kBN, tk.bc);
+      tr.ev(p, kEvLdKv, kv_it);
+      ++kv_it;
+      return true;
+    };
+    if (!load_q(0) || !load_q(1)) goto out;
     if constexpr (TS) {
       if (tk.ksplit != 0) {  // key-split tail task: the order the MMA warp reads
         // the next ring tile: K (which = 0) or V (1) of the block at key row `row`
@@ -1292,26 +1371,7 @@ __device__ __forceinline__ void load_role(const Params& p, const uint32_t sbase,
     for (int j = 0; j < tk.nmax; ++j) {
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // K_j then V_j
-        const uint32_t slot = kv_it % L::NS;
-        tr.ev(p, kEvLdKvWait, kv_it);
-        if (kv_it >= static_cast<uint32_t>(L::NS) &&
-            !mbar_wait(bar(L::bKvEmpty + static_cast<int>(slot)), ((kv_it / L::NS) - 1u) & 1u, wc, kSiteLoadKv))
-          goto out;
-        if constexpr (CK) {  // the K/V tile starts inside k / v
-          const int row = tk.k_row0 + j * kBN;
-          if (!dbg_check(row >= 0 && row < pr.Sk && tk.kvh >= 0 && tk.kvh < pr.Hkv && tk.bc >= 0 && tk.bc < pr.B, wc,
-                         kSiteCheckKvCoord))
-            goto out;
-        }
-        const uint32_t fb = bar(L::bKvFull + static_cast<int>(slot));
-        const uint32_t dst = sbase + L::oRing + slot * L::kSlotBytes;
-        const int nch = which == 0 ? L::NQC : L::NVC;
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nch * kChunkBytes));
-        for (int c = 0; c < nch; ++c)
-          tma_load_4d(dst + c * kChunkBytes, which == 0 ? static_cast<const void*>(&p.tm_k) : &p.tm_v, fb,
-                      c * 64, tk.kvh, tk.k_row0 + j * kBN, tk.bc);
-        tr.ev(p, kEvLdKv, kv_it);
-        ++kv_it;
+        if (!load_kv(which, j)) goto out;
       }
     }
   }
@@ -1373,7 +1433,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(b + 8 * (L::bPFull + s), 256);
       mbar_init(b + 8 * (L::bODone + s), 1);
       mbar_init(b + 8 * (L::bCorrFull + s), 128);
-      mbar_init(b + 8 * (L::bFinFull + s), 128);
+      mbar_init(b + 8 * (L::bFinFull + 2 * s), 128);
+      mbar_init(b + 8 * (L::bFinFull + 2 * s + 1), 128);
       mbar_init(b + 8 * (L::bStagger + s), 128);
     }
     for (int i = 0; i < L::NS; ++i) {
@@ -1383,6 +1444,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     mbar_init(b + 8 * L::bEpiFull, 128);
     mbar_init(b + 8 * L::bStageFree, 1);
     mbar_init(b + 8 * L::bDrain, 1);
+    mbar_init(b + 8 * L::bSink, 256);
     for (int r = 0; r < kTaskRing; ++r) {
       mbar_init(b + 8 * (L::bTaskFull + r), 1);
       mbar_init(b + 8 * (L::bTaskEmpty + r), kTaskReaders);
