@@ -560,7 +560,7 @@ static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float
   }
 
   fa::Problem prob = fa::make_problem(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal,
-                                      st->l2_bytes / 2, opt.pack);
+                                      fa::causal_section_budget(st->l2_bytes), opt.pack);
   if (split_api) {
     fa::set_splits(prob, num_splits > 0 ? num_splits : fa::choose_splits(prob, st->sms));
     if (prob.splits > 1) {
@@ -1290,7 +1290,7 @@ int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_
     return FA_ERR_INVALID_ARG;
   if (kernel_index(d_qk, d_v, 0, 0) < 0) return FA_ERR_UNSUPPORTED;
   if (pack < 0 || (pack > 0 && (fa::kBM % pack != 0 || (heads_q / heads_kv) % pack != 0))) return FA_ERR_INVALID_ARG;
-  if (l2_bytes <= 0) l2_bytes = int64_t(64) << 20;
+  if (l2_bytes <= 0) l2_bytes = fa::kCausalSectionBytes;  // what fa_fwd uses on an L2 of 16 MiB or more
   const fa::Problem p =
       fa::make_problem(batch, heads_q, heads_kv, seqlen_q, seqlen_k, d_qk, d_v, causal ? 1 : 0, l2_bytes, pack);
   out->batch = p.B, out->heads_q = p.Hq, out->heads_kv = p.Hkv, out->seqlen_q = p.Sq, out->seqlen_k = p.Sk;

@@ -20,7 +20,8 @@
 //  * Task order: linear for the non-causal case (uniform cost).  For the
 //    causal case longest-processing-time first: the heavier half of the
 //    m_blocks (m >= M - ceil(M/2)) in decreasing order inside sections of
-//    `section_units` (b, g) units whose K/V fit in L2 together, then the
+//    `section_units` (b, g) units whose K/V fill a section budget (about
+//    8 MiB, well inside L2: causal_section_budget), then the
 //    lighter half level by level (m decreasing, all units per level).  Light
 //    tasks read only the first half of a unit's K/V, and ending the list with
 //    the cheapest tasks keeps the last CTAs from finishing late (a static
@@ -227,6 +228,18 @@ FA_HD Problem make_problem_core(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk
   p.splits = 1;
   p.split_blocks = p.kv_blocks;
   return p;
+}
+
+// K/V bytes per section of the fixed-length causal order: about 8 MiB (at
+// most half the L2).  Measured on GB300 (L2 126 MiB) against half the L2:
+// causal 2k and 8k +2 %, 4k +1.5 %, 1k +0.8 %, 16k +0.4 %, 32k -0.4 %, GQA /
+// MQA / (192, 128) within +-0.3 % (2 or 4 MiB: causal 8k -1 %, 4k -3 % at
+// 2 MiB).  Few units per section keep the CTAs that run at one time on the
+// K/V of few units, which they then read out of L2 together.
+constexpr int64_t kCausalSectionBytes = int64_t(8) << 20;
+FA_HD int64_t causal_section_budget(int64_t l2_bytes) {
+  const int64_t half = l2_bytes / 2;
+  return half < kCausalSectionBytes ? half : kCausalSectionBytes;
 }
 
 FA_HD Problem make_problem(int B, int Hq, int Hkv, int Sq, int Sk, int d_qk, int d_v, int causal,

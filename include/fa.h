@@ -486,7 +486,8 @@ typedef struct fa_task {
                           key blocks [0, key_split), stage 1 the next n_blocks[1]; else 0 */
 } fa_task;
 
-/* l2_bytes: L2 budget used to size causal sections (0 selects 64 MiB). */
+/* l2_bytes: K/V bytes per section of the causal order (0 selects 8 MiB: what
+   fa_fwd uses, min(L2 size / 2, 8 MiB), on an L2 of 16 MiB or more). */
 int fa_make_plan(int batch, int heads_q, int heads_kv, int seqlen_q, int seqlen_k, int d_qk, int d_v,
                  int causal, int64_t l2_bytes, int pack, fa_plan* out);
 int fa_plan_task(const fa_plan* plan, int64_t task, fa_task* out);
