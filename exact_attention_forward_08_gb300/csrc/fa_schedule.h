@@ -40,10 +40,12 @@
 //  * Paired causal order (static assignment): m_blocks m and M-1-m of a unit
 //    see (2m + 1.5) and (2M - 2m - 0.5) key blocks on average, a constant
 //    sum.  With M even, the list is laid out for G CTAs in blocks of 2G
-//    entries: G heavy tasks (pair i: the i-th task of the heavier half in
-//    the L2-section order above) followed by their G light complements, so
-//    that CTA c runs the heavy task of pair bG + c and then its complement;
-//    every CTA then gets the same work per two waves.  The r = P mod G pairs
+//    entries: G light tasks followed by their G heavy complements (pair i:
+//    the i-th task of the heavier half in the L2-section order above and its
+//    complement), so that CTA c runs the light task of pair bG + c and then
+//    its heavy complement, which re-reads the K/V prefix the light task just
+//    brought into L2 before streaming the rest; every CTA then gets the same
+//    work per two waves.  The r = P mod G pairs
 //    left over (P = units * M / 2) go last.  When 2r <= G each pair's two
 //    tasks go to two CTAs.  Otherwise the left-over pairs are taken from the
 //    heaviness levels whose heavy task costs about r / G of a pair: their
@@ -398,18 +400,18 @@ FA_HD Task decode_task_k(const Problem& p, int t) {
     bool light = false;  // paired order: the light complement of pair t
     if (PAIR && p.pair_grid > 0) {
       const int G = p.pair_grid;
-      if (t < p.pair_body) {  // blocks of G heavy tasks and their G complements
+      if (t < p.pair_body) {  // blocks of G light complements and their G heavy tasks
         const int blk = FAST ? fdiv(t, p.fd_pair2g) : t / (2 * G);
         const int w = t - blk * 2 * G;
-        light = w >= G;
-        t = blk * G + (light ? w - G : w);
+        light = w < G;
+        t = blk * G + (light ? w : w - G);
       } else {  // the pairs left over
         const int tt = t - p.pair_body;
         int pos;
-        if (!p.pair_pack) {  // both tasks of pair pos: positions pos and pos + half
+        if (!p.pair_pack) {  // both tasks of pair pos: positions pos (light) and pos + half (heavy)
           const int half = p.pair_split_tail ? p.pair_r : G;
-          light = tt >= half;
-          pos = light ? tt - half : tt;
+          light = tt < half;
+          pos = light ? tt : tt - half;
         } else {  // heavy tasks on CTAs 0 .. r-1, light ones dealt over the other CTAs
           const int w = FAST ? fdiv(tt, p.fd_grid) : tt / G;
           const int c = tt - w * G;

@@ -180,10 +180,10 @@ def test_paired_order(case):
         assert key not in seen
         seen[key] = (tuple(t.pos0), tuple(t.n_blocks))
     assert seen == plain
-    # inside the whole blocks CTA c runs a heavy task and then its complement
+    # inside the whole blocks CTA c runs a light task and then its heavy complement
     for i in range(0, body, 2 * grid):
         for c in range(grid):
-            h, l = tasks[i + c], tasks[i + grid + c]
+            l, h = tasks[i + c], tasks[i + grid + c]
             assert (h.b, h.g) == (l.b, l.g) and h.mblock + l.mblock == M - 1 and h.mblock >= M // 2
             if plan.pack == 1:  # (4m + 3) + (4(M - 1 - m) + 3) key blocks
                 assert blocks(h) + blocks(l) == 4 * M + 2
@@ -199,10 +199,10 @@ def test_paired_order(case):
         assert sorted((b, g, M - 1 - m) for b, g, m in heavy) == sorted((t.b, t.g, t.mblock) for _, t in lights)
     elif r and 2 * r <= grid:
         for c in range(r):
-            assert tail[c].mblock + tail[r + c].mblock == M - 1
+            assert tail[c].mblock + tail[r + c].mblock == M - 1 and tail[r + c].mblock >= M // 2
     elif r:
         for c in range(r):
-            assert tail[c].mblock + tail[grid + c].mblock == M - 1
+            assert tail[c].mblock + tail[grid + c].mblock == M - 1 and tail[grid + c].mblock >= M // 2
         assert all(blocks(t) == 0 for t in tail[r:grid])
 
 
