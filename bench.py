@@ -968,10 +968,15 @@ def trace_run_bwd(args) -> dict:
     out = {"config": args.config, "pass": "bwd", "workload": f"{w.name}: {w.notes}", "trace_ctas": args.trace_ctas,
            "call_ms_default": round(base_ms, 4), "call_ms_trace_build": round(trace_ms, 4),
            "unit": "SM clock cycles"}
+    raw = {}
     for kind, name in ((0, "dkdv"), (1, "dq")):
         ctas = tr.decode(host[kind * words:(kind + 1) * words], args.trace_ctas, args.trace_cap)
+        raw[name] = ctas
         out[f"{name}_records_dropped"] = sum(max(0, n - args.trace_cap) for c in ctas for n in c["_counts"].values())
         out[f"{name}_summary"] = tr.summarize_bwd(ctas)
+    if args.trace_out:
+        with open(args.trace_out, "w") as f:
+            json.dump(raw, f)
     return out
 
 
