@@ -226,6 +226,20 @@ def test_plan_sections_follow_l2_budget(fa):
     assert plan.section_units == 1
 
 
+def test_plan_default_section_budget_is_8_mib(fa):
+    """Without an explicit budget the plan sizes causal sections as the launch
+    does on a large L2: about 8 MiB of K/V per section."""
+    # causal 1k, 32 x 16 heads: K+V per (b, head) = 1024 * 256 * 2 B = 512 KiB -> 16 units
+    plan = fa.fa_make_plan(32, 16, 16, 1024, 1024, 128, 128, 1)
+    assert plan.section_units == 16
+    # causal 8k, 4 x 16: 4 MiB per unit -> 2 units
+    plan = fa.fa_make_plan(4, 16, 16, 8192, 8192, 128, 128, 1)
+    assert plan.section_units == 2
+    # more K/V per unit than the budget: one unit per section
+    plan = fa.fa_make_plan(1, 16, 16, 32768, 32768, 128, 128, 1)
+    assert plan.section_units == 1
+
+
 def test_plan_rejects_bad_pack(fa):
     with pytest.raises(fa.FaError):
         fa.fa_make_plan(1, 8, 2, 64, 64, 128, 128, 0, pack=3)
