@@ -8,9 +8,10 @@ mean|O - O_ref| <= 2e-3 over all of O (bf16 outputs of unit-normal inputs),
 arithmetic's, 2^-7 max|V|: P is rounded to bf16 (relative error up to 2^-8)
 for the P V product while the row sum stays fp32, and O is rounded to bf16.
 The oracle runs on all host cores (about a minute per configuration on 16
-cores); the other configurations of the causal sweep are covered by
-test_gpu_parity.py (every element of small problems, sampled rows at full
-size).
+cores); causal 16k and 32k are covered by test_gpu_parity.py (every element
+of small problems, sampled rows at full size).  The short causal rows run
+the direct-epilogue kernel and the variable-length batches the varlen
+kernel, so both are checked here on every element too.
 """
 import numpy as np
 import pytest
@@ -24,8 +25,8 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 MAX_TOL, MEAN_TOL, LSE_TOL = 2e-2, 2e-3, 1e-3
 
 # the MHA configuration, GQA and MQA, the asymmetric head dims with the wide
-# dynamic range, and causal 8k from the sweep
-FULL = ["mha8k", "gqa", "mqa", "asym", "causal8k"]
+# dynamic range, and causal 1k, 2k, 4k (direct epilogue) and 8k from the sweep
+FULL = ["mha8k", "gqa", "mqa", "asym", "causal1k", "causal2k", "causal4k", "causal8k"]
 
 
 @pytest.fixture(scope="module")
@@ -64,5 +65,36 @@ def test_every_element_at_full_size(fa, name):
     print(f"{name}: every element, max|dO| = {emax:.3e} (bound {max_bound:.3e}), mean|dO| = {emean:.3e}, "
           f"max|dLSE| = {lerr:.3e} ({og.size} outputs, {lg.size} rows)")
     assert emax <= max_bound, emax
+    assert emean <= MEAN_TOL, emean
+    assert lerr <= LSE_TOL, lerr
+
+
+@pytest.mark.parametrize("name", ["varlen32k", "varlen32k_nc"])
+def test_varlen_every_element_at_full_size(fa, name):
+    """The variable-length batches of the benchmark (15 sequences, 32k tokens)
+    on every element against the oracle's per-sequence attention."""
+    w = synthetic.varlen_workloads()[name]
+    q, k, v = w.generate()
+    cu = lambda c: torch.tensor(np.asarray(c, dtype=np.int32), device="cuda")
+    o, lse = fa.attention_forward_varlen(to_dev(q), to_dev(k), to_dev(v), cu(w.cu_seqlens_q), cu(w.cu_seqlens_k),
+                                         causal=w.causal, scale=w.softmax_scale)
+    torch.cuda.synchronize()
+    code, detail = fa.fa_device_status()
+    assert code == 0, detail
+    og = o.float().cpu().numpy().astype(np.float64).reshape(-1, w.d_v)
+    lg = lse.cpu().numpy().astype(np.float64).T.reshape(-1)
+    del o, lse
+    o_ref, lse_ref = oracle.attn_fwd_varlen(q, k, v, w.cu_seqlens_q, w.cu_seqlens_k, causal=w.causal,
+                                            scale=w.softmax_scale)
+    o_ref = o_ref.reshape(-1, w.d_v)
+    lse_ref = lse_ref.T.reshape(-1)
+    # every row of these batches lies in a sequence with keys
+    assert np.all(np.isfinite(lse_ref)) and np.all(np.isfinite(lg))
+    err = np.abs(og - o_ref)
+    emax, emean = float(err.max()), float(err.mean())
+    lerr = float(np.abs(lg - lse_ref).max())
+    print(f"{name}: every element, max|dO| = {emax:.3e}, mean|dO| = {emean:.3e}, max|dLSE| = {lerr:.3e} "
+          f"({og.size} outputs, {lg.size} rows)")
+    assert emax <= MAX_TOL, emax
     assert emean <= MEAN_TOL, emean
     assert lerr <= LSE_TOL, lerr
