@@ -190,6 +190,17 @@ def test_backward_mid_size_full(fa, causal):
     check(w, inputs, grads, f"mid causal={causal}")
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["causal1k", "causal8k"])
+def test_backward_benchmark_configs_full(fa, name):
+    """Every element of dQ, dK, dV of two benchmark configurations at full
+    size (the inputs and dO the backward bench uses), in the launch it times:
+    the short causal tasks and the long paired ones."""
+    w = synthetic.workloads()[name]
+    inputs, grads = run(fa, w, w.seed)
+    check(w, inputs, grads, f"full {name}")
+
+
 # Paired causal order of the backward kernels: the task of heaviness rank q
 # and its complement (blocks - 1 - q) on one CTA in consecutive waves.  Every
 # task computes what it computes in the plain order, so the gradients (written
