@@ -56,6 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--store-mode", type=int, default=0, choices=(0, 1, 2),
+                    help="ablation: the fixed-length epilogue (fa_options.store_mode): 0 chosen by the library, "
+                         "1 staged TMA stores, 2 direct stores from registers")
     ap.add_argument("--no-balance", action="store_true",
                     help="ablation: the plain static task order (fa_options.no_balance = 1)")
     ap.add_argument("--stagger", action="store_true",
@@ -510,6 +513,9 @@ def run_ours(args):
         if args.stagger:
             opts = opts or fa.default_options()
             opts.stagger = 1
+        if args.store_mode:
+            opts = opts or fa.default_options()
+            opts.store_mode = args.store_mode
         launches_per_step = 1
 
         def launch(ins, outs, stream):
@@ -575,10 +581,13 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, world, flops, args.dynamic, splits,
-                            "plain order (ablation)" if args.no_balance else
-                            (balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count) +
-                             "; staggered exponentials (ablation)") if args.stagger else
-                            balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count)),
+                            ("plain order (ablation)" if args.no_balance else
+                             (balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count) +
+                              "; staggered exponentials (ablation)") if args.stagger else
+                             balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count)) +
+                            ({1: "; staged TMA epilogue forced (ablation)",
+                              2: "; direct epilogue forced (ablation)"}.get(args.store_mode, "")
+                             if not (args.dynamic or is_varlen(w) or splits > 1) else "")),
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
         "gpu_launches": args.steps * launches_per_step,

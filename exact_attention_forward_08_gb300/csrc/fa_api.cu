@@ -36,9 +36,13 @@ constexpr int kVariants = fa::kNumModes;
 constexpr int kNumKernels = 5 * 2 * kVariants;
 constexpr int kVariantFixed = fa::kModeFixed, kVariantEmu = fa::kModeEmu, kVariantVarlen = fa::kModeVarlen,
               kVariantDyn = fa::kModeDyn, kVariantSplit = fa::kModeSplit, kVariantDirect = fa::kModeDirect;
-// the direct epilogue pays off while a task sees at most this many K/V blocks
-// (measured on GB300: causal 1k +8.5 %, 2k +3 %, 4k +1 %; 8k -0.3 %, mha8k -1.4 %)
-constexpr int kDirectMaxBlocks = 32;
+// The direct epilogue (O rows stored from registers) is the default for every
+// fixed-length problem: since a task's first P V waits only for the O-free
+// arrival after one stage's epilogue, it measures at least as fast as the
+// staged TMA store on long tasks too (GB300, 20 launches, two rounds: asym
+// +4.0 %, mha8k +0.2 / +1.9 %, causal 8k +1.1 %, 16k +0.9 %, mqa +0.1 / +1.2 %,
+// gqa -0.2 / +1.1 %; short causal rows +2.6 to +4.7 %).  store_mode 1 still
+// selects the staged TMA store.
 
 // variable-length batches: workspace = [task count (int) at byte 0, task counter (uint) at byte 16,
 // padding to 256 B][VarlenTask records]
@@ -571,7 +575,7 @@ static int fixed_fwd(const void* q, const void* k, const void* v, void* o, float
     }
   }
   const bool split = split_api && prob.splits > 1;
-  const bool direct = opt.store_mode == 2 || (opt.store_mode == 0 && prob.kv_blocks <= kDirectMaxBlocks);
+  const bool direct = opt.store_mode != 1;
   const int variant = split ? kVariantSplit
                             : (opt.workspace != nullptr ? kVariantDyn
                                                         : (opt.exp_emu ? kVariantEmu

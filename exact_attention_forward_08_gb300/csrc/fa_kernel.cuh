@@ -23,9 +23,9 @@
 // with dynamic task assignment; split-KV (each task one key range, partial
 // O / LSE in fp32 to a workspace, combined afterwards by the merge kernel);
 // fixed-length with a direct epilogue (each O row written from registers
-// with 16-byte stores instead of SMEM staging and TMA stores: faster when
-// tasks are short, since the correction warps then return sooner to the next
-// task; slower on long ones).
+// with 32-byte stores instead of SMEM staging and TMA stores, so the
+// correction warps return sooner to the next task; the default for
+// fixed-length problems, the staged mode on request).
 //
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DV),
 // O1 [384,384+DV).  P_s overwrites the first 64 columns of S_s as packed bf16

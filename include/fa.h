@@ -135,11 +135,9 @@ typedef struct fa_options {
                          4 on Blackwell", "Scheduling").  Calls that may overlap on different
                          streams need different buffers.  Not combinable with exp_emu; must
                          be NULL for the varlen calls (they take their own workspace). */
-  int store_mode;     /* fixed-length epilogue: 0 (default) chooses by problem (O rows written
-                         straight from registers when a task sees at most 32 K/V blocks, else
-                         staged in SMEM and written by TMA); 1 forces the TMA store; 2 forces
-                         the direct stores.  Results are identical; only the speed differs.
-                         Other values are rejected.  Ignored by the varlen, split-KV, dynamic
+  int store_mode;     /* fixed-length epilogue: 0 (default) and 2 write O rows straight from
+                         registers; 1 stages them in SMEM and writes them by TMA.  Results
+                         are identical; only the speed differs.  Other values are rejected.  Ignored by the varlen, split-KV, dynamic
                          and exp_emu paths. */
   int no_balance;     /* fixed-length calls with static assignment: 0 (default) balances the
                          work of the G persistent CTAs (task t on CTA t mod G).  Without the
