@@ -346,6 +346,19 @@ def balance_of(w, sms: int) -> str:
     return "plain order"
 
 
+def order_label(w, sms: int, no_balance: bool = False, stagger: bool = False, store_mode: int = 0,
+                dynamic: bool = False, splits: int = 1) -> str:
+    """The task-order part of the config's task_assignment text, with the
+    ablations a run selected (the plain order, the staggered exponentials, a
+    forced epilogue mode of the fixed-length kernels)."""
+    label = "plain order (ablation)" if no_balance else balance_of(w, sms)
+    if stagger and not no_balance:
+        label += "; staggered exponentials (ablation)"
+    if store_mode and not (dynamic or is_varlen(w) or splits > 1):
+        label += {1: "; staged TMA epilogue forced (ablation)", 2: "; direct epilogue forced (ablation)"}[store_mode]
+    return label
+
+
 def config_of(w, world: int, flops: float, dynamic: bool, splits: int = 1, balance: str = "") -> dict:
     assign = "dynamic (task counter)" if dynamic or is_varlen(w) else "static round-robin"
     if balance and not (dynamic or is_varlen(w) or splits > 1):
@@ -581,13 +594,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_of(w, world, flops, args.dynamic, splits,
-                            ("plain order (ablation)" if args.no_balance else
-                             (balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count) +
-                              "; staggered exponentials (ablation)") if args.stagger else
-                             balance_of(w, torch.cuda.get_device_properties(dev).multi_processor_count)) +
-                            ({1: "; staged TMA epilogue forced (ablation)",
-                              2: "; direct epilogue forced (ablation)"}.get(args.store_mode, "")
-                             if not (args.dynamic or is_varlen(w) or splits > 1) else "")),
+                            order_label(w, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                        args.no_balance, args.stagger, args.store_mode, args.dynamic, splits)),
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3)},
         "gpu_launches": args.steps * launches_per_step,

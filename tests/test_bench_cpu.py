@@ -19,3 +19,15 @@ def test_config_task_assignment():
     assert bench.config_of(w, 1, w.flops(), True, 1, "x")["task_assignment"] == "dynamic (task counter)"
     d = bench.get_workload("decode32k")
     assert bench.config_of(d, 1, d.flops(), False, 7, "x")["task_assignment"] == "static round-robin"
+
+
+def test_order_label_ablations():
+    w = bench.get_workload("causal8k")
+    assert bench.order_label(w, 152) == "heavy and light m_blocks paired on one CTA"
+    assert bench.order_label(w, 152, no_balance=True) == "plain order (ablation)"
+    assert bench.order_label(w, 152, stagger=True).endswith("; staggered exponentials (ablation)")
+    assert bench.order_label(w, 152, store_mode=1).endswith("; staged TMA epilogue forced (ablation)")
+    assert bench.order_label(w, 152, store_mode=2).endswith("; direct epilogue forced (ablation)")
+    # the epilogue modes exist only in the fixed-length static kernels
+    assert "epilogue" not in bench.order_label(w, 152, store_mode=1, dynamic=True)
+    assert "epilogue" not in bench.order_label(bench.get_workload("varlen32k"), 152, store_mode=2)
